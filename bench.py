@@ -1,0 +1,473 @@
+"""Benchmark of the 2:4 sparse multiply-accumulate hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+    sp24_compress (mask mode)  ->  sp24_meta_prepare  ->  sp24_mma (D = A_sp B + C)
+Default workload: bf16, M = N = K = 4096, keep-mask drawn per group from the six
+two-of-four patterns, A, B ~ N(0,1), C f32 ~ N(0,1), f32 output.  The metric is
+dense-equivalent TFLOP/s = 2 M N K / step time.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+Prints ONE JSON line (rank 0).  For N > 1 it runs under torch.distributed.run, one rank
+per GPU, each rank an independent problem (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import inputs  # noqa: E402
+
+METRIC = "2:4 sparse GEMM dense-equiv TFLOPS/TOPS and % of GB300 sparse tensor peak"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# NVIDIA's nominal dense peaks, used only for their ratios: fp8 / bf16 = 4.5 / 2.25 = 2,
+# and 2:4 sparse executes twice the dense-equivalent rate of dense.
+FP8_OVER_BF16 = 2.0
+SPARSE_OVER_DENSE = 2.0
+
+CONFIGS = {
+    # name: (generator, ta, mode, out dtype, description)
+    "c2": (lambda: inputs.config2(), "bf16", "mask", torch.float32,
+           "bf16 M=N=K=4096, random 2:4 mask, C f32, D f32"),
+    "c1": (lambda: inputs.config1(), "f16", "mask", torch.float32,
+           "f16 64x64x128, fixed positions-0-and-2 pattern, integers in [-4,4], C f32"),
+    "c3-e4m3": (lambda: inputs.config3("e4m3"), "e4m3", "mask", torch.float32,
+                "fp8 E4M3 M=N=K=8192, random 2:4 mask, no C, D f32"),
+    "c3-e5m2": (lambda: inputs.config3("e5m2"), "e5m2", "mask", torch.float32,
+                "fp8 E5M2 M=N=K=8192, random 2:4 mask, no C, D f32"),
+    "c5-16": (lambda: inputs.config5(16), "bf16", "magnitude", torch.bfloat16,
+              "LLM layer W 14336x4096 bf16 magnitude-pruned, X 4096x16, D bf16"),
+    "c5-128": (lambda: inputs.config5(128), "bf16", "magnitude", torch.bfloat16,
+               "LLM layer W 14336x4096 bf16 magnitude-pruned, X 4096x128, D bf16"),
+    "c5-2048": (lambda: inputs.config5(2048), "bf16", "magnitude", torch.bfloat16,
+                "LLM layer W 14336x4096 bf16 magnitude-pruned, X 4096x2048, D bf16"),
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    cs = os.path.join(ROOT, "structured_sparse_matrix_gb300", "csrc")
+    for name in sorted(os.listdir(cs)):
+        with open(os.path.join(cs, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(config: str):
+    """DRAM bytes per sp24_mma launch from the committed ncu summary of this workload,
+    or None when no summary exists or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"spmma_{config}.txt")
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_hash") != source_hash():
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.25)
+        self.text = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.text, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.text, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.text or "")) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9])
+                          if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+def oracle_sample(c: dict, mode: str, budget_s: float):
+    """Time the oracle (as it stands) on a bounded row sample of the workload: its
+    compression of those rows plus its product.  Returns (flops/s, rows, seconds,
+    threads)."""
+    import oracle
+    M, N, K, ta, tb = c["M"], c["N"], c["K"], c["ta"], c["tb"]
+    Ab = inputs.bits(c["A"])
+    Bb = inputs.bits(c["B"])
+    mask = c["mask"].numpy() if (mode == "mask" and c["mask"] is not None) else None
+    C = None if c["C"] is None else c["C"].numpy()
+
+    def run(rows):
+        t0 = time.perf_counter()
+        sub = np.ascontiguousarray(Ab[:rows])
+        v, i, _ = oracle.compress(sub, ta, mode, mask=None if mask is None else mask[:rows])
+        Csub = None if C is None else np.ascontiguousarray(C[:rows])
+        if ta in ("s8", "u8"):
+            oracle.mma_i64(v, i, Bb, Csub, ta, tb, K)
+        else:
+            oracle.mma_f64(v, i, Bb, Csub, ta, tb, K, tc="f32" if C is not None else "f32")
+        return time.perf_counter() - t0
+
+    rows = min(M, 16)
+    dt = run(rows)
+    while dt < budget_s / 4 and rows < M:
+        rows = min(M, max(rows * 2, int(rows * budget_s / max(dt, 1e-3) * 0.9)))
+        dt = run(rows)
+    return 2.0 * rows * N * K / dt, rows, dt, oracle.num_threads()
+
+
+def reference_arm(args, world, rank):
+    """The oracle as the reference arm: each step a bounded row sample of the workload."""
+    if rank != 0:
+        return
+    gen, ta, mode, out_dtype, desc = CONFIGS[args.config]
+    c = gen()
+    budget = float(os.environ.get("SP24_REF_STEP_SECONDS", "8"))
+    # size the per-step sample once, then time warmup + steps on that sample
+    _, rows, _, threads = oracle_sample(c, mode, budget)
+    import oracle
+    Ab = inputs.bits(c["A"])[:rows]
+    mask = c["mask"].numpy()[:rows] if (mode == "mask" and c["mask"] is not None) else None
+    Bb = inputs.bits(c["B"])
+    C = None if c["C"] is None else np.ascontiguousarray(c["C"].numpy()[:rows])
+
+    def step():
+        v, i, _ = oracle.compress(np.ascontiguousarray(Ab), ta, mode, mask=mask)
+        if ta in ("s8", "u8"):
+            oracle.mma_i64(v, i, Bb, C, ta, c["tb"], c["K"])
+        else:
+            oracle.mma_f64(v, i, Bb, C, ta, c["tb"], c["K"])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = 2.0 * rows * c["N"] * c["K"] / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64" if ta not in ("s8", "u8") else "int64",
+        "data": "synthetic", "config": {"workload": desc, "M": c["M"], "N": c["N"], "K": c["K"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {rows} of {c['M']} rows per step (compress + product)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def gpu_arm(args, world, rank, local):
+    import structured_sparse_matrix_gb300 as sp
+    gen, ta, mode, out_dtype, desc = CONFIGS[args.config]
+    dev = torch.device("cuda", local if world > 1 else 0)
+    base = gen()
+    M, N, K = base["M"], base["N"], base["K"]
+    flops = 2.0 * M * N * K
+    tdt = base["A"].dtype
+
+    # input sets resident in HBM, rotated so that the working set exceeds L2
+    def make_set(c):
+        s = {"A": c["A"].to(dev), "B": c["B"].to(dev),
+             "C": None if c["C"] is None else c["C"].to(dev),
+             "mask": None if c["mask"] is None else c["mask"].to(dev).to(torch.uint8)}
+        s["values"] = torch.empty((M, K // 2), dtype=tdt, device=dev)
+        s["index"] = torch.empty((M, K // 32), dtype=torch.int32, device=dev)
+        s["meta"] = torch.empty(max(sp.meta_bytes(tdt, M, K), 16), dtype=torch.uint8, device=dev)
+        s["D"] = torch.empty((M, N), dtype=out_dtype, device=dev)
+        return s
+
+    def set_bytes(s):
+        return sum(t.numel() * t.element_size() for t in s.values() if t is not None)
+
+    sets = [make_set(base)]
+    while len(sets) * set_bytes(sets[0]) < 3 * L2_BYTES and len(sets) < 16:
+        # distinct contents per set: roll the rows (cheap, same distribution)
+        c2 = dict(base)
+        shift = 37 * len(sets)
+        c2["A"] = torch.roll(base["A"], shift, 0)
+        if base["mask"] is not None:
+            c2["mask"] = torch.roll(base["mask"], shift, 0)
+        c2["B"] = torch.roll(base["B"], shift, 0)
+        sets.append(make_set(c2))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    L = sp.lib()
+    codes = sp.DTYPE_CODES
+    cs = {"ta": codes[tdt], "td": codes[out_dtype], "tc": codes[torch.float32]}
+
+    def launch(s, ev=None):
+        # the three C-ABI calls of one step, on the current stream
+        st = sp._stream(stream)
+        m = s["mask"]
+        if ev is not None:
+            ev[0].record(stream)
+        rc = L.sp24_compress(cs["ta"], M, K, sp._ptr(s["A"]), K, sp._ptr(m), K,
+                             sp.MODES[mode], sp._ptr(s["values"]), K // 2, sp._ptr(s["index"]),
+                             K // 32, sp._ptr(status), st)
+        if ev is not None:
+            ev[1].record(stream)
+        rc |= L.sp24_meta_prepare(cs["ta"], M, K, sp._ptr(s["index"]), K // 32,
+                                  sp._ptr(s["meta"]), st)
+        if ev is not None:
+            ev[2].record(stream)
+        rc |= L.sp24_mma(cs["ta"], cs["ta"], cs["tc"], cs["td"], M, N, K, sp._ptr(s["values"]),
+                         K // 2, sp._ptr(s["meta"]), sp._ptr(s["B"]), N, sp._ptr(s["C"]), N,
+                         sp._ptr(s["D"]), N, sp._ptr(status), st)
+        if ev is not None:
+            ev[3].record(stream)
+        if rc != 0:
+            raise RuntimeError(f"sp24 call failed (status bits {rc})")
+
+    for i in range(max(args.warmup, 3)):
+        launch(sets[i % len(sets)])
+    torch.cuda.synchronize(dev)
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} during warm-up")
+
+    # timed region: K steps back to back; per-kernel events on every step
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            launch(sets[i % len(sets)], evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, world)
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} in the timed region")
+    ms_step = total_ms / args.steps
+    k_compress = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    k_meta = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    k_mma = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    value = flops * world / (ms_step * 1e-3) / 1e12
+
+    # --- roofline of the dominant kernel (sp24_mma): tensor-bound sparse contraction
+    peaks, src = load_peaks()
+    dense = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    dense_peak = dense * (FP8_OVER_BF16 if ta in ("e4m3", "e5m2") else 1.0)
+    peak = dense_peak * SPARSE_OVER_DENSE
+    esz = torch.empty((), dtype=tdt).element_size()
+    osz = torch.empty((), dtype=out_dtype).element_size()
+    mma_bytes = (M * K // 2 * esz + sp.meta_bytes(tdt, M, K) + K * N * esz +
+                 (M * N * 4 if base["C"] is not None else 0) + M * N * osz)
+    achieved_tf = flops / (k_mma * 1e-3) / 1e12
+    intensity = flops / mma_bytes
+    ridge = peak * 1e12 / (peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]) * 1e9)
+    if intensity >= ridge:
+        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved_tf / peak}
+    else:
+        gbs = mma_bytes / (k_mma * 1e-3) / 1e9
+        hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm}
+    roof["traffic"] = profile_traffic(args.config)
+    roof["kernel"] = "sp24_mma (spmma_kernel)"
+    roof["algorithmic_bytes"] = mma_bytes
+    roof["peak_source"] = (f"{src}: bf16 dense {dense} TFLOP/s"
+                           f"{' x2 (fp8/bf16 nominal)' if ta in ('e4m3', 'e5m2') else ''}"
+                           " x2 (2:4 sparse / dense nominal), burst figure")
+    # compression kernel: HBM-bound, algorithmic bytes = A + mask read, values + index written
+    cbytes = M * K * esz + (M * K if mode == "mask" else 0) + M * K // 2 * esz + M * K // 8
+    kernels = {
+        "sp24_compress_us": k_compress * 1e3,
+        "sp24_compress_gbs": cbytes / (k_compress * 1e-3) / 1e9,
+        "sp24_meta_prepare_us": k_meta * 1e3,
+        "sp24_mma_us": k_mma * 1e3,
+        "sp24_mma_tflops": achieved_tf,
+    }
+
+    # --- end to end through the C ABI with host buffers: H2D inputs, 3 calls, D2H result
+    e2e = None
+    if not args.no_e2e:
+        hs = {k: base[k].pin_memory() if base[k] is not None else None for k in ("A", "B", "C")}
+        hmask = base["mask"].to(torch.uint8).pin_memory() if base["mask"] is not None else None
+        hD = torch.empty((M, N), dtype=out_dtype).pin_memory()
+        s = sets[0]
+        h2d = sum(t.numel() * t.element_size() for t in (hs["A"], hs["B"], hs["C"], hmask)
+                  if t is not None)
+        d2h = hD.numel() * hD.element_size()
+
+        def e2e_step():
+            s["A"].copy_(hs["A"], non_blocking=True)
+            if hmask is not None:
+                s["mask"].copy_(hmask, non_blocking=True)
+            s["B"].copy_(hs["B"], non_blocking=True)
+            if hs["C"] is not None:
+                s["C"].copy_(hs["C"], non_blocking=True)
+            launch(s)
+            hD.copy_(s["D"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 20))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / n_e2e, world)
+        e2e = {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    # --- CPU baseline: the oracle on this host's cores, bounded sample, rank 0 at N=1
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        fps, rows, dt, threads = oracle_sample(base, mode, float(os.environ.get(
+            "SP24_CPU_SECONDS", "12")))
+        cpu = {"value": fps / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"first {rows} of {M} rows (oracle compress + float64 product), "
+                         f"{dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": ta, "data": "synthetic",
+            "config": {"workload": desc, "name": args.config, "M": M, "N": N, "K": K,
+                       "step": f"sp24_compress({mode}) + sp24_meta_prepare + sp24_mma",
+                       "l2": f"{len(sets)} rotating input sets, "
+                             f"{len(sets) * set_bytes(sets[0]) / 2**20:.0f} MiB > L2",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "kernels": kernels,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="c2", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            reference_arm(args, world, rank)
+        else:
+            gpu_arm(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

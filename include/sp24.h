@@ -1,0 +1,183 @@
+/*
+ * sp24.h -- C ABI of libsp24: 2:4 structured-sparse multiply-accumulate D = A_sp * B + C
+ * on one GB300 (sm_103a).
+ *
+ * The operation is the one the sparse matrix-multiply builtins on these pages define:
+ *   "RDNA4 sparse WMMA builtins", "Structured sparsity (2:4 pattern)": in every
+ *     contiguous group of four elements of A along K exactly two are non-zero; A is
+ *     stored as its packed non-zeros (half the K length) plus a sparsity index that
+ *     gives, for each kept element, its 2-bit position 0-3 within the group;
+ *   same page, "Builtin reference": every builtin returns
+ *     expand(srcA, index) x srcB + srcC;
+ *   "CDNA and CDNA2 sparse MFMA builtins", "Structured sparsity (4:2 pattern)" and the
+ *     FP16 sparse kernels under "Using sparse MFMA builtins as a compute policy": the
+ *     positions-0-and-2 pattern has the index byte 0x88 (two groups of four);
+ *   "v_smfmac_f32_32x32x32_bf8_bf8", "Semantics": D = A (sparse) * B + D.
+ *
+ * Conventions for every entry point
+ *   - All matrices are row-major; a leading dimension ("ld") counts elements (words for
+ *     the index) between the starts of consecutive rows.
+ *   - Pointers named d_* or documented as "device" are device pointers on the current
+ *     CUDA device; `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   - The caller owns every buffer.  The library never allocates, frees or
+ *     synchronises; all work is enqueued on `stream` and the call returns as soon as it
+ *     is enqueued.
+ *   - A synchronous return code reports argument and launch errors; nothing is enqueued
+ *     when it is not SP24_OK.  Data-dependent conditions found on the device are OR-ed
+ *     into the caller's 32-bit status word (nullable) as SP24_DEV_* bits; read it after
+ *     the stream has synchronised.  The library never clears that word.
+ *   - There is no CPU fallback: without an sm_103 device every compute call returns
+ *     SP24_ERR_NO_DEVICE.
+ */
+#ifndef SP24_H
+#define SP24_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SP24_VERSION 1
+
+/* Element types.  F16 = IEEE binary16, BF16 = bfloat16, E4M3 = OCP FP8 E4M3 (the
+ * pages' "FP8"), E5M2 = OCP FP8 E5M2 (the pages' "BF8"), S8 / U8 = signed / unsigned
+ * 8-bit integers (the a_neg / b_neg choice of "RDNA4 dense WMMA builtins", "Common
+ * parameters"), F32 / S32 = accumulator and output types. */
+typedef enum sp24_dtype {
+    SP24_F16 = 0,
+    SP24_BF16 = 1,
+    SP24_E4M3 = 2,
+    SP24_E5M2 = 3,
+    SP24_S8 = 4,
+    SP24_U8 = 5,
+    SP24_F32 = 6,
+    SP24_S32 = 7
+} sp24_dtype;
+
+typedef enum sp24_status {
+    SP24_OK = 0,
+    SP24_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad K, ld too small   */
+    SP24_ERR_UNSUPPORTED = 2, /* element-type combination not supported             */
+    SP24_ERR_ALIGN = 3,       /* pointer or row pitch not 16-byte aligned           */
+    SP24_ERR_CUDA = 4,        /* CUDA runtime or driver error while enqueueing      */
+    SP24_ERR_TIMEOUT = 5,     /* reserved: the device reports timeouts via SP24_DEV_TIMEOUT */
+    SP24_ERR_NOT_2_4 = 6,     /* reserved: the device reports this via SP24_DEV_NOT_2_4     */
+    SP24_ERR_NO_DEVICE = 7    /* no sm_103 device is current                        */
+} sp24_status;
+
+/* How sp24_compress chooses the two kept positions of each group of four. */
+typedef enum sp24_mode {
+    SP24_MODE_EXACT = 0,     /* the non-zero elements (the pages' host compression)  */
+    SP24_MODE_MASK = 1,      /* the positions a byte mask marks (non-zero = keep)    */
+    SP24_MODE_MAGNITUDE = 2  /* the two largest |x|; equal |x| -> the lower position */
+} sp24_mode;
+
+/* Device status bits, OR-ed into the caller's int32 status word. */
+#define SP24_DEV_NOT_2_4 1 /* a group did not hold exactly two kept elements          */
+#define SP24_DEV_TIMEOUT 2 /* a bounded wait inside a kernel gave up; output invalid  */
+
+/*
+ * sp24_compress -- dense (or masked) A -> packed values + sparsity index.
+ *
+ * Walks each row of A in groups of four along K and keeps two positions p0 < p1 per
+ * group ("RDNA4 sparse WMMA builtins", "Structured sparsity (2:4 pattern)": extract the
+ * two non-zero positions and pack them consecutively; the offline pruning pass of the
+ * note under "Instantiating the kernel" is SP24_MODE_MAGNITUDE):
+ *   values[i*ldv + 2g]   = A[i*lda + 4g + p0]      (bit copy)
+ *   values[i*ldv + 2g+1] = A[i*lda + 4g + p1]
+ *   index[i*ldi + g/8]   bits 4*(g%8) .. +3  = p0 | (p1 << 2)
+ * (the nibble order is the one the CDNA example's literal 0x88 fixes for positions 0
+ * and 2: the lower position in the low two bits).
+ *
+ * t      : SP24_F16, SP24_BF16, SP24_E4M3, SP24_E5M2, SP24_S8 or SP24_U8.
+ * M, K   : rows and dense columns of A; K % 32 == 0 (one index word per 32 columns).
+ * A      : device, M x K elements of type t, leading dimension lda >= K.
+ * mask   : device, M x K bytes (ldm >= K), used only in SP24_MODE_MASK, else ignored.
+ * values : device, M x K/2 elements of type t, ldv >= K/2.
+ * index  : device, M x K/32 uint32 words, ldi >= K/32.
+ * Group rules: EXACT keeps the non-zeros (+0 and -0 are zero); with fewer than two it
+ * adds the lowest free positions, with more than two it keeps the two lowest and sets
+ * SP24_DEV_NOT_2_4.  MASK keeps the marked positions by the same rules and sets
+ * SP24_DEV_NOT_2_4 unless exactly two are marked.  MAGNITUDE never flags.
+ * Alignment: A, values and mask 16-byte aligned; lda*size(t), ldv*size(t) and ldm
+ * multiples of 16 bytes; index 4-byte aligned.  Otherwise SP24_ERR_ALIGN.
+ */
+sp24_status sp24_compress(sp24_dtype t, int64_t M, int64_t K, const void *A, int64_t lda,
+                          const uint8_t *mask, int64_t ldm, sp24_mode mode, void *values,
+                          int64_t ldv, uint32_t *index, int64_t ldi, int32_t *d_status,
+                          void *stream);
+
+/*
+ * sp24_decompress -- the inverse: A[i][4g+p] = the kept value for p in {p0, p1}, zero
+ * elsewhere (the expand() of "Builtin reference").  Same arguments, types and alignment
+ * rules as sp24_compress; A is written.
+ */
+sp24_status sp24_decompress(sp24_dtype t, int64_t M, int64_t K, const void *values,
+                            int64_t ldv, const uint32_t *index, int64_t ldi, void *A,
+                            int64_t lda, void *stream);
+
+/*
+ * sp24_meta_bytes -- size in bytes of the metadata image sp24_meta_prepare writes for
+ * an M x K (dense) operand of element type t; 0 for an unsupported t or bad size.
+ */
+size_t sp24_meta_bytes(sp24_dtype t, int64_t M, int64_t K);
+
+/*
+ * sp24_meta_prepare -- re-lay the canonical index (as sp24_compress writes it) into the
+ * image sp24_mma copies into tensor memory: for every 128-row tile of A, every K step of
+ * the kernel (128 dense K for 16-bit types, 256 for 8-bit types) and each of the step's
+ * four MMAs, one [128][16-byte] block.  Rows are padded to a multiple of 128 and K to
+ * the K step; pad groups get the valid pattern {0,1} and their values are zero, so they
+ * add nothing.  The image is a format private to sp24_mma (sp24_meta_bytes() gives its
+ * size); the canonical index stays the interchange format.
+ * index : device, M x K/32 words, ldi >= K/32, 4-byte aligned.
+ * meta  : device, sp24_meta_bytes(t, M, K) bytes, 16-byte aligned.
+ */
+sp24_status sp24_meta_prepare(sp24_dtype t, int64_t M, int64_t K, const uint32_t *index,
+                              int64_t ldi, void *meta, void *stream);
+
+/*
+ * sp24_mma -- D = expand(values, index) * B + C, one launch of the tcgen05 sparse GEMM.
+ *
+ * ta, tb, tc, td supported combinations (anything else: SP24_ERR_UNSUPPORTED):
+ *   (F16, F16) and (BF16, BF16)     -> f32 accumulate, tc in {F32, none}, td in {F32, BF16}
+ *   (E4M3, E4M3) and (E5M2, E5M2)   -> f32 accumulate, tc in {F32, none}, td in {F32, BF16}
+ *   (S8, S8) and (U8, S8)           -> exact integer accumulate, tc in {S32, none}, td = S32
+ *                                      (two's-complement wrap, no clamp)
+ * "none" for tc means C == NULL (treated as zero); tc is then ignored.
+ * M, N, K : D is M x N; K is the dense depth, K % 32 == 0 (K % 64 == 0 for 8-bit types).
+ * values  : device, M x K/2 of ta (ldv >= K/2), from sp24_compress.
+ * meta    : device, the image sp24_meta_prepare wrote for (ta, M, K).
+ * B       : device, K x N of tb, row-major (ldb >= N).
+ * C       : device or NULL, M x N of tc (ldc >= N).      D : device, M x N of td (ldd >= N).
+ * Accumulation: floats in f32 on the tensor cores; D (BF16) is the f32 result rounded
+ * to nearest-even; integer inputs are exact in 32-bit two's complement.
+ * Alignment: values, B, C, D 16-byte aligned, every row pitch a multiple of 16 bytes.
+ * Device status: SP24_DEV_TIMEOUT if a pipeline wait gave up (D is then invalid).
+ */
+sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
+                     int64_t M, int64_t N, int64_t K, const void *values, int64_t ldv,
+                     const void *meta, const void *B, int64_t ldb, const void *C,
+                     int64_t ldc, void *D, int64_t ldd, int32_t *d_status, void *stream);
+
+/*
+ * sp24_diag_wait_timeout -- self-test of the bounded waits every kernel uses.  Launches
+ * one thread that waits on a barrier nothing ever arrives at; after limit_ns nanoseconds
+ * the wait gives up and SP24_DEV_TIMEOUT is OR-ed into *d_status (device, 4 bytes).  The
+ * context stays usable.  It exists so that the give-up path can be tested without a
+ * faulting or hanging GPU.
+ */
+sp24_status sp24_diag_wait_timeout(int32_t *d_status, uint64_t limit_ns, void *stream);
+
+/* Static description of a status code (never NULL). */
+const char *sp24_status_string(sp24_status s);
+
+/* SP24_VERSION of the loaded library. */
+int sp24_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SP24_H */

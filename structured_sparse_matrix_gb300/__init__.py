@@ -1,0 +1,183 @@
+"""structured_sparse_matrix_gb300 -- 2:4 structured-sparse multiply-accumulate on GB300.
+
+A thin ctypes binding over the C ABI of ``libsp24.so`` (``include/sp24.h``).  Every step
+of the computation runs in the library's sm_103a kernels; this module only allocates the
+output tensors with PyTorch, passes raw device pointers and the current CUDA stream, and
+turns non-OK status codes into exceptions.  There is no CPU fallback: if the library is
+missing or no sm_103 device is current, calls raise.
+
+    values, index = compress(A, mode="mask", mask=keep)     # A: M x K on cuda
+    meta = meta_prepare(index, A.dtype, M, K)
+    D = mma(values, meta, B, C, out_dtype=torch.float32)     # D = A_sp @ B + C
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = ["lib", "compress", "decompress", "meta_bytes", "meta_prepare", "mma",
+           "SparseMatrix", "Sp24Error", "DEV_NOT_2_4", "DEV_TIMEOUT", "DTYPE_CODES"]
+
+DTYPE_CODES = {
+    torch.float16: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2, torch.float8_e5m2: 3,
+    torch.int8: 4, torch.uint8: 5, torch.float32: 6, torch.int32: 7,
+}
+MODES = {"exact": 0, "mask": 1, "magnitude": 2}
+DEV_NOT_2_4 = 1
+DEV_TIMEOUT = 2
+
+# every symbol include/sp24.h declares
+EXPORTS = ("sp24_compress", "sp24_decompress", "sp24_meta_bytes", "sp24_meta_prepare",
+           "sp24_mma", "sp24_diag_wait_timeout", "sp24_status_string", "sp24_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Sp24Error(RuntimeError):
+    def __init__(self, fn: str, code: int, text: str):
+        super().__init__(f"{fn} failed: {text} (status {code})")
+        self.code = code
+
+
+def lib():
+    """Load libsp24.so (building it in-tree with nvcc if it is absent or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not _build.up_to_date():
+                path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError("libsp24.so is missing and could not be built")
+            L = ctypes.CDLL(path)
+            i64, p, i32, u64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
+            L.sp24_compress.restype = i32
+            L.sp24_compress.argtypes = [i32, i64, i64, p, i64, p, i64, i32, p, i64, p, i64, p, p]
+            L.sp24_decompress.restype = i32
+            L.sp24_decompress.argtypes = [i32, i64, i64, p, i64, p, i64, p, i64, p]
+            L.sp24_meta_bytes.restype = ctypes.c_size_t
+            L.sp24_meta_bytes.argtypes = [i32, i64, i64]
+            L.sp24_meta_prepare.restype = i32
+            L.sp24_meta_prepare.argtypes = [i32, i64, i64, p, i64, p, p]
+            L.sp24_mma.restype = i32
+            L.sp24_mma.argtypes = [i32, i32, i32, i32, i64, i64, i64, p, i64, p, p, i64, p, i64,
+                                   p, i64, p, p]
+            L.sp24_diag_wait_timeout.restype = i32
+            L.sp24_diag_wait_timeout.argtypes = [p, u64, p]
+            L.sp24_status_string.restype = ctypes.c_char_p
+            L.sp24_status_string.argtypes = [i32]
+            L.sp24_version.restype = i32
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise Sp24Error(fn, code, lib().sp24_status_string(code).decode())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _code(dtype):
+    if dtype not in DTYPE_CODES:
+        raise TypeError(f"unsupported element type {dtype}")
+    return DTYPE_CODES[dtype]
+
+
+def _ld(t):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D row-major tensor (unit column stride)")
+    return t.stride(0)
+
+
+def compress(A: torch.Tensor, mode: str = "exact", mask: torch.Tensor | None = None,
+             status: torch.Tensor | None = None, stream=None):
+    """Dense M x K (2:4 along K) -> (values M x K/2, index M x K/32 int32 words)."""
+    M, K = A.shape
+    values = torch.empty((M, K // 2), dtype=A.dtype, device=A.device)
+    index = torch.empty((M, K // 32), dtype=torch.int32, device=A.device)
+    m = None
+    ldm = K
+    if mode == "mask":
+        if mask is None:
+            raise ValueError("mask mode needs a mask")
+        m = mask.to(torch.uint8) if mask.dtype != torch.uint8 else mask
+        ldm = _ld(m)
+    _check("sp24_compress", lib().sp24_compress(
+        _code(A.dtype), M, K, _ptr(A), _ld(A), _ptr(m), ldm, MODES[mode], _ptr(values),
+        _ld(values), _ptr(index), _ld(index), _ptr(status), _stream(stream)))
+    return values, index
+
+
+def decompress(values: torch.Tensor, index: torch.Tensor, K: int, stream=None) -> torch.Tensor:
+    M = values.shape[0]
+    A = torch.empty((M, K), dtype=values.dtype, device=values.device)
+    _check("sp24_decompress", lib().sp24_decompress(
+        _code(values.dtype), M, K, _ptr(values), _ld(values), _ptr(index), _ld(index), _ptr(A),
+        _ld(A), _stream(stream)))
+    return A
+
+
+def meta_bytes(dtype, M: int, K: int) -> int:
+    return int(lib().sp24_meta_bytes(_code(dtype), M, K))
+
+
+def meta_prepare(index: torch.Tensor, dtype, M: int, K: int, stream=None) -> torch.Tensor:
+    nbytes = meta_bytes(dtype, M, K)
+    meta = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=index.device)
+    _check("sp24_meta_prepare", lib().sp24_meta_prepare(
+        _code(dtype), M, K, _ptr(index), _ld(index), _ptr(meta), _stream(stream)))
+    return meta
+
+
+def mma(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
+        out_dtype=torch.float32, out: torch.Tensor | None = None,
+        status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """D = expand(values, meta) @ B + C  (values M x K/2, B K x N, C/D M x N)."""
+    M = values.shape[0]
+    K, N = B.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=B.device)
+    tc = _code(C.dtype) if C is not None else _code(torch.float32)
+    _check("sp24_mma", lib().sp24_mma(
+        _code(values.dtype), _code(B.dtype), tc, _code(out.dtype), M, N, K,
+        _ptr(values), _ld(values), _ptr(meta), _ptr(B), _ld(B), _ptr(C),
+        _ld(C) if C is not None else N, _ptr(out), _ld(out), _ptr(status), _stream(stream)))
+    return out
+
+
+class SparseMatrix:
+    """A compressed 2:4 operand: values + canonical index + the GEMM's metadata image."""
+
+    def __init__(self, values, index, meta, K):
+        self.values, self.index, self.meta, self.K = values, index, meta, K
+
+    @property
+    def shape(self):
+        return (self.values.shape[0], self.K)
+
+    @classmethod
+    def from_dense(cls, A, mode="exact", mask=None, status=None, stream=None):
+        values, index = compress(A, mode=mode, mask=mask, status=status, stream=stream)
+        meta = meta_prepare(index, A.dtype, A.shape[0], A.shape[1], stream=stream)
+        return cls(values, index, meta, A.shape[1])
+
+    def to_dense(self, stream=None):
+        return decompress(self.values, self.index, self.K, stream=stream)
+
+    def matmul(self, B, C=None, out_dtype=torch.float32, status=None, stream=None):
+        return mma(self.values, self.meta, B, C, out_dtype=out_dtype, status=status,
+                   stream=stream)

@@ -1,0 +1,207 @@
+// api.cu -- the extern "C" entry points of libsp24 (declared in include/sp24.h):
+// argument validation, device checks and stream-ordered launches.  No entry point
+// allocates, frees or synchronises.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/sp24.h"
+#include "sp24_device.cuh"
+#include "sp24_internal.h"
+
+namespace sp24 {
+
+bool current_device(int* num_sms) {
+  static std::mutex mu;
+  static int cached_sms[64];
+  static signed char cached_ok[64];  // 0 unknown, 1 sm_103, -1 other
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return false;
+  }
+  if (dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached_ok[dev] == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    cached_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    cached_sms[dev] = sms;
+  }
+  if (cached_ok[dev] != 1) return false;
+  *num_sms = cached_sms[dev];
+  return true;
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// bounded-wait self-test: one thread waits on an mbarrier that nothing arrives at
+__global__ void wait_timeout_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  mbar_init(&bar, 1);
+  abort_flag = 0;
+  fence_mbar_init();
+  if (!mbar_wait(&bar, 0, &abort_flag, limit_ns)) atomicOr(status, kDevTimeout);
+}
+
+}  // namespace
+}  // namespace sp24
+
+using namespace sp24;
+
+extern "C" {
+
+int sp24_version(void) { return SP24_VERSION; }
+
+const char* sp24_status_string(sp24_status s) {
+  switch (s) {
+    case SP24_OK: return "ok";
+    case SP24_ERR_INVALID_ARG: return "invalid argument";
+    case SP24_ERR_UNSUPPORTED: return "unsupported element-type combination";
+    case SP24_ERR_ALIGN: return "pointer or row pitch not 16-byte aligned";
+    case SP24_ERR_CUDA: return "CUDA error while enqueueing";
+    case SP24_ERR_TIMEOUT: return "device wait timed out";
+    case SP24_ERR_NOT_2_4: return "input is not 2:4 sparse";
+    case SP24_ERR_NO_DEVICE: return "no sm_103 device is current";
+    default: return "unknown status";
+  }
+}
+
+sp24_status sp24_compress(sp24_dtype t, int64_t M, int64_t K, const void* A, int64_t lda,
+                          const uint8_t* mask, int64_t ldm, sp24_mode mode, void* values,
+                          int64_t ldv, uint32_t* index, int64_t ldi, int32_t* d_status,
+                          void* stream) {
+  if (!is_ab_type(t)) return SP24_ERR_UNSUPPORTED;
+  if (mode < SP24_MODE_EXACT || mode > SP24_MODE_MAGNITUDE) return SP24_ERR_INVALID_ARG;
+  if (M < 0 || K < 0 || (K % 32) != 0) return SP24_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return SP24_OK;
+  if (!A || !values || !index || (mode == SP24_MODE_MASK && !mask)) return SP24_ERR_INVALID_ARG;
+  if (lda < K || ldv < K / 2 || ldi < K / 32 || (mode == SP24_MODE_MASK && ldm < K))
+    return SP24_ERR_INVALID_ARG;
+  const int esz = dtype_bytes(t);
+  if (!aligned16(A) || !aligned16(values) || (reinterpret_cast<uintptr_t>(index) & 3u) ||
+      (lda * esz) % 16 || (ldv * esz) % 16)
+    return SP24_ERR_ALIGN;
+  if (mode == SP24_MODE_MASK && (!aligned16(mask) || ldm % 16)) return SP24_ERR_ALIGN;
+  int sms = 0;
+  if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
+  CompressArgs a;
+  a.A = static_cast<const uint8_t*>(A);
+  a.lda_bytes = lda * esz;
+  a.mask = mask;
+  a.ldm = ldm;
+  a.values = static_cast<uint8_t*>(values);
+  a.ldv_bytes = ldv * esz;
+  a.index = index;
+  a.ldi = ldi;
+  a.M = M;
+  a.K = K;
+  a.status = d_status;
+  if (launch_compress(a, t, mode, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SP24_ERR_CUDA;
+  return SP24_OK;
+}
+
+sp24_status sp24_decompress(sp24_dtype t, int64_t M, int64_t K, const void* values,
+                            int64_t ldv, const uint32_t* index, int64_t ldi, void* A,
+                            int64_t lda, void* stream) {
+  if (!is_ab_type(t)) return SP24_ERR_UNSUPPORTED;
+  if (M < 0 || K < 0 || (K % 32) != 0) return SP24_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return SP24_OK;
+  if (!A || !values || !index) return SP24_ERR_INVALID_ARG;
+  if (lda < K || ldv < K / 2 || ldi < K / 32) return SP24_ERR_INVALID_ARG;
+  const int esz = dtype_bytes(t);
+  if (!aligned16(A) || !aligned16(values) || (reinterpret_cast<uintptr_t>(index) & 3u) ||
+      (lda * esz) % 16 || (ldv * esz) % 16)
+    return SP24_ERR_ALIGN;
+  int sms = 0;
+  if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
+  DecompressArgs a;
+  a.values = static_cast<const uint8_t*>(values);
+  a.ldv_bytes = ldv * esz;
+  a.index = index;
+  a.ldi = ldi;
+  a.A = static_cast<uint8_t*>(A);
+  a.lda_bytes = lda * esz;
+  a.M = M;
+  a.K = K;
+  if (launch_decompress(a, t, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SP24_ERR_CUDA;
+  return SP24_OK;
+}
+
+size_t sp24_meta_bytes(sp24_dtype t, int64_t M, int64_t K) {
+  if (!is_ab_type(t) || M < 0 || K < 0 || (K % 32) != 0) return 0;
+  const int64_t mtiles = (M + kBM - 1) / kBM;
+  const int64_t ksteps = (K + stage_k(t) - 1) / stage_k(t);
+  return size_t(mtiles * ksteps * meta_stage_bytes(t));
+}
+
+sp24_status sp24_meta_prepare(sp24_dtype t, int64_t M, int64_t K, const uint32_t* index,
+                              int64_t ldi, void* meta, void* stream) {
+  if (!is_ab_type(t)) return SP24_ERR_UNSUPPORTED;
+  if (M < 0 || K < 0 || (K % 32) != 0) return SP24_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return SP24_OK;
+  if (!index || !meta || ldi < K / 32) return SP24_ERR_INVALID_ARG;
+  if (!aligned16(meta) || (reinterpret_cast<uintptr_t>(index) & 3u)) return SP24_ERR_ALIGN;
+  int sms = 0;
+  if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
+  MetaArgs a;
+  a.index = index;
+  a.ldi = ldi;
+  a.meta = static_cast<uint32_t*>(meta);
+  a.M = M;
+  a.K = K;
+  a.mtiles = (M + kBM - 1) / kBM;
+  a.ksteps = (K + stage_k(t) - 1) / stage_k(t);
+  if (launch_meta_prepare(a, t, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SP24_ERR_CUDA;
+  return SP24_OK;
+}
+
+sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td, int64_t M,
+                     int64_t N, int64_t K, const void* values, int64_t ldv, const void* meta,
+                     const void* B, int64_t ldb, const void* C, int64_t ldc, void* D,
+                     int64_t ldd, int32_t* d_status, void* stream) {
+  const bool f16ish = (ta == SP24_F16 || ta == SP24_BF16);
+  const bool f8 = (ta == SP24_E4M3 || ta == SP24_E5M2);
+  if (!(f16ish || f8) || tb != ta) return SP24_ERR_UNSUPPORTED;
+  if (C != nullptr && tc != SP24_F32) return SP24_ERR_UNSUPPORTED;
+  if (td != SP24_F32 && td != SP24_BF16) return SP24_ERR_UNSUPPORTED;
+  if (M < 0 || N < 0 || K < 0 || (K % 32) != 0) return SP24_ERR_INVALID_ARG;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return SP24_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return SP24_OK;
+  if (!D || (K > 0 && (!values || !meta || !B))) return SP24_ERR_INVALID_ARG;
+  if (ldd < N || (C && ldc < N) || (K > 0 && (ldv < K / 2 || ldb < N))) return SP24_ERR_INVALID_ARG;
+  const int esz = dtype_bytes(ta);
+  const int dsz = dtype_bytes(td);
+  if (!aligned16(D) || (ldd * dsz) % 16) return SP24_ERR_ALIGN;
+  if (C && (!aligned16(C) || (ldc * 4) % 16)) return SP24_ERR_ALIGN;
+  if (K > 0 && (!aligned16(values) || !aligned16(meta) || !aligned16(B) || (ldv * esz) % 16 ||
+                (ldb * esz) % 16))
+    return SP24_ERR_ALIGN;
+  int sms = 0;
+  if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
+  const int rc = launch_spmma(ta, tb, tc, td, M, N, K, values, ldv, meta, B, ldb, C, ldc, D, ldd,
+                              d_status, sms, static_cast<cudaStream_t>(stream));
+  return static_cast<sp24_status>(rc);
+}
+
+sp24_status sp24_diag_wait_timeout(int32_t* d_status, uint64_t limit_ns, void* stream) {
+  if (!d_status) return SP24_ERR_INVALID_ARG;
+  int sms = 0;
+  if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
+  wait_timeout_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(d_status, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? SP24_OK : SP24_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// meta.cu -- re-layout of the canonical sparsity index into the image that the sparse
+// GEMM copies, MMA by MMA, from shared memory into tensor memory.
+//
+// Canonical index (as sp24_compress writes it): M x K/32 words, group g of row i in bits
+// 4(g%8)..+3 of word g/8, nibble = p0 | p1 << 2.
+//
+// tcgen05.mma.sp reads the metadata of A from tensor memory (TMEM).  The GEMM gives each
+// MMA its own column-aligned TMEM slot and fills it with one tcgen05.cp.128x128b from a
+// [128 lanes][4 words] block in shared memory.  The image therefore holds, for every
+// 128-row tile, every pipeline stage of the GEMM and each of the stage's 4 MMAs, one
+// such block; the MMA's words come first in each lane's 16 bytes, the rest is padding.
+//
+// Word placement inside a block (measured on sm_103a with tcgen05.mma.sp, M = 128):
+//   kind::f16 (16-bit types, 32 dense K per MMA, one word per lane): in each 16-row
+//     band b, lane 16b+l holds the halves (h = l/8) of two rows' canonical words:
+//       word = ((w[16b+l%8] >> 16h) & 0xffff) | ((w[16b+l%8+8] >> 16h) & 0xffff) << 16
+//     so nibble q of lane 16b+l is group (q%4)+4h of row 16b+l%8+8(q/4).
+//   kind::f8f6f4 (8-bit types, 64 dense K per MMA, two words per lane): lane = row,
+//     words 0 and 1 = the row's two canonical words of that K range.
+// Rows beyond M, words beyond K/32 and the padding words hold 0x44444444 (pattern {0,1}
+// in every group); the matching values are zero, so they add nothing.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sp24_internal.h"
+
+namespace sp24 {
+namespace {
+
+constexpr uint32_t kPadWord = 0x44444444u;
+
+__device__ __forceinline__ uint32_t canon(const MetaArgs& a, int64_t row, int64_t w) {
+  if (row >= a.M || w >= a.K / 32) return kPadWord;
+  return a.index[row * a.ldi + w];
+}
+
+// one thread per image word; block = [mma j][128 lanes][4 words]
+template <bool kEightBit>
+__global__ void __launch_bounds__(256) meta_kernel(MetaArgs a) {
+  const int64_t total = a.mtiles * a.ksteps * kMmasPerStage * 128 * 4;
+  for (int64_t o = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; o < total;
+       o += int64_t(gridDim.x) * blockDim.x) {
+    const int q = int(o & 3);                 // word within the lane's 16 bytes
+    const int lane = int((o >> 2) & 127);     // TMEM lane
+    const int j = int((o >> 9) & 3);          // MMA within the stage
+    const int64_t blk = o >> 11;              // (mtile, kstep)
+    const int64_t mt = blk / a.ksteps, ks = blk % a.ksteps;
+    uint32_t word = kPadWord;
+    if constexpr (kEightBit) {
+      if (q < 2) word = canon(a, mt * 128 + lane, ks * 8 + j * 2 + q);
+    } else {
+      if (q == 0) {
+        const int64_t w = ks * 4 + j;         // canonical word (32 dense K)
+        const int band = lane >> 4, l = lane & 15;
+        const int64_t rA = mt * 128 + band * 16 + (l & 7);
+        const int h = l >> 3;
+        const uint32_t lo = (canon(a, rA, w) >> (16 * h)) & 0xFFFFu;
+        const uint32_t hi = (canon(a, rA + 8, w) >> (16 * h)) & 0xFFFFu;
+        word = lo | (hi << 16);
+      }
+    }
+    a.meta[o] = word;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_meta_prepare(const MetaArgs& a, int dtype, int num_sms, cudaStream_t s) {
+  const int64_t words = a.mtiles * a.ksteps * meta_stage_bytes(dtype) / 4;
+  int64_t want = (words + 255) / 256;
+  int64_t cap = int64_t(num_sms) * 8;
+  const int grid = int(want < cap ? (want > 0 ? want : 1) : cap);
+  if (dtype_bytes(dtype) == 2)
+    meta_kernel<false><<<grid, 256, 0, s>>>(a);
+  else
+    meta_kernel<true><<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace sp24

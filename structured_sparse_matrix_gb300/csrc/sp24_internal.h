@@ -1,0 +1,71 @@
+// sp24_internal.h -- host-side declarations shared by the translation units of libsp24.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sp24 {
+
+// element codes: identical to sp24_dtype in include/sp24.h
+enum : int { kF16 = 0, kBF16 = 1, kE4M3 = 2, kE5M2 = 3, kS8 = 4, kU8 = 5, kF32 = 6, kS32 = 7 };
+
+inline int dtype_bytes(int t) {
+  switch (t) {
+    case kF16: case kBF16: return 2;
+    case kE4M3: case kE5M2: case kS8: case kU8: return 1;
+    case kF32: case kS32: return 4;
+    default: return 0;
+  }
+}
+inline bool is_ab_type(int t) { return t >= kF16 && t <= kU8; }
+
+// ---- sparse-GEMM K-step geometry (one pipeline stage) shared by meta.cu and spmma.cu
+// 16-bit operands: 128 dense K per stage = 4 MMAs of K=32, metadata one TMEM column
+// per MMA; 8-bit operands: 256 dense K per stage = 4 MMAs of K=64, two columns per MMA.
+// In both cases a stage of compressed A is 128 rows x 128 bytes.  Each MMA's metadata
+// is staged as its own [128 lanes][4 words] block (its words first, the rest padding),
+// copied by one tcgen05.cp.128x128b into a column-aligned TMEM slot.
+constexpr int kBM = 128;
+constexpr int kMmasPerStage = 4;
+constexpr int kMetaBlockBytes = kBM * 16;  // one [128][4-word] block
+inline int stage_k(int t) { return dtype_bytes(t) == 2 ? 128 : 256; }
+inline int64_t meta_stage_bytes(int) { return int64_t(kMmasPerStage) * kMetaBlockBytes; }
+
+struct CompressArgs {
+  const uint8_t* A; int64_t lda_bytes;
+  const uint8_t* mask; int64_t ldm;
+  uint8_t* values; int64_t ldv_bytes;
+  uint32_t* index; int64_t ldi;
+  int64_t M, K;
+  int32_t* status;
+};
+
+struct DecompressArgs {
+  const uint8_t* values; int64_t ldv_bytes;
+  const uint32_t* index; int64_t ldi;
+  uint8_t* A; int64_t lda_bytes;
+  int64_t M, K;
+};
+
+struct MetaArgs {
+  const uint32_t* index; int64_t ldi;
+  uint32_t* meta;
+  int64_t M, K;       // dense sizes
+  int64_t mtiles, ksteps;
+};
+
+cudaError_t launch_compress(const CompressArgs& a, int dtype, int mode, int num_sms, cudaStream_t s);
+cudaError_t launch_decompress(const DecompressArgs& a, int dtype, int num_sms, cudaStream_t s);
+cudaError_t launch_meta_prepare(const MetaArgs& a, int dtype, int num_sms, cudaStream_t s);
+
+// returns 0 on success, else an sp24_status value
+int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K,
+                 const void* values, int64_t ldv, const void* meta, const void* B, int64_t ldb,
+                 const void* C, int64_t ldc, void* D, int64_t ldd, int32_t* status,
+                 int num_sms, cudaStream_t s);
+
+// device properties of the current device, cached; returns false if not sm_103
+bool current_device(int* num_sms);
+
+}  // namespace sp24

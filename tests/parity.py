@@ -1,0 +1,94 @@
+"""Shared helpers for the GPU-vs-oracle parity tests (CUDA path through the C ABI on one
+side, the CPU oracle on the other, fed the same seeded inputs)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import inputs
+import oracle
+import structured_sparse_matrix_gb300 as sp
+
+REL, ABS = 1e-4, 1e-6  # float acceptance: |D - D_ref| <= REL * sum_k |a b| + ABS
+
+
+def dev(t):
+    return None if t is None else t.cuda()
+
+
+def index_np(index_t: torch.Tensor) -> np.ndarray:
+    return index_t.cpu().numpy().view(np.uint32)
+
+
+def sample_rows(M: int) -> np.ndarray:
+    """Rows 0..127, the last 128 and every 61st row: covers first/last tiles and a
+    spread of interior tiles and lanes."""
+    rows = set(range(min(128, M))) | set(range(max(0, M - 128), M)) | set(range(0, M, 61))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    e = np.maximum(e, -126)
+    return np.exp2(e - 7)
+
+
+def check_float(D: np.ndarray, Dref: np.ndarray, S: np.ndarray, out_bf16: bool, what: str):
+    """Float parity: f32 output within REL*S + ABS; bf16 output compared with the
+    round-to-nearest-even bf16 of the exact result, plus one bf16 ulp (the f32
+    accumulation error may flip a rounding)."""
+    D = np.asarray(D, dtype=np.float64)
+    if out_bf16:
+        ref = oracle.decode("bf16", oracle.round_bf16(Dref))
+        tol = REL * S + ABS + bf16_ulp(ref)
+    else:
+        ref = Dref
+        tol = REL * S + ABS
+    err = np.abs(D - ref)
+    bad = ~(err <= tol)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; first at "
+            f"{tuple(int(v) for v in i)}: got {D[tuple(i)]!r}, want {ref[tuple(i)]!r}, "
+            f"tol {tol[tuple(i)]!r}")
+
+
+def gpu_compress(c: dict, mode: str):
+    A = dev(c["A"])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mask = dev(c["mask"]) if mode == "mask" else None
+    values, index = sp.compress(A, mode=mode, mask=mask, status=status)
+    return values, index, status
+
+
+def run_case(c: dict, mode: str = "mask", out_dtype=torch.float32, rows=None, check=True):
+    """Compress + meta_prepare + mma on the GPU, oracle on the CPU, compare."""
+    ta, tb = c["ta"], c["tb"]
+    M, N, K = c["M"], c["N"], c["K"]
+    values, index, status = gpu_compress(c, mode)
+    meta = sp.meta_prepare(index, c["A"].dtype, M, K)
+    B = dev(c["B"])
+    C = dev(c["C"])
+    D = sp.mma(values, meta, B, C, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    # oracle: its own compression of the same dense input, then its own product
+    mask_np = c["mask"].numpy() if mode == "mask" else None
+    v_ref, i_ref, _ = oracle.compress(inputs.bits(c["A"]), ta, mode, mask=mask_np)
+    assert np.array_equal(index_np(index), i_ref), "index differs from the oracle"
+    assert np.array_equal(inputs.bits(values.cpu()), v_ref), "values differ from the oracle"
+    if rows is None:
+        rows = np.arange(M)
+    Dg = D.float().cpu().numpy()[rows] if out_dtype != torch.int32 else D.cpu().numpy()[rows]
+    C_np = None if c["C"] is None else c["C"].numpy()
+    if ta in ("s8", "u8"):
+        Dref = oracle.mma_i64(v_ref, i_ref, inputs.bits(c["B"]), C_np, ta, tb, K, rows=rows)
+        if check:
+            assert np.array_equal(Dg.astype(np.int64), oracle.wrap_i32(Dref).astype(np.int64))
+        return Dg, Dref, None
+    Dref, S = oracle.mma_f64(v_ref, i_ref, inputs.bits(c["B"]), C_np, ta, tb, K, rows=rows)
+    if check:
+        check_float(Dg, Dref, S, out_dtype == torch.bfloat16, f"{ta} {M}x{N}x{K}")
+    return Dg, Dref, S

@@ -1,0 +1,137 @@
+"""The sparse GEMM (tcgen05.mma.sp) against the oracle: small ragged cases span several
+tiles and every tail; the workload sizes run at full size in the bench's launch
+configuration and are compared on sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+import oracle
+import structured_sparse_matrix_gb300 as sp
+from parity import check_float, dev, run_case, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+FLOAT_TYPES = ["f16", "bf16", "e4m3", "e5m2"]
+
+
+def test_config1_bit_exact():
+    # integer-valued f16 inputs: every partial sum is a small integer, so D is exact
+    c = inputs.config1()
+    Dg, Dref, _ = run_case(c, mode="mask", check=False)
+    assert np.array_equal(Dg.astype(np.float64), Dref)
+
+
+@pytest.mark.parametrize("ta", FLOAT_TYPES)
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 192, 320), (257, 64, 96),
+                                   (64, 304, 512), (1, 16, 32), (384, 400, 1056)])
+def test_small_ragged_shapes(ta, M, N, K):
+    c = inputs.case(ta, ta, M, N, K, seed=M + N + K, tc="f32")
+    run_case(c, mode="mask")
+
+
+@pytest.mark.parametrize("ta", FLOAT_TYPES)
+def test_no_C_and_bf16_output(ta):
+    c = inputs.case(ta, ta, 300, 272, 384, seed=12, tc=None)
+    run_case(c, mode="mask", out_dtype=torch.float32)
+    run_case(c, mode="mask", out_dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("ta", ["f16", "e4m3"])
+def test_every_single_pattern(ta):
+    # one pattern everywhere, for each of the six: exercises every metadata nibble value
+    for pat in inputs.PATTERNS:
+        M, N, K = 128, 128, 256
+        g = inputs.gen(100)
+        A = inputs.values((M, K), ta, "normal", g)
+        m = inputs.keep_mask(M, K, None, fixed=pat)
+        c = {"A": inputs.apply_mask(A, m), "mask": m,
+             "B": inputs.values((K, N), ta, "normal", inputs.gen(101)),
+             "C": None, "ta": ta, "tb": ta, "tc": None, "M": M, "N": N, "K": K}
+        run_case(c, mode="mask")
+
+
+@pytest.mark.parametrize("ta", ["bf16", "e5m2"])
+def test_padded_leading_dimensions_and_ragged_N(ta):
+    # N = 300 is not a legal row pitch for 8-bit B; padded buffers (ld = 320) carry it
+    M, N, K, ld = 160, 300, 256, 320
+    c = inputs.case(ta, ta, M, N, K, seed=40, tc="f32")
+    Bp = torch.zeros((K, ld), dtype=c["B"].dtype)
+    Bp[:, :N] = c["B"]
+    Cp = torch.zeros((M, ld), dtype=torch.float32)
+    Cp[:, :N] = c["C"]
+    Dp = torch.full((M, ld), 7.0, dtype=torch.float32, device="cuda")
+    values, index = sp.compress(dev(c["A"]), mode="mask", mask=dev(c["mask"]))
+    meta = sp.meta_prepare(index, c["A"].dtype, M, K)
+    sp.mma(values, meta, Bp.cuda()[:, :N], Cp.cuda()[:, :N], out=Dp[:, :N])
+    torch.cuda.synchronize()
+    v, i, _ = oracle.compress(inputs.bits(c["A"]), ta, "mask", mask=c["mask"].numpy())
+    R, S = oracle.mma_f64(v, i, inputs.bits(c["B"]), c["C"].numpy(), ta, ta, K)
+    Dh = Dp.cpu().numpy()
+    check_float(Dh[:, :N], R, S, False, "padded")
+    assert np.all(Dh[:, N:] == 7.0), "wrote past N"
+
+
+def test_identity_B_returns_A_plus_C():
+    # the pages' verification idiom: with B = I the product is A itself
+    M, K = 256, 256
+    c = inputs.case("bf16", "bf16", M, K, K, seed=31, tc="f32")
+    c["B"] = torch.eye(K, dtype=torch.bfloat16)
+    values, index = sp.compress(dev(c["A"]), mode="mask", mask=dev(c["mask"]))
+    meta = sp.meta_prepare(index, torch.bfloat16, M, K)
+    D = sp.mma(values, meta, dev(c["B"]), dev(c["C"]))
+    torch.cuda.synchronize()
+    want = (c["A"].float() + c["C"]).numpy()
+    assert np.array_equal(D.cpu().numpy(), want)
+
+
+def test_K_zero_gives_C():
+    M, N = 130, 72
+    C = torch.randn(M, N, generator=inputs.gen(2)).cuda()
+    B = torch.empty((0, N), dtype=torch.float16, device="cuda")
+    values = torch.empty((M, 0), dtype=torch.float16, device="cuda")
+    meta = torch.empty(16, dtype=torch.uint8, device="cuda")
+    D = sp.mma(values, meta, B, C)
+    torch.cuda.synchronize()
+    assert torch.equal(D, C)
+
+
+def test_matmul_through_sparse_matrix_object():
+    c = inputs.case("f16", "f16", 192, 64, 128, seed=3, dist="int4", tc="f32", c_dist="int4")
+    W = sp.SparseMatrix.from_dense(dev(c["A"]), mode="mask", mask=dev(c["mask"]))
+    D = W.matmul(dev(c["B"]), dev(c["C"]))
+    back = W.to_dense()
+    torch.cuda.synchronize()
+    assert torch.equal(back.cpu(), c["A"])
+    want = c["C"].double() + c["A"].double() @ c["B"].double()
+    assert np.array_equal(D.cpu().double().numpy(), want.numpy())
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = sp.lib().sp24_diag_wait_timeout(sp._ptr(status), 20_000_000, sp._stream())
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert status.item() & sp.DEV_TIMEOUT
+    # the context is still usable
+    x = torch.ones(4, device="cuda") * 2
+    assert float(x.sum()) == 8.0
+
+
+# ---- full-size workloads, compared on sampled rows --------------------------------------
+
+def test_config2_full_size_bf16():
+    c = inputs.config2()
+    run_case(c, mode="mask", rows=sample_rows(c["M"]))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_config3_full_size_fp8(fmt):
+    c = inputs.config3(fmt)
+    run_case(c, mode="mask", rows=sample_rows(c["M"])[::4])
+
+
+@pytest.mark.parametrize("N", [16, 128, 2048])
+def test_config5_llm_layer(N):
+    c = inputs.config5(N=N)
+    run_case(c, mode="magnitude", out_dtype=torch.bfloat16, rows=sample_rows(c["M"]))
