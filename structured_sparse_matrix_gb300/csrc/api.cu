@@ -141,7 +141,7 @@ sp24_status sp24_decompress(sp24_dtype t, int64_t M, int64_t K, const void* valu
 
 size_t sp24_meta_bytes(sp24_dtype t, int64_t M, int64_t K) {
   if (!is_ab_type(t) || M < 0 || K < 0 || (K % 32) != 0) return 0;
-  const int64_t mtiles = (M + kBM - 1) / kBM;
+  const int64_t mtiles = meta_mtiles(M);
   const int64_t ksteps = (K + stage_k(t) - 1) / stage_k(t);
   return size_t(mtiles * ksteps * meta_stage_bytes(t));
 }
@@ -161,7 +161,7 @@ sp24_status sp24_meta_prepare(sp24_dtype t, int64_t M, int64_t K, const uint32_t
   a.meta = static_cast<uint32_t*>(meta);
   a.M = M;
   a.K = K;
-  a.mtiles = (M + kBM - 1) / kBM;
+  a.mtiles = meta_mtiles(M);
   a.ksteps = (K + stage_k(t) - 1) / stage_k(t);
   if (launch_meta_prepare(a, t, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SP24_ERR_CUDA;

@@ -1,14 +1,16 @@
-// meta.cu -- re-layout of the canonical sparsity index into the image that the sparse
-// GEMM copies, MMA by MMA, from shared memory into tensor memory.
+// meta.cu -- re-layout of the canonical sparsity index into the image the sparse GEMM
+// copies, stage by stage, into tensor memory.
 //
 // Canonical index (as sp24_compress writes it): M x K/32 words, group g of row i in bits
 // 4(g%8)..+3 of word g/8, nibble = p0 | p1 << 2.
 //
-// tcgen05.mma.sp reads the metadata of A from tensor memory (TMEM).  The GEMM gives each
-// MMA its own column-aligned TMEM slot and fills it with one tcgen05.cp.128x128b from a
-// [128 lanes][4 words] block in shared memory.  The image therefore holds, for every
-// 128-row tile, every pipeline stage of the GEMM and each of the stage's 4 MMAs, one
-// such block; the MMA's words come first in each lane's 16 bytes, the rest is padding.
+// tcgen05.mma.sp reads the metadata of A from tensor memory (TMEM), and each MMA's
+// metadata must start at a 16-column-aligned TMEM address.  The GEMM fills one such slot
+// per MMA with one tcgen05.cp.128x128b, which copies 16 bytes per lane into 4 consecutive
+// columns.  So the image holds, for every 128-row tile, every stage of the GEMM and each
+// of the stage's 4 MMAs, one block [128 lanes][4 words] with the MMA's words first.  The
+// image reaches shared memory by TMA together with the operands, and the tensor pipe
+// copies it to TMEM in order with the MMAs; nothing on the way is written by threads.
 //
 // Word placement inside a block (measured on sm_103a with tcgen05.mma.sp, M = 128):
 //   kind::f16 (16-bit types, 32 dense K per MMA, one word per lane): in each 16-row
@@ -16,9 +18,11 @@
 //       word = ((w[16b+l%8] >> 16h) & 0xffff) | ((w[16b+l%8+8] >> 16h) & 0xffff) << 16
 //     so nibble q of lane 16b+l is group (q%4)+4h of row 16b+l%8+8(q/4).
 //   kind::f8f6f4 (8-bit types, 64 dense K per MMA, two words per lane): lane = row,
-//     words 0 and 1 = the row's two canonical words of that K range.
-// Rows beyond M, words beyond K/32 and the padding words hold 0x44444444 (pattern {0,1}
-// in every group); the matching values are zero, so they add nothing.
+//     words 0 and 1 = the row's two canonical words of that K range, unchanged.
+// The image covers M rounded up to a multiple of 256 and K to a multiple of the stage;
+// rows beyond M, words beyond K/32 and the unused words of each 16-byte row hold
+// 0x44444444 (pattern {0,1} in every group).  The matching values are zero, so they add
+// nothing.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -34,7 +38,7 @@ __device__ __forceinline__ uint32_t canon(const MetaArgs& a, int64_t row, int64_
   return a.index[row * a.ldi + w];
 }
 
-// one thread per image word; block = [mma j][128 lanes][4 words]
+// one thread per image word; per (tile, stage): [mma j][128 lanes][4 words]
 template <bool kEightBit>
 __global__ void __launch_bounds__(256) meta_kernel(MetaArgs a) {
   const int64_t total = a.mtiles * a.ksteps * kMmasPerStage * 128 * 4;
@@ -48,16 +52,14 @@ __global__ void __launch_bounds__(256) meta_kernel(MetaArgs a) {
     uint32_t word = kPadWord;
     if constexpr (kEightBit) {
       if (q < 2) word = canon(a, mt * 128 + lane, ks * 8 + j * 2 + q);
-    } else {
-      if (q == 0) {
-        const int64_t w = ks * 4 + j;         // canonical word (32 dense K)
-        const int band = lane >> 4, l = lane & 15;
-        const int64_t rA = mt * 128 + band * 16 + (l & 7);
-        const int h = l >> 3;
-        const uint32_t lo = (canon(a, rA, w) >> (16 * h)) & 0xFFFFu;
-        const uint32_t hi = (canon(a, rA + 8, w) >> (16 * h)) & 0xFFFFu;
-        word = lo | (hi << 16);
-      }
+    } else if (q == 0) {
+      const int64_t w = ks * 4 + j;           // canonical word (32 dense K)
+      const int band = lane >> 4, l = lane & 15;
+      const int64_t rA = mt * 128 + band * 16 + (l & 7);
+      const int h = l >> 3;
+      const uint32_t lo = (canon(a, rA, w) >> (16 * h)) & 0xFFFFu;
+      const uint32_t hi = (canon(a, rA + 8, w) >> (16 * h)) & 0xFFFFu;
+      word = lo | (hi << 16);
     }
     a.meta[o] = word;
   }

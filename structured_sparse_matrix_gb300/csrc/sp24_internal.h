@@ -23,14 +23,16 @@ inline bool is_ab_type(int t) { return t >= kF16 && t <= kU8; }
 // ---- sparse-GEMM K-step geometry (one pipeline stage) shared by meta.cu and spmma.cu
 // 16-bit operands: 128 dense K per stage = 4 MMAs of K=32, metadata one TMEM column
 // per MMA; 8-bit operands: 256 dense K per stage = 4 MMAs of K=64, two columns per MMA.
-// In both cases a stage of compressed A is 128 rows x 128 bytes.  Each MMA's metadata
-// is staged as its own [128 lanes][4 words] block (its words first, the rest padding),
-// copied by one tcgen05.cp.128x128b into a column-aligned TMEM slot.
+// In both cases a stage of compressed A is 128 rows x 128 bytes, and the stage's
+// metadata is one [128 lanes][4 words] block per MMA (the MMA's words first), the
+// source of one tcgen05.cp.128x128b into the MMA's column-aligned TMEM slot.
 constexpr int kBM = 128;
 constexpr int kMmasPerStage = 4;
-constexpr int kMetaBlockBytes = kBM * 16;  // one [128][4-word] block
+constexpr int kMetaBlockBytes = kBM * 16;  // one [128][4-word] block = one tcgen05.cp
 inline int stage_k(int t) { return dtype_bytes(t) == 2 ? 128 : 256; }
 inline int64_t meta_stage_bytes(int) { return int64_t(kMmasPerStage) * kMetaBlockBytes; }
+// The image covers whole 256-row tile pairs (the CTA-pair GEMM loads both halves).
+inline int64_t meta_mtiles(int64_t M) { return 2 * ((M + 2 * kBM - 1) / (2 * kBM)); }
 
 struct CompressArgs {
   const uint8_t* A; int64_t lda_bytes;

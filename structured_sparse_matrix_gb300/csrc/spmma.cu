@@ -3,22 +3,28 @@
 // Semantics: "RDNA4 sparse WMMA builtins", "Builtin reference" (each builtin returns
 // expand(srcA, index) x srcB + srcC, f32 accumulate); "v_smfmac_f32_32x32x32_bf8_bf8",
 // "Semantics" (D = A(sparse) * B + D).  The pages' kernels issue one 16x16 (or 32x32)
-// builtin per wavefront per K step from LDS tiles; here one elected thread per CTA issues
-// tcgen05.mma.sp on a 128 x BN tile held in tensor memory.
+// builtin per wavefront per K step from LDS tiles; here one elected thread issues
+// tcgen05.mma.sp on whole 128- or 256-row tiles whose accumulators live in tensor memory.
 //
-// Structure (one CTA per SM, persistent over output tiles, 6 warps):
-//   warp 0     TMA producer: per K stage, one 128x128-byte box of compressed A
-//              (K-major, 128-byte swizzle), BN/atom boxes of B (K x N row-major =
-//              MN-major, 128-byte swizzle) and one contiguous block of the metadata
-//              image (cp.async.bulk), all completing on the stage's "full" mbarrier.
-//   warp 1     TMEM owner + MMA issuer: copies the stage's metadata smem -> TMEM
-//              (tcgen05.cp), issues 4 tcgen05.mma.sp, and tcgen05.commit releases the
-//              stage; after the last stage it commits the accumulator buffer.
-//   warps 2-5  epilogue: tcgen05.ld of their 32 TMEM lanes, + C, cast, store; then free
-//              the accumulator buffer.  Accumulators are double-buffered in TMEM, so
-//              the epilogue of tile t overlaps the main loop of tile t+1.
-// Every mbarrier wait is bounded (see mbar_wait); a wait that gives up sets
-// SP24_DEV_TIMEOUT in the caller's status word and the CTA drains and exits.
+// Two variants of one kernel:
+//   single  (N <= 128): one CTA per 128 x 128 tile, tcgen05 cta_group::1, accumulator
+//           double-buffered in TMEM so the epilogue of one tile overlaps the next.
+//   pair    (N > 128):  a cluster of two CTAs per 256 x 256 tile, cta_group::2: each CTA
+//           stages its own 128 rows of A and its own 128-column half of B and the even
+//           CTA issues the MMAs, so each loaded byte feeds twice the work.  The 256-column
+//           accumulator is single-buffered; eight epilogue warps drain it to registers
+//           first and release it before they add C and store.
+// Warp roles (persistent over tiles, one CTA per SM):
+//   warp 0   TMA producer: per stage one box of compressed A (K-major, 128-byte swizzle),
+//            the B boxes (K x N row-major = MN-major, 128-byte swizzle) and the stage's
+//            8 KB of the metadata image (one [128 lanes][16 bytes] block per MMA).
+//   warp 1   TMEM owner and MMA issuer: per stage 4 x tcgen05.cp (metadata block -> its
+//            MMA's 16-column-aligned TMEM slot; slot set = ring stage), 4 x tcgen05.mma.sp
+//            and one tcgen05.commit that frees the stage.  The copies run in the same
+//            in-order tcgen05 pipe as the MMAs, so no thread touches the metadata.
+//   warps 2+ epilogue: tcgen05.ld, + C, cast to f32 / bf16, 16-byte stores.
+// Every mbarrier wait is bounded; a wait that gives up sets SP24_DEV_TIMEOUT in the
+// caller's status word and the CTA drains its in-flight work and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -35,47 +41,109 @@ namespace sp24 {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = 128 * 128;  // one stage of compressed A: 128 rows x 128 bytes
+constexpr int kBColsPerCta = 128;   // B columns staged by each CTA per stage
+constexpr int kSlotCols = 16;       // TMEM columns per MMA metadata slot (aligned)
 
 struct MmaParams {
-  const uint8_t* meta;
   const void* C;
   void* D;
   int64_t ldc, ldd;
   int32_t* status;
   int M, N, K;
-  int mtiles, ntiles, num_kb;
+  int mtiles, ntiles, num_kb;  // tiles of the variant (128 or 256 rows, 128 or 256 cols)
   uint64_t limit_ns;
 };
 
-template <int ESZ, int BN>
+template <int ESZ, bool kPair>
 struct Geo {
-  static constexpr int kStageK = ESZ == 2 ? 128 : 256;          // dense K per stage
-  static constexpr int kMmaK = ESZ == 2 ? 32 : 64;               // dense K per MMA
-  static constexpr int kMmas = kStageK / kMmaK;                  // 4
-  static constexpr int kMetaBytes = kMmas * kMetaBlockBytes;     // 4 blocks of 2 KB
-  static constexpr int kMetaSlotCols = 16;                       // TMEM columns per MMA slot
-  static constexpr int kAtomN = 128 / ESZ;                       // N elements per 128 B
-  static constexpr int kAtoms = BN / kAtomN;
-  static constexpr int kAtomBytes = kStageK * 128;               // one B box
-  static constexpr int kBBytes = kAtoms * kAtomBytes;
+  static constexpr int kStageK = ESZ == 2 ? 128 : 256;       // dense K per stage
+  static constexpr int kMmaK = ESZ == 2 ? 32 : 64;            // dense K per MMA
+  static constexpr int kMmas = kStageK / kMmaK;               // 4
+  static constexpr int kMetaBytes = kMmas * kMetaBlockBytes;  // 8 KB per stage
+  static constexpr int kAtomN = 128 / ESZ;                    // B columns per 128 bytes
+  static constexpr int kAtoms = kBColsPerCta / kAtomN;
+  static constexpr int kAtomBytes = kStageK * 128;            // one B box
+  static constexpr int kBBytes = kAtoms * kAtomBytes;         // 32 KB
   static constexpr int kStageBytes = kABytes + kBBytes + kMetaBytes;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
-  static constexpr uint32_t kTx = kABytes + kBBytes + kMetaBytes;
-  static constexpr uint32_t kMetaTmemCol = 2 * BN;               // after both accumulators
-  static_assert(BN % kAtomN == 0, "BN must be a multiple of the swizzle atom");
-  static_assert(2 * BN + kStages * kMmas * kMetaSlotCols <= int(kTmemCols), "TMEM budget");
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static constexpr uint32_t kTx = uint32_t(kStageBytes) * (kPair ? 2 : 1);
+  static constexpr int kTileM = kPair ? 256 : 128;
+  static constexpr int kTileN = kPair ? 256 : 128;
+  static constexpr int kAccBufs = kPair ? 1 : 2;
+  static constexpr int kAccCols = kAccBufs * kTileN;          // 256 in both variants
+  static constexpr uint32_t kMetaCol = kAccCols;              // slot set s at + s * 64
+  static constexpr int kEpiWarps = kPair ? 8 : 4;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);       // 192 or 320
+  static_assert(kAccCols + kStages * kMmas * kSlotCols <= int(kTmemCols), "TMEM budget");
+  static_assert(kSmemBytes <= 232448 - 256, "shared memory budget");
 };
 
-// OUT: 0 = f32, 1 = bf16, 2 = s32 (reserved).  C (if present) is f32 for float paths.
-template <int ESZ, int BN, int OUT>
-__global__ void __launch_bounds__(kThreads, 1)
+// Epilogue for one 32-column chunk of one output row: v += C (f32, nullable), cast, store.
+// Columns at or beyond N are not touched; full chunks use 16-byte vector accesses.
+template <int OUT>
+__device__ __forceinline__ void store_chunk(float (&v)[32], const MmaParams& p, int row, int col0) {
+  const bool full = col0 + 32 <= p.N;
+  if (p.C != nullptr) {
+    const float* crow = static_cast<const float*>(p.C) + int64_t(row) * p.ldc + col0;
+    if (full) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 cv = __ldcs(reinterpret_cast<const float4*>(crow + j));
+        v[j] += cv.x;
+        v[j + 1] += cv.y;
+        v[j + 2] += cv.z;
+        v[j + 3] += cv.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < p.N) v[j] += crow[j];
+    }
+  }
+  if constexpr (OUT == 0) {
+    float* drow = static_cast<float*>(p.D) + int64_t(row) * p.ldd + col0;
+    if (full) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        __stcs(reinterpret_cast<float4*>(drow + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < p.N) drow[j] = v[j];
+    }
+  } else {
+    __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + int64_t(row) * p.ldd + col0;
+    if (full) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        __nv_bfloat162 h0 = __floats2bfloat162_rn(v[j], v[j + 1]);
+        __nv_bfloat162 h1 = __floats2bfloat162_rn(v[j + 2], v[j + 3]);
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(v[j + 4], v[j + 5]);
+        __nv_bfloat162 h3 = __floats2bfloat162_rn(v[j + 6], v[j + 7]);
+        uint4 u;
+        memcpy(&u.x, &h0, 4);
+        memcpy(&u.y, &h1, 4);
+        memcpy(&u.z, &h2, 4);
+        memcpy(&u.w, &h3, 4);
+        __stcs(reinterpret_cast<uint4*>(drow + j), u);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < p.N) drow[j] = __float2bfloat16_rn(v[j]);
+    }
+  }
+}
+
+// OUT: 0 = f32 output, 1 = bf16 output.  C (nullable) is f32.
+template <int ESZ, int OUT, bool kPair>
+__global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
     spmma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const MmaParams p, const uint32_t idesc) {
-  using G = Geo<ESZ, BN>;
+                 const __grid_constant__ CUtensorMap tmM, const MmaParams p,
+                 const uint32_t idesc) {
+  using G = Geo<ESZ, kPair>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
@@ -84,9 +152,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int unit = kPair ? int(blockIdx.x >> 1) : int(blockIdx.x);
+  const int nunits = kPair ? int(gridDim.x >> 1) : int(gridDim.x);
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kABytes;
+  uint8_t* sB = sA + kStages * kABytes;
   uint8_t* sM = sB + kStages * G::kBBytes;
+  const int ntiles_total = p.mtiles * p.ntiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -95,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], G::kEpiWarps * (kPair ? 2 : 1));
     }
     mbar_init(&drain_bar, 1);
     abort_flag = 0;
@@ -104,187 +176,194 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    prefetch_tmap(&tmM);
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(&tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();  // the peer's barriers exist before any remote use
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const int ntiles_total = p.mtiles * p.ntiles;
   volatile int* abort = &abort_flag;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int t = blockIdx.x; t < ntiles_total && !*abort; t += gridDim.x) {
+      int q = 0;
+      for (int t = unit; t < ntiles_total && !*abort; t += nunits) {
         const int mt = t % p.mtiles, nt = t / p.mtiles;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort, p.limit_ns)) break;
-          mbar_arrive_expect_tx(&full_bar[stage], G::kTx);
-          tma_load_2d(sA + stage * kABytes, &tmA, &full_bar[stage], kb * (G::kStageK / 2),
-                      mt * 128);
+        const int mt128 = kPair ? mt * 2 + int(rank) : mt;  // this CTA's 128-row tile
+        const int bcol = nt * G::kTileN + int(rank) * kBColsPerCta;
+        for (int kb = 0; kb < p.num_kb; ++kb, ++q) {
+          const int s = q % kStages;
+          if (!mbar_wait(&empty_bar[s], ((q / kStages) & 1) ^ 1u, abort, p.limit_ns)) break;
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], G::kTx);
+          const int kx = kb * (G::kStageK / 2);
+          const int mrow = (mt128 * p.num_kb + kb) * (G::kMetaBytes / 128);
+          if constexpr (kPair) {
+            const uint32_t fb = mapa(&full_bar[s], 0);
+            tma_load_2d_pair(sA + s * kABytes, &tmA, fb, kx, mt128 * 128);
 #pragma unroll
-          for (int a = 0; a < G::kAtoms; ++a)
-            tma_load_2d(sB + stage * G::kBBytes + a * G::kAtomBytes, &tmB, &full_bar[stage],
-                        nt * BN + a * G::kAtomN, kb * G::kStageK);
-          bulk_load(sM + stage * G::kMetaBytes,
-                    p.meta + (int64_t(mt) * p.num_kb + kb) * G::kMetaBytes, G::kMetaBytes,
-                    &full_bar[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+            for (int a = 0; a < G::kAtoms; ++a)
+              tma_load_2d_pair(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, fb,
+                               bcol + a * G::kAtomN, kb * G::kStageK);
+            tma_load_2d_pair(sM + s * G::kMetaBytes, &tmM, fb, 0, mrow);
+          } else {
+            tma_load_2d(sA + s * kABytes, &tmA, &full_bar[s], kx, mt128 * 128);
+#pragma unroll
+            for (int a = 0; a < G::kAtoms; ++a)
+              tma_load_2d(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, &full_bar[s],
+                          bcol + a * G::kAtomN, kb * G::kStageK);
+            tma_load_2d(sM + s * G::kMetaBytes, &tmM, &full_bar[s], 0, mrow);
           }
         }
       }
-      if (*abort) {
-        // give copies already issued time to land before the CTA can exit
+      if (*abort) {  // give copies already issued time to land before the CTA exits
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 2000000ull) {
         }
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (rank == 0 && lane == 0) {
       const uint64_t adesc_hi = smem_desc_hi(16, 1024, 2);
       const uint64_t bdesc_hi = smem_desc_hi(G::kAtomBytes, 1024, 2);
       const uint64_t mdesc_hi = smem_desc_hi(0, 128, 0);
-      int stage = 0;
-      uint32_t phase = 0;
-      int local = 0;
-      for (int t = blockIdx.x; t < ntiles_total && !*abort; t += gridDim.x, ++local) {
-        const int abuf = local & 1;
-        const uint32_t acc_parity = ((local >> 1) & 1) ^ 1u;
-        if (!mbar_wait(&acc_empty[abuf], acc_parity, abort, p.limit_ns)) break;
+      int q = 0, local = 0;
+      for (int t = unit; t < ntiles_total && !*abort; t += nunits, ++local) {
+        const int abuf = kPair ? 0 : (local & 1);
+        const int use = kPair ? local : (local >> 1);  // earlier uses of this buffer
+        if (!mbar_wait(&acc_empty[abuf], (use & 1) ^ 1u, abort, p.limit_ns)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + uint32_t(abuf * BN);
+        const uint32_t d_tmem = tmem + uint32_t(abuf * G::kTileN);
         bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort, p.limit_ns)) {
+        for (int kb = 0; kb < p.num_kb; ++kb, ++q) {
+          const int s = q % kStages;
+          const uint32_t par = (q / kStages) & 1;
+          if (!mbar_wait(&full_bar[s], par, abort, p.limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // metadata: MMA j of this stage reads the 16-column-aligned slot (stage, j)
-          const uint32_t e_tmem =
-              tmem + G::kMetaTmemCol + uint32_t(stage * G::kMmas * G::kMetaSlotCols);
-          const uint32_t m_saddr = smem_addr(sM + stage * G::kMetaBytes);
+          const uint32_t e_tmem = tmem + G::kMetaCol + uint32_t(s * G::kMmas * kSlotCols);
+          const uint32_t p_saddr = smem_addr(sM + s * G::kMetaBytes);
 #pragma unroll
-          for (int j = 0; j < G::kMmas; ++j)
-            tc_cp_128x128b(e_tmem + j * G::kMetaSlotCols,
-                           smem_desc(m_saddr + j * kMetaBlockBytes, mdesc_hi));
-          const uint32_t a_saddr = smem_addr(sA + stage * kABytes);
-          const uint32_t b_saddr = smem_addr(sB + stage * G::kBBytes);
+          for (int j = 0; j < G::kMmas; ++j) {
+            const uint64_t md = smem_desc(p_saddr + j * kMetaBlockBytes, mdesc_hi);
+            if constexpr (kPair)
+              tc_cp_128x128b_pair(e_tmem + j * kSlotCols, md);
+            else
+              tc_cp_128x128b(e_tmem + j * kSlotCols, md);
+          }
+          const uint32_t a_saddr = smem_addr(sA + s * kABytes);
+          const uint32_t b_saddr = smem_addr(sB + s * G::kBBytes);
           const int k0 = kb * G::kStageK;
 #pragma unroll
           for (int j = 0; j < G::kMmas; ++j) {
             if (k0 + j * G::kMmaK < p.K) {
-              tc_mma_sp<ESZ == 1>(d_tmem, smem_desc(a_saddr + 32 * j, adesc_hi),
-                                  smem_desc(b_saddr + j * G::kMmaK * 128, bdesc_hi),
-                                  e_tmem + j * G::kMetaSlotCols, idesc,
-                                  (kb > 0 || j > 0) ? 1u : 0u);
+              const uint64_t ad = smem_desc(a_saddr + 32 * j, adesc_hi);
+              const uint64_t bd = smem_desc(b_saddr + j * G::kMmaK * 128, bdesc_hi);
+              const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+              if constexpr (kPair)
+                tc_mma_sp_pair<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, idesc, acc);
+              else
+                tc_mma_sp<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, idesc, acc);
             }
           }
-          tc_commit(&empty_bar[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if constexpr (kPair)
+            tc_commit_pair_mc(&empty_bar[s], 3);
+          else
+            tc_commit(&empty_bar[s]);
         }
         if (!ok) break;
-        tc_commit(&acc_full[abuf]);
+        if constexpr (kPair)
+          tc_commit_pair_mc(&acc_full[abuf], 3);
+        else
+          tc_commit(&acc_full[abuf]);
       }
-      // all MMAs issued by this thread complete before TMEM can be released
-      tc_commit(&drain_bar);
+      // every MMA issued by this thread completes before TMEM can be released
+      if constexpr (kPair)
+        tc_commit_pair(&drain_bar);
+      else
+        tc_commit(&drain_bar);
       mbar_wait_drain(&drain_bar, 0, 1000000000ull);
     }
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    // ---------------------------------------------------------------- epilogue
+    const int ew = warp - 2;
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 (hardware rule: warp id % 4)
+    const uint32_t acc_empty_addr =
+        kPair ? mapa(&acc_empty[0], 0) : smem_addr(&acc_empty[0]);
     int local = 0;
-    for (int t = blockIdx.x; t < ntiles_total; t += gridDim.x, ++local) {
+    for (int t = unit; t < ntiles_total; t += nunits, ++local) {
       const int mt = t % p.mtiles, nt = t / p.mtiles;
-      const int abuf = local & 1;
-      if (!mbar_wait(&acc_full[abuf], (local >> 1) & 1, abort, p.limit_ns)) break;
+      const int abuf = kPair ? 0 : (local & 1);
+      const int use = kPair ? local : (local >> 1);
+      if (!mbar_wait(&acc_full[abuf], use & 1, abort, p.limit_ns)) break;
       tc_fence_after();
-      const int row = mt * 128 + quad * 32 + lane;
-      const bool row_ok = row < p.M;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tc_ld_32x32b_x32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(abuf * BN + c * 32), r);
+      const int row = mt * G::kTileM + int(rank) * 128 + quad * 32 + lane;
+      const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16) + uint32_t(abuf * G::kTileN);
+      if constexpr (kPair) {
+        // drain this warp's 32 rows x 128 columns, free the accumulator, then store
+        const int half = ew >> 2;
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(lane_base + uint32_t(half * 128 + c * 32), r[c]);
         tc_wait_ld();
-        const int col0 = nt * BN + c * 32;
-        if (!row_ok || col0 >= p.N) continue;
-        float v[32];
-        if (p.K > 0) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(abuf * sizeof(uint64_t)));
+        if (row < p.M) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        } else {
+          for (int c = 0; c < 4; ++c) {
+            const int col0 = nt * G::kTileN + half * 128 + c * 32;
+            if (col0 < p.N) {
+              float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        }
-        const bool full = col0 + 32 <= p.N;
-        if (p.C != nullptr) {
-          const float* crow = static_cast<const float*>(p.C) + int64_t(row) * p.ldc + col0;
-          if (full) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              const float4 cv = __ldcs(reinterpret_cast<const float4*>(crow + j));
-              v[j] += cv.x;
-              v[j + 1] += cv.y;
-              v[j + 2] += cv.z;
-              v[j + 3] += cv.w;
+              for (int j = 0; j < 32; ++j) v[j] = p.K > 0 ? __uint_as_float(r[c][j]) : 0.f;
+              store_chunk<OUT>(v, p, row, col0);
             }
-          } else {
-            for (int j = 0; j < 32 && col0 + j < p.N; ++j) v[j] += crow[j];
           }
         }
-        if constexpr (OUT == 0) {
-          float* drow = static_cast<float*>(p.D) + int64_t(row) * p.ldd + col0;
-          if (full) {
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < G::kTileN / 32; ++c) {
+          uint32_t r[32];
+          tc_ld_32x32b_x32(lane_base + uint32_t(c * 32), r);
+          tc_wait_ld();
+          const int col0 = nt * G::kTileN + c * 32;
+          if (row >= p.M || col0 >= p.N) continue;
+          float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              __stcs(reinterpret_cast<float4*>(drow + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
-          } else {
-            for (int j = 0; j < 32 && col0 + j < p.N; ++j) drow[j] = v[j];
-          }
-        } else {
-          __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + int64_t(row) * p.ldd + col0;
-          if (full) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              __nv_bfloat162 h0 = __floats2bfloat162_rn(v[j], v[j + 1]);
-              __nv_bfloat162 h1 = __floats2bfloat162_rn(v[j + 2], v[j + 3]);
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(v[j + 4], v[j + 5]);
-              __nv_bfloat162 h3 = __floats2bfloat162_rn(v[j + 6], v[j + 7]);
-              uint4 u;
-              memcpy(&u.x, &h0, 4);
-              memcpy(&u.y, &h1, 4);
-              memcpy(&u.z, &h2, 4);
-              memcpy(&u.w, &h3, 4);
-              __stcs(reinterpret_cast<uint4*>(drow + j), u);
-            }
-          } else {
-            for (int j = 0; j < 32 && col0 + j < p.N; ++j) drow[j] = __float2bfloat16_rn(v[j]);
-          }
+          for (int j = 0; j < 32; ++j) v[j] = p.K > 0 ? __uint_as_float(r[j]) : 0.f;
+          store_chunk<OUT>(v, p, row, col0);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(abuf * sizeof(uint64_t)));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[abuf]);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) {
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
+  }
   if (threadIdx.x == 0 && *abort && p.status != nullptr) atomicOr(p.status, kDevTimeout);
 }
 
@@ -304,46 +383,89 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 2-D tensor map over a row-major matrix: inner extent `cols` elements of `esz` bytes,
-// `rows` rows, row pitch `pitch_bytes`; box = box_cols x box_rows, 128-byte swizzle.
+// `rows` rows, row pitch `pitch_bytes`; box = box_cols x box_rows.
 bool make_tmap(CUtensorMap* m, const void* base, int esz, uint64_t cols, uint64_t rows,
-               uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows) {
+               uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows,
+               CUtensorMapSwizzle swz) {
   auto enc = get_encode();
   if (!enc) return false;
-  const CUtensorMapDataType dt =
-      esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType dt = esz == 4   ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                 : esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                            : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {pitch_bytes};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int ESZ, int BN, int OUT>
-int run(const MmaParams& p, const void* values, int64_t ldv, const void* B, int64_t ldb,
-        uint32_t idesc, int num_sms, cudaStream_t s) {
-  using G = Geo<ESZ, BN>;
-  CUtensorMap tA, tB;
+template <int ESZ, int OUT, bool kPair>
+int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const void* B,
+        int64_t ldb, uint32_t idesc, int num_sms, cudaStream_t s) {
+  using G = Geo<ESZ, kPair>;
+  p.mtiles = (p.M + G::kTileM - 1) / G::kTileM;
+  p.ntiles = (p.N + G::kTileN - 1) / G::kTileN;
+  CUtensorMap tA, tB, tM;
   memset(&tA, 0, sizeof(tA));
   memset(&tB, 0, sizeof(tB));
+  memset(&tM, 0, sizeof(tM));
   if (p.K > 0) {  // with K == 0 no stage is loaded and the maps are never read
     if (!make_tmap(&tA, values, ESZ, uint64_t(p.K / 2), uint64_t(p.M), uint64_t(ldv) * ESZ,
-                   128 / ESZ, 128))
+                   128 / ESZ, 128, CU_TENSOR_MAP_SWIZZLE_128B))
       return 4;
     if (!make_tmap(&tB, B, ESZ, uint64_t(p.N), uint64_t(p.K), uint64_t(ldb) * ESZ, G::kAtomN,
-                   G::kStageK))
+                   G::kStageK, CU_TENSOR_MAP_SWIZZLE_128B))
+      return 4;
+    // the compact metadata image as rows of 128 bytes; one (tile, stage) block per box
+    const uint64_t mrows = uint64_t(meta_mtiles(p.M)) * p.num_kb * (G::kMetaBytes / 128);
+    if (!make_tmap(&tM, meta, 4, 32, mrows, 128, 32, G::kMetaBytes / 128,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
       return 4;
   }
-  auto kern = spmma_kernel<ESZ, BN, OUT>;
+  auto kern = spmma_kernel<ESZ, OUT, kPair>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) !=
       cudaSuccess)
     return 4;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(G::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = G::kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   const int tiles = p.mtiles * p.ntiles;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, kThreads, G::kSmemBytes, s>>>(tA, tB, p, idesc);
+  int units = num_sms;
+  if (kPair) {
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess ||
+        max_clusters < 1) {
+      cudaGetLastError();
+      max_clusters = num_sms / 2;
+    }
+    units = max_clusters;
+  }
+  if (tiles < units) units = tiles;
+  cfg.gridDim = dim3(units * (kPair ? 2 : 1), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tM, p, idesc) != cudaSuccess) return 4;
   return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+template <int ESZ, int OUT>
+int dispatch(const MmaParams& p, const void* values, int64_t ldv, const void* meta,
+             const void* B, int64_t ldb, uint32_t at, uint32_t bt, int num_sms, cudaStream_t s) {
+  if (p.N > 128)  // wide outputs: 256 x 256 tiles on CTA pairs
+    return run<ESZ, OUT, true>(p, values, ldv, meta, B, ldb, idesc_sparse_f32(at, bt, 256, 256),
+                               num_sms, s);
+  return run<ESZ, OUT, false>(p, values, ldv, meta, B, ldb, idesc_sparse_f32(at, bt, 128, 128),
+                              num_sms, s);
 }
 
 }  // namespace
@@ -355,7 +477,6 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   (void)tc;
   const int esz = dtype_bytes(ta);
   MmaParams p;
-  p.meta = static_cast<const uint8_t*>(meta);
   p.C = C;
   p.D = D;
   p.ldc = ldc;
@@ -364,22 +485,18 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
-  p.mtiles = int((M + 127) / 128);
-  const int stage_k = esz == 2 ? 128 : 256;
-  p.num_kb = int((K + stage_k - 1) / stage_k);
+  p.mtiles = p.ntiles = 0;
+  p.num_kb = int((K + stage_k(ta) - 1) / stage_k(ta));
   p.limit_ns = 1000000000ull;  // 1 s per wait
-  constexpr int BN = 128;
-  p.ntiles = int((N + BN - 1) / BN);
   // kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2
   const uint32_t at = (ta == kBF16 || ta == kE5M2) ? 1u : 0u;
   const uint32_t bt = (tb == kBF16 || tb == kE5M2) ? 1u : 0u;
-  const uint32_t idesc = idesc_sparse_f32(at, bt, 128, BN);
   const bool out_bf16 = td == kBF16;
   if (esz == 2)
-    return out_bf16 ? run<2, BN, 1>(p, values, ldv, B, ldb, idesc, num_sms, s)
-                    : run<2, BN, 0>(p, values, ldv, B, ldb, idesc, num_sms, s);
-  return out_bf16 ? run<1, BN, 1>(p, values, ldv, B, ldb, idesc, num_sms, s)
-                  : run<1, BN, 0>(p, values, ldv, B, ldb, idesc, num_sms, s);
+    return out_bf16 ? dispatch<2, 1>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s)
+                    : dispatch<2, 0>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s);
+  return out_bf16 ? dispatch<1, 1>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s)
+                  : dispatch<1, 0>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s);
 }
 
 }  // namespace sp24

@@ -51,10 +51,10 @@ def test_version_and_status_strings():
 
 def test_meta_bytes_host_only():
     L = sp.lib()
-    # 8 KiB per (128-row tile, stage): four [128][16-byte] blocks, one per MMA;
-    # a stage is 128 dense K for 16-bit types and 256 for 8-bit types
+    # 8 KiB per (128-row tile, stage): four [128][16-byte] blocks, one per MMA; a stage
+    # is 128 dense K for 16-bit types and 256 for 8-bit types; M rounds up to 256 rows
     assert L.sp24_meta_bytes(BF16, 4096, 4096) == 32 * 32 * 8192
-    assert L.sp24_meta_bytes(F16, 64, 128) == 8192
+    assert L.sp24_meta_bytes(F16, 64, 128) == 2 * 8192
     assert L.sp24_meta_bytes(F16, 129, 160) == 2 * 2 * 8192
     assert L.sp24_meta_bytes(E4M3, 8192, 8192) == 64 * 32 * 8192
     assert L.sp24_meta_bytes(F16, 64, 100) == 0      # K % 32 != 0

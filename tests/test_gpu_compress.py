@@ -131,9 +131,10 @@ def test_empty_inputs_are_no_ops():
 
 def _meta_image_np(index: np.ndarray, M: int, K: int, eight_bit: bool) -> np.ndarray:
     """Image layout: per (128-row tile, stage, MMA j) one [128 lanes][4 words] block with
-    the MMA's metadata words first and 0x44444444 padding after them."""
+    the MMA's words first (16-bit: one interleaved word; 8-bit: the row's two canonical
+    words) and 0x44444444 elsewhere; the tiles cover M rounded up to 256 rows."""
     stage = 256 if eight_bit else 128
-    mt, ks = -(-M // 128), -(-K // stage)
+    mt, ks = 2 * -(-M // 256), -(-K // stage)
     canon = np.full((mt * 128, ks * stage // 32), 0x44444444, dtype=np.uint64)
     canon[:M, :K // 32] = index[:, :K // 32]
     out = []
