@@ -50,6 +50,10 @@ CONFIGS = {
                 "fp8 E4M3 M=N=K=8192, random 2:4 mask, no C, D f32"),
     "c3-e5m2": (lambda: inputs.config3("e5m2"), "e5m2", "mask", torch.float32,
                 "fp8 E5M2 M=N=K=8192, random 2:4 mask, no C, D f32"),
+    "c4-s8": (lambda: inputs.config4("s8"), "s8", "mask", torch.int32,
+              "int8 s8 x s8 M=N=K=8192, random 2:4 mask, C s32, D s32 (exact)"),
+    "c4-u8": (lambda: inputs.config4("u8"), "u8", "mask", torch.int32,
+              "int8 u8 x s8 M=N=K=8192, random 2:4 mask, C s32, D s32 (exact)"),
     "c5-16": (lambda: inputs.config5(16), "bf16", "magnitude", torch.bfloat16,
               "LLM layer W 14336x4096 bf16 magnitude-pruned, X 4096x16, D bf16"),
     "c5-128": (lambda: inputs.config5(128), "bf16", "magnitude", torch.bfloat16,
@@ -239,15 +243,16 @@ def reference_arm(args, world, rank):
         step()
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
     value = 2.0 * rows * c["N"] * c["K"] / dt / 1e12
+    unit = "TOP/s" if ta in ("s8", "u8") else "TFLOP/s"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64" if ta not in ("s8", "u8") else "int64",
         "data": "synthetic", "config": {"workload": desc, "M": c["M"], "N": c["N"], "K": c["K"]},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
                          "sample": f"first {rows} of {c['M']} rows per step (compress + product)"},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -292,7 +297,12 @@ def gpu_arm(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     L = sp.lib()
     codes = sp.DTYPE_CODES
-    cs = {"ta": codes[tdt], "td": codes[out_dtype], "tc": codes[torch.float32]}
+    integer = ta in ("s8", "u8")
+    cs = {"ta": codes[tdt], "tb": codes[base["B"].dtype], "td": codes[out_dtype],
+          "tc": codes[torch.int32 if integer else torch.float32]}
+    # scratch for the integer path (operands widened to bf16), reused by every step
+    ws_bytes = sp.workspace_bytes(tdt, base["B"].dtype, M, N, K)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
 
     def launch(s, ev=None):
         # the three C-ABI calls of one step, on the current stream
@@ -309,9 +319,9 @@ def gpu_arm(args, world, rank, local):
                                   sp._ptr(s["meta"]), st)
         if ev is not None:
             ev[2].record(stream)
-        rc |= L.sp24_mma(cs["ta"], cs["ta"], cs["tc"], cs["td"], M, N, K, sp._ptr(s["values"]),
+        rc |= L.sp24_mma(cs["ta"], cs["tb"], cs["tc"], cs["td"], M, N, K, sp._ptr(s["values"]),
                          K // 2, sp._ptr(s["meta"]), sp._ptr(s["B"]), N, sp._ptr(s["C"]), N,
-                         sp._ptr(s["D"]), N, sp._ptr(status), st)
+                         sp._ptr(s["D"]), N, sp._ptr(ws), ws_bytes, sp._ptr(status), st)
         if ev is not None:
             ev[3].record(stream)
         if rc != 0:
@@ -349,17 +359,19 @@ def gpu_arm(args, world, rank, local):
     # --- roofline of the dominant kernel (sp24_mma): tensor-bound sparse contraction
     peaks, src = load_peaks()
     dense = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    # 8-bit integers run widened to bf16: their roof is the bf16 sparse rate
     dense_peak = dense * (FP8_OVER_BF16 if ta in ("e4m3", "e5m2") else 1.0)
     peak = dense_peak * SPARSE_OVER_DENSE
     esz = torch.empty((), dtype=tdt).element_size()
     osz = torch.empty((), dtype=out_dtype).element_size()
     mma_bytes = (M * K // 2 * esz + sp.meta_bytes(tdt, M, K) + K * N * esz +
                  (M * N * 4 if base["C"] is not None else 0) + M * N * osz)
+    unit = "TOP/s" if integer else "TFLOP/s"
     achieved_tf = flops / (k_mma * 1e-3) / 1e12
     intensity = flops / mma_bytes
     ridge = peak * 1e12 / (peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]) * 1e9)
     if intensity >= ridge:
-        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": peak, "unit": "TFLOP/s",
+        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": peak, "unit": unit,
                 "frac": achieved_tf / peak}
     else:
         gbs = mma_bytes / (k_mma * 1e-3) / 1e9
@@ -370,10 +382,12 @@ def gpu_arm(args, world, rank, local):
     roof["algorithmic_bytes"] = mma_bytes
     roof["peak_source"] = (f"{src}: bf16 dense {dense} TFLOP/s"
                            f"{' x2 (fp8/bf16 nominal)' if ta in ('e4m3', 'e5m2') else ''}"
-                           " x2 (2:4 sparse / dense nominal), burst figure")
+                           " x2 (2:4 sparse / dense nominal), burst figure"
+                           f"{'; int8 runs exactly on the bf16 path' if integer else ''}")
     # compression kernel: HBM-bound, algorithmic bytes = A + mask read, values + index written
     cbytes = M * K * esz + (M * K if mode == "mask" else 0) + M * K // 2 * esz + M * K // 8
     kernels = {
+        "note": "sp24_mma time includes the int8->bf16 widening pass" if integer else None,
         "sp24_compress_us": k_compress * 1e3,
         "sp24_compress_gbs": cbytes / (k_compress * 1e-3) / 1e9,
         "sp24_meta_prepare_us": k_meta * 1e3,
@@ -414,7 +428,7 @@ def gpu_arm(args, world, rank, local):
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(a.elapsed_time(b) / n_e2e, world)
-        e2e = {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": unit,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     # --- CPU baseline: the oracle on this host's cores, bounded sample, rank 0 at N=1
@@ -422,13 +436,13 @@ def gpu_arm(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu:
         fps, rows, dt, threads = oracle_sample(base, mode, float(os.environ.get(
             "SP24_CPU_SECONDS", "12")))
-        cpu = {"value": fps / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"first {rows} of {M} rows (oracle compress + float64 product), "
-                         f"{dt:.1f} s"}
+        cpu = {"value": fps / 1e12, "unit": unit, "cores": threads, "kind": "oracle",
+               "sample": f"first {rows} of {M} rows (oracle compress + "
+                         f"{'int64' if integer else 'float64'} product), {dt:.1f} s"}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ta, "data": "synthetic",

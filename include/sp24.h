@@ -127,11 +127,13 @@ size_t sp24_meta_bytes(sp24_dtype t, int64_t M, int64_t K);
 /*
  * sp24_meta_prepare -- re-lay the canonical index (as sp24_compress writes it) into the
  * image sp24_mma copies into tensor memory: for every 128-row tile of A, every K step of
- * the kernel (128 dense K for 16-bit types, 256 for 8-bit types) and each of the step's
- * four MMAs, one [128][16-byte] block.  Rows are padded to a multiple of 128 and K to
+ * the kernel (128 dense K for 16-bit types, 256 for FP8 types) and each of the step's
+ * four MMAs, one [128][16-byte] block.  Rows are padded to a multiple of 256 and K to
  * the K step; pad groups get the valid pattern {0,1} and their values are zero, so they
  * add nothing.  The image is a format private to sp24_mma (sp24_meta_bytes() gives its
  * size); the canonical index stays the interchange format.
+ * 8-bit integer types use the layout of the 16-bit types (their product runs on the
+ * bf16 tensor path).
  * index : device, M x K/32 words, ldi >= K/32, 4-byte aligned.
  * meta  : device, sp24_meta_bytes(t, M, K) bytes, 16-byte aligned.
  */
@@ -139,28 +141,42 @@ sp24_status sp24_meta_prepare(sp24_dtype t, int64_t M, int64_t K, const uint32_t
                               int64_t ldi, void *meta, void *stream);
 
 /*
- * sp24_mma -- D = expand(values, index) * B + C, one launch of the tcgen05 sparse GEMM.
+ * sp24_mma_workspace_bytes -- device workspace sp24_mma needs for (ta, tb, M, N, K): for
+ * 8-bit integer operands the bytes of both operands widened to bf16 (A_c: M x K/2, B:
+ * K x N with the row pitch rounded up to 8 elements); 0 for float operands.
+ */
+size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t N, int64_t K);
+
+/*
+ * sp24_mma -- D = expand(values, index) * B + C, the sparse product of "Builtin reference"
+ * (expand(srcA, index) x srcB + srcC) on the tcgen05 sparse tensor cores.
  *
  * ta, tb, tc, td supported combinations (anything else: SP24_ERR_UNSUPPORTED):
  *   (F16, F16) and (BF16, BF16)     -> f32 accumulate, tc in {F32, none}, td in {F32, BF16}
  *   (E4M3, E4M3) and (E5M2, E5M2)   -> f32 accumulate, tc in {F32, none}, td in {F32, BF16}
- *   (S8, S8) and (U8, S8)           -> exact integer accumulate, tc in {S32, none}, td = S32
- *                                      (two's-complement wrap, no clamp)
+ *   (S8, S8) and (U8, S8)           -> exact integer result, tc in {S32, none}, td = S32,
+ *                                      32-bit two's-complement wrap, no clamp
  * "none" for tc means C == NULL (treated as zero); tc is then ignored.
- * M, N, K : D is M x N; K is the dense depth, K % 32 == 0 (K % 64 == 0 for 8-bit types).
+ * M, N, K : D is M x N; K is the dense depth, K % 32 == 0.
  * values  : device, M x K/2 of ta (ldv >= K/2), from sp24_compress.
  * meta    : device, the image sp24_meta_prepare wrote for (ta, M, K).
  * B       : device, K x N of tb, row-major (ldb >= N).
  * C       : device or NULL, M x N of tc (ldc >= N).      D : device, M x N of td (ldd >= N).
- * Accumulation: floats in f32 on the tensor cores; D (BF16) is the f32 result rounded
- * to nearest-even; integer inputs are exact in 32-bit two's complement.
- * Alignment: values, B, C, D 16-byte aligned, every row pitch a multiple of 16 bytes.
+ * workspace, workspace_bytes : device scratch of at least sp24_mma_workspace_bytes(),
+ *           16-byte aligned, owned by the caller and used only by this call's kernels
+ *           (integer operands only; NULL / 0 otherwise).
+ * Accumulation: floats in f32 on the tensor cores; a BF16 D is the f32 result rounded to
+ * nearest-even.  Integers are widened to bf16 (exact) and accumulated in f32 in chunks of
+ * 1024 dense K (every chunk sum is an exact integer below 2^24), the chunks then summed in
+ * int32: the result is exact.
+ * Alignment: values, meta, B, C, D 16-byte aligned, every row pitch a multiple of 16 bytes.
  * Device status: SP24_DEV_TIMEOUT if a pipeline wait gave up (D is then invalid).
  */
 sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
                      int64_t M, int64_t N, int64_t K, const void *values, int64_t ldv,
                      const void *meta, const void *B, int64_t ldb, const void *C,
-                     int64_t ldc, void *D, int64_t ldd, int32_t *d_status, void *stream);
+                     int64_t ldc, void *D, int64_t ldd, void *workspace,
+                     size_t workspace_bytes, int32_t *d_status, void *stream);
 
 /*
  * sp24_diag_wait_timeout -- self-test of the bounded waits every kernel uses.  Launches

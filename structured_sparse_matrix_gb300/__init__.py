@@ -20,7 +20,7 @@ import torch
 
 from . import _build
 
-__all__ = ["lib", "compress", "decompress", "meta_bytes", "meta_prepare", "mma",
+__all__ = ["lib", "compress", "decompress", "meta_bytes", "meta_prepare", "mma", "workspace_bytes",
            "SparseMatrix", "Sp24Error", "DEV_NOT_2_4", "DEV_TIMEOUT", "DTYPE_CODES"]
 
 DTYPE_CODES = {
@@ -33,7 +33,8 @@ DEV_TIMEOUT = 2
 
 # every symbol include/sp24.h declares
 EXPORTS = ("sp24_compress", "sp24_decompress", "sp24_meta_bytes", "sp24_meta_prepare",
-           "sp24_mma", "sp24_diag_wait_timeout", "sp24_status_string", "sp24_version")
+           "sp24_mma_workspace_bytes", "sp24_mma", "sp24_diag_wait_timeout",
+           "sp24_status_string", "sp24_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,9 +66,11 @@ def lib():
             L.sp24_meta_bytes.argtypes = [i32, i64, i64]
             L.sp24_meta_prepare.restype = i32
             L.sp24_meta_prepare.argtypes = [i32, i64, i64, p, i64, p, p]
+            L.sp24_mma_workspace_bytes.restype = ctypes.c_size_t
+            L.sp24_mma_workspace_bytes.argtypes = [i32, i32, i64, i64, i64]
             L.sp24_mma.restype = i32
             L.sp24_mma.argtypes = [i32, i32, i32, i32, i64, i64, i64, p, i64, p, p, i64, p, i64,
-                                   p, i64, p, p]
+                                   p, i64, p, ctypes.c_size_t, p, p]
             L.sp24_diag_wait_timeout.restype = i32
             L.sp24_diag_wait_timeout.argtypes = [p, u64, p]
             L.sp24_status_string.restype = ctypes.c_char_p
@@ -143,19 +146,34 @@ def meta_prepare(index: torch.Tensor, dtype, M: int, K: int, stream=None) -> tor
     return meta
 
 
+def workspace_bytes(a_dtype, b_dtype, M: int, N: int, K: int) -> int:
+    """Device workspace sp24_mma needs (non-zero only for 8-bit integer operands)."""
+    return int(lib().sp24_mma_workspace_bytes(_code(a_dtype), _code(b_dtype), M, N, K))
+
+
 def mma(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
-        out_dtype=torch.float32, out: torch.Tensor | None = None,
+        out_dtype=None, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
         status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """D = expand(values, meta) @ B + C  (values M x K/2, B K x N, C/D M x N)."""
+    """D = expand(values, meta) @ B + C  (values M x K/2, B K x N, C/D M x N).
+
+    Float operands give f32 (default) or bf16 output; 8-bit integer operands give int32."""
     M = values.shape[0]
     K, N = B.shape
+    integer = values.dtype in (torch.int8, torch.uint8)
     if out is None:
+        if out_dtype is None:
+            out_dtype = torch.int32 if integer else torch.float32
         out = torch.empty((M, N), dtype=out_dtype, device=B.device)
-    tc = _code(C.dtype) if C is not None else _code(torch.float32)
+    tc = _code(C.dtype) if C is not None else _code(out.dtype if integer else torch.float32)
+    ws_bytes = workspace_bytes(values.dtype, B.dtype, M, N, K)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=B.device)
     _check("sp24_mma", lib().sp24_mma(
         _code(values.dtype), _code(B.dtype), tc, _code(out.dtype), M, N, K,
         _ptr(values), _ld(values), _ptr(meta), _ptr(B), _ld(B), _ptr(C),
-        _ld(C) if C is not None else N, _ptr(out), _ld(out), _ptr(status), _stream(stream)))
+        _ld(C) if C is not None else N, _ptr(out), _ld(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream)))
     return out
 
 
@@ -178,6 +196,6 @@ class SparseMatrix:
     def to_dense(self, stream=None):
         return decompress(self.values, self.index, self.K, stream=stream)
 
-    def matmul(self, B, C=None, out_dtype=torch.float32, status=None, stream=None):
+    def matmul(self, B, C=None, out_dtype=None, status=None, stream=None):
         return mma(self.values, self.meta, B, C, out_dtype=out_dtype, status=status,
                    stream=stream)

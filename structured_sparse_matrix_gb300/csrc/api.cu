@@ -168,20 +168,37 @@ sp24_status sp24_meta_prepare(sp24_dtype t, int64_t M, int64_t K, const uint32_t
   return SP24_OK;
 }
 
+size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t N, int64_t K) {
+  if (!is_i8(ta) || tb != SP24_S8 || M < 0 || N < 0 || K < 0) return 0;
+  return int_workspace_bytes(M, N, K);
+}
+
 sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td, int64_t M,
                      int64_t N, int64_t K, const void* values, int64_t ldv, const void* meta,
                      const void* B, int64_t ldb, const void* C, int64_t ldc, void* D,
-                     int64_t ldd, int32_t* d_status, void* stream) {
+                     int64_t ldd, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                     void* stream) {
   const bool f16ish = (ta == SP24_F16 || ta == SP24_BF16);
-  const bool f8 = (ta == SP24_E4M3 || ta == SP24_E5M2);
-  if (!(f16ish || f8) || tb != ta) return SP24_ERR_UNSUPPORTED;
-  if (C != nullptr && tc != SP24_F32) return SP24_ERR_UNSUPPORTED;
-  if (td != SP24_F32 && td != SP24_BF16) return SP24_ERR_UNSUPPORTED;
+  const bool f8 = is_f8(ta);
+  const bool i8 = is_i8(ta);
+  if (f16ish || f8) {
+    if (tb != ta) return SP24_ERR_UNSUPPORTED;
+    if (C != nullptr && tc != SP24_F32) return SP24_ERR_UNSUPPORTED;
+    if (td != SP24_F32 && td != SP24_BF16) return SP24_ERR_UNSUPPORTED;
+  } else if (i8) {
+    if (tb != SP24_S8) return SP24_ERR_UNSUPPORTED;
+    if (C != nullptr && tc != SP24_S32) return SP24_ERR_UNSUPPORTED;
+    if (td != SP24_S32) return SP24_ERR_UNSUPPORTED;
+  } else {
+    return SP24_ERR_UNSUPPORTED;
+  }
   if (M < 0 || N < 0 || K < 0 || (K % 32) != 0) return SP24_ERR_INVALID_ARG;
   if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return SP24_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return SP24_OK;
   if (!D || (K > 0 && (!values || !meta || !B))) return SP24_ERR_INVALID_ARG;
   if (ldd < N || (C && ldc < N) || (K > 0 && (ldv < K / 2 || ldb < N))) return SP24_ERR_INVALID_ARG;
+  if (i8 && K > 0 && (!workspace || workspace_bytes < int_workspace_bytes(M, N, K)))
+    return SP24_ERR_INVALID_ARG;
   const int esz = dtype_bytes(ta);
   const int dsz = dtype_bytes(td);
   if (!aligned16(D) || (ldd * dsz) % 16) return SP24_ERR_ALIGN;
@@ -189,10 +206,11 @@ sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
   if (K > 0 && (!aligned16(values) || !aligned16(meta) || !aligned16(B) || (ldv * esz) % 16 ||
                 (ldb * esz) % 16))
     return SP24_ERR_ALIGN;
+  if (i8 && K > 0 && !aligned16(workspace)) return SP24_ERR_ALIGN;
   int sms = 0;
   if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
   const int rc = launch_spmma(ta, tb, tc, td, M, N, K, values, ldv, meta, B, ldb, C, ldc, D, ldd,
-                              d_status, sms, static_cast<cudaStream_t>(stream));
+                              workspace, d_status, sms, static_cast<cudaStream_t>(stream));
   return static_cast<sp24_status>(rc);
 }
 

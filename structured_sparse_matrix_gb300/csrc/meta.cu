@@ -17,8 +17,9 @@
 //     band b, lane 16b+l holds the halves (h = l/8) of two rows' canonical words:
 //       word = ((w[16b+l%8] >> 16h) & 0xffff) | ((w[16b+l%8+8] >> 16h) & 0xffff) << 16
 //     so nibble q of lane 16b+l is group (q%4)+4h of row 16b+l%8+8(q/4).
-//   kind::f8f6f4 (8-bit types, 64 dense K per MMA, two words per lane): lane = row,
+//   kind::f8f6f4 (FP8 types, 64 dense K per MMA, two words per lane): lane = row,
 //     words 0 and 1 = the row's two canonical words of that K range, unchanged.
+//   8-bit integer types run widened to bf16 on kind::f16 and use its layout.
 // The image covers M rounded up to a multiple of 256 and K to a multiple of the stage;
 // rows beyond M, words beyond K/32 and the unused words of each 16-byte row hold
 // 0x44444444 (pattern {0,1} in every group).  The matching values are zero, so they add
@@ -72,10 +73,10 @@ cudaError_t launch_meta_prepare(const MetaArgs& a, int dtype, int num_sms, cudaS
   int64_t want = (words + 255) / 256;
   int64_t cap = int64_t(num_sms) * 8;
   const int grid = int(want < cap ? (want > 0 ? want : 1) : cap);
-  if (dtype_bytes(dtype) == 2)
-    meta_kernel<false><<<grid, 256, 0, s>>>(a);
-  else
+  if (is_f8(dtype))
     meta_kernel<true><<<grid, 256, 0, s>>>(a);
+  else
+    meta_kernel<false><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

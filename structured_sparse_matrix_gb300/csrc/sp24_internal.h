@@ -19,17 +19,20 @@ inline int dtype_bytes(int t) {
   }
 }
 inline bool is_ab_type(int t) { return t >= kF16 && t <= kU8; }
+inline bool is_f8(int t) { return t == kE4M3 || t == kE5M2; }
+inline bool is_i8(int t) { return t == kS8 || t == kU8; }
 
 // ---- sparse-GEMM K-step geometry (one pipeline stage) shared by meta.cu and spmma.cu
 // 16-bit operands: 128 dense K per stage = 4 MMAs of K=32, metadata one TMEM column
-// per MMA; 8-bit operands: 256 dense K per stage = 4 MMAs of K=64, two columns per MMA.
+// per MMA; FP8 operands: 256 dense K per stage = 4 MMAs of K=64, two columns per MMA.
+// 8-bit integers run widened to bf16 on the 16-bit path, so they use its geometry.
 // In both cases a stage of compressed A is 128 rows x 128 bytes, and the stage's
 // metadata is one [128 lanes][4 words] block per MMA (the MMA's words first), the
 // source of one tcgen05.cp.128x128b into the MMA's column-aligned TMEM slot.
 constexpr int kBM = 128;
 constexpr int kMmasPerStage = 4;
 constexpr int kMetaBlockBytes = kBM * 16;  // one [128][4-word] block = one tcgen05.cp
-inline int stage_k(int t) { return dtype_bytes(t) == 2 ? 128 : 256; }
+inline int stage_k(int t) { return is_f8(t) ? 256 : 128; }
 inline int64_t meta_stage_bytes(int) { return int64_t(kMmasPerStage) * kMetaBlockBytes; }
 // The image covers whole 256-row tile pairs (the CTA-pair GEMM loads both halves).
 inline int64_t meta_mtiles(int64_t M) { return 2 * ((M + 2 * kBM - 1) / (2 * kBM)); }
@@ -60,12 +63,22 @@ struct MetaArgs {
 cudaError_t launch_compress(const CompressArgs& a, int dtype, int mode, int num_sms, cudaStream_t s);
 cudaError_t launch_decompress(const DecompressArgs& a, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_meta_prepare(const MetaArgs& a, int dtype, int num_sms, cudaStream_t s);
+// rows x cols 8-bit integers (pitch ld_src bytes) -> bfloat16 (pitch ld_dst elements)
+cudaError_t launch_widen(const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
+                         int64_t rows, int64_t cols, bool is_signed, int num_sms,
+                         cudaStream_t s);
+
+// Integer operands are widened to bf16 into a caller-provided workspace: A_c (M x K/2)
+// then B (K x N, pitch rounded up to 8 elements).  Returns its size in bytes (0 for
+// float operands).
+int64_t int_ws_ldb(int64_t N);
+size_t int_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 // returns 0 on success, else an sp24_status value
 int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K,
                  const void* values, int64_t ldv, const void* meta, const void* B, int64_t ldb,
-                 const void* C, int64_t ldc, void* D, int64_t ldd, int32_t* status,
-                 int num_sms, cudaStream_t s);
+                 const void* C, int64_t ldc, void* D, int64_t ldd, void* workspace,
+                 int32_t* status, int num_sms, cudaStream_t s);
 
 // device properties of the current device, cached; returns false if not sm_103
 bool current_device(int* num_sms);

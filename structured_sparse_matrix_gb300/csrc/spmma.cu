@@ -45,6 +45,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = 128 * 128;  // one stage of compressed A: 128 rows x 128 bytes
 constexpr int kBColsPerCta = 128;   // B columns staged by each CTA per stage
 constexpr int kSlotCols = 16;       // TMEM columns per MMA metadata slot (aligned)
+// Integer mode: 8-bit integers widened to bf16 are exact, every product |a b| <= 255 * 128,
+// so 512 non-zero products (1024 dense K = 8 bf16 stages) sum to less than 2^24 and the
+// f32 accumulator of one such chunk holds an exact integer.  The epilogue adds the chunks
+// in int32 (two's-complement wrap).
+constexpr int kIntChunkStages = 8;
 
 struct MmaParams {
   const void* C;
@@ -137,7 +142,45 @@ __device__ __forceinline__ void store_chunk(float (&v)[32], const MmaParams& p, 
   }
 }
 
-// OUT: 0 = f32 output, 1 = bf16 output.  C (nullable) is f32.
+// Integer epilogue for one 32-column chunk: D = sum + C (s32, nullable), wrapping.
+__device__ __forceinline__ void store_chunk_s32(const uint32_t* v, const MmaParams& p, int row,
+                                                int col0) {
+  uint32_t o[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) o[j] = v[j];
+  const bool full = col0 + 32 <= p.N;
+  if (p.C != nullptr) {
+    const int32_t* crow = static_cast<const int32_t*>(p.C) + int64_t(row) * p.ldc + col0;
+    if (full) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const int4 cv = __ldcs(reinterpret_cast<const int4*>(crow + j));
+        o[j] += uint32_t(cv.x);
+        o[j + 1] += uint32_t(cv.y);
+        o[j + 2] += uint32_t(cv.z);
+        o[j + 3] += uint32_t(cv.w);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < p.N) o[j] += uint32_t(crow[j]);
+    }
+  }
+  int32_t* drow = static_cast<int32_t*>(p.D) + int64_t(row) * p.ldd + col0;
+  if (full) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+      __stcs(reinterpret_cast<int4*>(drow + j),
+             make_int4(int(o[j]), int(o[j + 1]), int(o[j + 2]), int(o[j + 3])));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (col0 + j < p.N) drow[j] = int32_t(o[j]);
+  }
+}
+
+// OUT: 0 = f32 output, 1 = bf16 output, 2 = s32 output (integer mode, single variant).
+// C (nullable) is f32 for float outputs, s32 for integer mode.
 template <int ESZ, int OUT, bool kPair>
 __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
     spmma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -238,17 +281,33 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
       const uint64_t adesc_hi = smem_desc_hi(16, 1024, 2);
       const uint64_t bdesc_hi = smem_desc_hi(G::kAtomBytes, 1024, 2);
       const uint64_t mdesc_hi = smem_desc_hi(0, 128, 0);
-      int q = 0, local = 0;
+      int q = 0, local = 0, chunk = 0;
       for (int t = unit; t < ntiles_total && !*abort; t += nunits, ++local) {
-        const int abuf = kPair ? 0 : (local & 1);
-        const int use = kPair ? local : (local >> 1);  // earlier uses of this buffer
-        if (!mbar_wait(&acc_empty[abuf], (use & 1) ^ 1u, abort, p.limit_ns)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + uint32_t(abuf * G::kTileN);
         bool ok = true;
+        int abuf = 0;
+        uint32_t d_tmem = tmem;
+        if constexpr (OUT != 2) {
+          abuf = kPair ? 0 : (local & 1);
+          const int use = kPair ? local : (local >> 1);  // earlier uses of this buffer
+          if (!mbar_wait(&acc_empty[abuf], (use & 1) ^ 1u, abort, p.limit_ns)) break;
+          tc_fence_after();
+          d_tmem = tmem + uint32_t(abuf * G::kTileN);
+        }
         for (int kb = 0; kb < p.num_kb; ++kb, ++q) {
           const int s = q % kStages;
           const uint32_t par = (q / kStages) & 1;
+          const int kc = kb % kIntChunkStages;  // stage within an integer chunk
+          if constexpr (OUT == 2) {
+            if (kc == 0) {  // new chunk: next accumulator buffer
+              abuf = chunk & 1;
+              if (!mbar_wait(&acc_empty[abuf], ((chunk >> 1) & 1) ^ 1u, abort, p.limit_ns)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              d_tmem = tmem + uint32_t(abuf * G::kTileN);
+            }
+          }
           if (!mbar_wait(&full_bar[s], par, abort, p.limit_ns)) {
             ok = false;
             break;
@@ -267,12 +326,13 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
           const uint32_t a_saddr = smem_addr(sA + s * kABytes);
           const uint32_t b_saddr = smem_addr(sB + s * G::kBBytes);
           const int k0 = kb * G::kStageK;
+          const int first = (OUT == 2) ? kc : kb;  // accumulate unless the chunk/tile starts
 #pragma unroll
           for (int j = 0; j < G::kMmas; ++j) {
             if (k0 + j * G::kMmaK < p.K) {
               const uint64_t ad = smem_desc(a_saddr + 32 * j, adesc_hi);
               const uint64_t bd = smem_desc(b_saddr + j * G::kMmaK * 128, bdesc_hi);
-              const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+              const uint32_t acc = (first > 0 || j > 0) ? 1u : 0u;
               if constexpr (kPair)
                 tc_mma_sp_pair<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, idesc, acc);
               else
@@ -283,12 +343,20 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
             tc_commit_pair_mc(&empty_bar[s], 3);
           else
             tc_commit(&empty_bar[s]);
+          if constexpr (OUT == 2) {
+            if (kc == kIntChunkStages - 1 || kb == p.num_kb - 1) {  // chunk done
+              tc_commit(&acc_full[abuf]);
+              ++chunk;
+            }
+          }
         }
         if (!ok) break;
-        if constexpr (kPair)
-          tc_commit_pair_mc(&acc_full[abuf], 3);
-        else
-          tc_commit(&acc_full[abuf]);
+        if constexpr (OUT != 2) {
+          if constexpr (kPair)
+            tc_commit_pair_mc(&acc_full[abuf], 3);
+          else
+            tc_commit(&acc_full[abuf]);
+        }
       }
       // every MMA issued by this thread completes before TMEM can be released
       if constexpr (kPair)
@@ -303,16 +371,56 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
     const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 (hardware rule: warp id % 4)
     const uint32_t acc_empty_addr =
         kPair ? mapa(&acc_empty[0], 0) : smem_addr(&acc_empty[0]);
-    int local = 0;
+    int local = 0, ichunk = 0;
     for (int t = unit; t < ntiles_total; t += nunits, ++local) {
       const int mt = t % p.mtiles, nt = t / p.mtiles;
       const int abuf = kPair ? 0 : (local & 1);
       const int use = kPair ? local : (local >> 1);
-      if (!mbar_wait(&acc_full[abuf], use & 1, abort, p.limit_ns)) break;
-      tc_fence_after();
+      if constexpr (OUT != 2) {
+        if (!mbar_wait(&acc_full[abuf], use & 1, abort, p.limit_ns)) break;
+        tc_fence_after();
+      }
       const int row = mt * G::kTileM + int(rank) * 128 + quad * 32 + lane;
       const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16) + uint32_t(abuf * G::kTileN);
-      if constexpr (kPair) {
+      if constexpr (OUT == 2) {
+        // integer mode: one f32 chunk per 1024 dense K, summed exactly in int32
+        // (single variant: 4 epilogue warps, each thread one row x 128 columns)
+        (void)abuf;
+        uint32_t sum[128];
+#pragma unroll
+        for (int j = 0; j < 128; ++j) sum[j] = 0u;
+        const int nch = (p.num_kb + kIntChunkStages - 1) / kIntChunkStages;
+        bool ok = true;
+        for (int c = 0; c < nch; ++c, ++ichunk) {
+          const int b = ichunk & 1;
+          if (!mbar_wait(&acc_full[b], (ichunk >> 1) & 1, abort, p.limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t base = tmem + (uint32_t(quad * 32) << 16) + uint32_t(b * G::kTileN);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t r[32];
+            tc_ld_32x32b_x32(base + uint32_t(q4 * 32), r);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              sum[q4 * 32 + j] += uint32_t(__float2int_rn(__uint_as_float(r[j])));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(b * sizeof(uint64_t)));
+        }
+        if (!ok) break;
+        if (row < p.M) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col0 = nt * G::kTileN + c * 32;
+            if (col0 < p.N) store_chunk_s32(&sum[c * 32], p, row, col0);
+          }
+        }
+      } else if constexpr (kPair) {
         // drain this warp's 32 rows x 128 columns, free the accumulator, then store
         const int half = ew >> 2;
         uint32_t r[4][32];
@@ -470,12 +578,19 @@ int dispatch(const MmaParams& p, const void* values, int64_t ldv, const void* me
 
 }  // namespace
 
+int64_t int_ws_ldb(int64_t N) { return (N + 7) / 8 * 8; }
+
+size_t int_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int64_t a = (M * (K / 2) * 2 + 255) / 256 * 256;
+  const int64_t b = K * int_ws_ldb(N) * 2;
+  return size_t(a + b);
+}
+
 int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K,
                  const void* values, int64_t ldv, const void* meta, const void* B, int64_t ldb,
-                 const void* C, int64_t ldc, void* D, int64_t ldd, int32_t* status,
-                 int num_sms, cudaStream_t s) {
+                 const void* C, int64_t ldc, void* D, int64_t ldd, void* workspace,
+                 int32_t* status, int num_sms, cudaStream_t s) {
   (void)tc;
-  const int esz = dtype_bytes(ta);
   MmaParams p;
   p.C = C;
   p.D = D;
@@ -488,6 +603,23 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   p.mtiles = p.ntiles = 0;
   p.num_kb = int((K + stage_k(ta) - 1) / stage_k(ta));
   p.limit_ns = 1000000000ull;  // 1 s per wait
+  if (is_i8(ta)) {
+    // integers: widen both operands to bf16 (exact) and run the bf16 tensor path with
+    // chunked integer accumulation; 128 x 128 tiles with double-buffered accumulators
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint8_t* wa = ws;
+    uint8_t* wb = ws + (M * (K / 2) * 2 + 255) / 256 * 256;
+    const int64_t ldbw = int_ws_ldb(N);
+    if (K > 0) {
+      if (launch_widen(values, ldv, wa, K / 2, M, K / 2, ta == kS8, num_sms, s) != cudaSuccess ||
+          launch_widen(B, ldb, wb, ldbw, K, N, tb == kS8, num_sms, s) != cudaSuccess)
+        return 4;
+    }
+    // kind::f16 with bf16 operands: type code 1 for A and B
+    return run<2, 2, false>(p, wa, K / 2, meta, wb, ldbw, idesc_sparse_f32(1, 1, 128, 128),
+                            num_sms, s);
+  }
+  const int esz = dtype_bytes(ta);
   // kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2
   const uint32_t at = (ta == kBF16 || ta == kE5M2) ? 1u : 0u;
   const uint32_t bt = (tb == kBF16 || tb == kE5M2) ? 1u : 0u;

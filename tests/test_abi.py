@@ -57,6 +57,8 @@ def test_meta_bytes_host_only():
     assert L.sp24_meta_bytes(F16, 64, 128) == 2 * 8192
     assert L.sp24_meta_bytes(F16, 129, 160) == 2 * 2 * 8192
     assert L.sp24_meta_bytes(E4M3, 8192, 8192) == 64 * 32 * 8192
+    # 8-bit integers use the 16-bit layout (their product runs on the bf16 path)
+    assert L.sp24_meta_bytes(S8, 8192, 8192) == 64 * 64 * 8192
     assert L.sp24_meta_bytes(F16, 64, 100) == 0      # K % 32 != 0
     assert L.sp24_meta_bytes(F32, 64, 128) == 0      # not an operand type
 
@@ -84,9 +86,9 @@ def test_compress_argument_checks():
 
 
 def _mma(ta=BF16, tb=BF16, tc=F32, td=F32, M=128, N=128, K=128, values=FAKE, ldv=64, meta=FAKE,
-         B=FAKE, ldb=128, C=FAKE, ldc=128, D=FAKE, ldd=128):
+         B=FAKE, ldb=128, C=FAKE, ldc=128, D=FAKE, ldd=128, ws=None, ws_bytes=0):
     return sp.lib().sp24_mma(ta, tb, tc, td, M, N, K, values, ldv, meta, B, ldb, C, ldc, D, ldd,
-                             None, None)
+                             ws, ws_bytes, None, None)
 
 
 def test_mma_argument_checks():
@@ -95,6 +97,16 @@ def test_mma_argument_checks():
     assert _mma(td=S32) == UNSUPPORTED
     assert _mma(tc=S32) == UNSUPPORTED
     assert _mma(ta=F32, tb=F32) == UNSUPPORTED
+    assert _mma(ta=S8, tb=U8, tc=S32, td=S32) == UNSUPPORTED      # B must be signed
+    assert _mma(ta=U8, tb=S8, tc=S32, td=F32) == UNSUPPORTED      # integers give s32
+    assert _mma(ta=S8, tb=S8, tc=F32, td=S32) == UNSUPPORTED      # C must be s32
+    # integer operands need the workspace
+    assert _mma(ta=S8, tb=S8, tc=S32, td=S32) == INVALID
+    need = sp.lib().sp24_mma_workspace_bytes(S8, S8, 128, 128, 128)
+    assert need == 128 * 64 * 2 + 128 * 128 * 2
+    assert _mma(ta=S8, tb=S8, tc=S32, td=S32, ws=FAKE, ws_bytes=need - 16) == INVALID
+    assert _mma(ta=S8, tb=S8, tc=S32, td=S32, ws=FAKE_ODD, ws_bytes=need) == ALIGN
+    assert sp.lib().sp24_mma_workspace_bytes(BF16, BF16, 128, 128, 128) == 0
     assert _mma(K=48) == INVALID
     assert _mma(N=-3) == INVALID
     assert _mma(D=None) == INVALID

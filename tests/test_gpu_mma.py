@@ -135,3 +135,48 @@ def test_config3_full_size_fp8(fmt):
 def test_config5_llm_layer(N):
     c = inputs.config5(N=N)
     run_case(c, mode="magnitude", out_dtype=torch.bfloat16, rows=sample_rows(c["M"]))
+
+
+# ---- 8-bit integers: exact, through the bf16 path with chunked int32 accumulation ----------
+
+@pytest.mark.parametrize("ta", ["s8", "u8"])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 192, 1056), (33, 48, 2080),
+                                   (257, 272, 320)])
+def test_int8_small_ragged_exact(ta, M, N, K):
+    c = inputs.case(ta, "s8", M, N, K, seed=M + K, dist="full", tc="s32")
+    run_case(c, mode="mask", out_dtype=torch.int32)
+
+
+@pytest.mark.parametrize("ta,aval", [("s8", -128), ("u8", 255)])
+def test_int8_extreme_values_many_chunks(ta, aval):
+    # every kept a at its extreme and every b = -128: the largest |a b| terms; K = 4096
+    # spans four 1024-K chunks and each output is -2048 * |a| * 128, far beyond 2^24
+    M, N, K = 128, 144, 4096
+    m = inputs.keep_mask(M, K, inputs.gen(5))
+    Ai = torch.where(m, torch.full((M, K), aval), torch.zeros((M, K), dtype=torch.long))
+    A = Ai.to(torch.int8 if ta == "s8" else torch.uint8)
+    B = torch.full((K, N), -128, dtype=torch.int8)
+    C = torch.full((M, N), -(1 << 20), dtype=torch.int32)
+    c = {"A": A, "mask": m, "B": B, "C": C, "ta": ta, "tb": "s8", "tc": "s32",
+         "M": M, "N": N, "K": K}
+    Dg, Dref, _ = run_case(c, mode="mask", out_dtype=torch.int32)
+    assert int(np.abs(Dref).max()) > (1 << 24)
+
+
+def test_int8_wraps_like_int32():
+    # C near the int32 limit: the result wraps modulo 2^32 (no clamp)
+    M, N, K = 128, 128, 64
+    m = inputs.keep_mask(M, K, None, fixed=(0, 1))
+    A = torch.where(m, torch.full((M, K), 127), torch.zeros((M, K), dtype=torch.long)).to(torch.int8)
+    B = torch.full((K, N), 127, dtype=torch.int8)
+    C = torch.full((M, N), 2**31 - 1000, dtype=torch.int32)
+    c = {"A": A, "mask": m, "B": B, "C": C, "ta": "s8", "tb": "s8", "tc": "s32",
+         "M": M, "N": N, "K": K}
+    Dg, Dref, _ = run_case(c, mode="mask", out_dtype=torch.int32)
+    assert int(Dref.max()) > 2**31 - 1 and int(Dg.min()) < 0
+
+
+@pytest.mark.parametrize("ta", ["s8", "u8"])
+def test_config4_full_size_int8(ta):
+    c = inputs.config4(ta)
+    run_case(c, mode="mask", out_dtype=torch.int32, rows=sample_rows(c["M"])[::4])
