@@ -64,7 +64,8 @@ typedef enum sp24_status {
     SP24_ERR_CUDA = 4,        /* CUDA runtime or driver error while enqueueing      */
     SP24_ERR_TIMEOUT = 5,     /* reserved: the device reports timeouts via SP24_DEV_TIMEOUT */
     SP24_ERR_NOT_2_4 = 6,     /* reserved: the device reports this via SP24_DEV_NOT_2_4     */
-    SP24_ERR_NO_DEVICE = 7    /* no sm_103 device is current                        */
+    SP24_ERR_NO_DEVICE = 7,   /* no sm_103 device is current                        */
+    SP24_ERR_SCRATCH_TOO_SMALL = 8 /* the problem needs more than the built-in scratch */
 } sp24_status;
 
 /* How sp24_compress chooses the two kept positions of each group of four. */
@@ -186,6 +187,33 @@ sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
  * faulting or hanging GPU.
  */
 sp24_status sp24_diag_wait_timeout(int32_t *d_status, uint64_t limit_ns, void *stream);
+
+/* Bytes of the fixed device scratch array sp24_mma_i8_noalloc uses (16 MiB). */
+#define SP24_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * sp24_mma_i8_noalloc -- the 8-bit integer form of sp24_mma without a workspace argument.
+ * The source pages have no counterpart; this entry point exists for callers that cannot
+ * allocate device memory at the point of the call: for example a plugin inside a host
+ * framework that owns all device memory and hands out no workspace, or a caller with a
+ * fixed memory plan that forbids allocations after start-up (cudaMalloc may also
+ * synchronise the device).  It allocates nothing and calls no allocating routine.
+ *
+ * Arguments, types and results are those of sp24_mma for (S8, S8) and (U8, S8) operands
+ * (tc in {S32, none}, td = S32).  The scratch for the operands widened to bf16 is a device
+ * array of SP24_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that loads it
+ * until the process exits; a problem needing more than that (sp24_mma_workspace_bytes())
+ * returns SP24_ERR_SCRATCH_TOO_SMALL and enqueues nothing.  All calls share the array and
+ * each call writes what it uses before reading it; calls whose work overlaps on the GPU
+ * (no stream ordering between them) race on it.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.
+ */
+sp24_status sp24_mma_i8_noalloc(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
+                                int64_t M, int64_t N, int64_t K, const void *values,
+                                int64_t ldv, const void *meta, const void *B, int64_t ldb,
+                                const void *C, int64_t ldc, void *D, int64_t ldd,
+                                int32_t *d_status, void *stream);
 
 /* Static description of a status code (never NULL). */
 const char *sp24_status_string(sp24_status s);

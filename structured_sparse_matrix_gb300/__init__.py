@@ -33,8 +33,8 @@ DEV_TIMEOUT = 2
 
 # every symbol include/sp24.h declares
 EXPORTS = ("sp24_compress", "sp24_decompress", "sp24_meta_bytes", "sp24_meta_prepare",
-           "sp24_mma_workspace_bytes", "sp24_mma", "sp24_diag_wait_timeout",
-           "sp24_status_string", "sp24_version")
+           "sp24_mma_workspace_bytes", "sp24_mma", "sp24_mma_i8_noalloc",
+           "sp24_diag_wait_timeout", "sp24_status_string", "sp24_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +71,9 @@ def lib():
             L.sp24_mma.restype = i32
             L.sp24_mma.argtypes = [i32, i32, i32, i32, i64, i64, i64, p, i64, p, p, i64, p, i64,
                                    p, i64, p, ctypes.c_size_t, p, p]
+            L.sp24_mma_i8_noalloc.restype = i32
+            L.sp24_mma_i8_noalloc.argtypes = [i32, i32, i32, i32, i64, i64, i64, p, i64, p, p,
+                                              i64, p, i64, p, i64, p, p]
             L.sp24_diag_wait_timeout.restype = i32
             L.sp24_diag_wait_timeout.argtypes = [p, u64, p]
             L.sp24_status_string.restype = ctypes.c_char_p
@@ -174,6 +177,23 @@ def mma(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor, C: torch.Tens
         _ld(C) if C is not None else N, _ptr(out), _ld(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream)))
+    return out
+
+
+def mma_i8_noalloc(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor,
+                   C: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                   status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The 8-bit integer product through sp24_mma_i8_noalloc: no workspace is passed, the
+    library's fixed scratch array is used (for callers that cannot allocate; see the
+    header).  Only the output tensor is allocated here, and only if `out` is None."""
+    M = values.shape[0]
+    K, N = B.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.int32, device=B.device)
+    _check("sp24_mma_i8_noalloc", lib().sp24_mma_i8_noalloc(
+        _code(values.dtype), _code(B.dtype), _code(torch.int32), _code(out.dtype), M, N, K,
+        _ptr(values), _ld(values), _ptr(meta), _ptr(B), _ld(B), _ptr(C),
+        _ld(C) if C is not None else N, _ptr(out), _ld(out), _ptr(status), _stream(stream)))
     return out
 
 

@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsp24.so")
-SOURCES = ["api.cu", "compress.cu", "convert.cu", "meta.cu", "spmma.cu"]
+SOURCES = ["api.cu", "compress.cu", "convert.cu", "meta.cu", "noalloc.cu", "spmma.cu"]
 HEADERS = ["sp24_device.cuh", "sp24_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -72,6 +72,7 @@ const char* sp24_status_string(sp24_status s) {
     case SP24_ERR_TIMEOUT: return "device wait timed out";
     case SP24_ERR_NOT_2_4: return "input is not 2:4 sparse";
     case SP24_ERR_NO_DEVICE: return "no sm_103 device is current";
+    case SP24_ERR_SCRATCH_TOO_SMALL: return "problem needs more than the built-in scratch array";
     default: return "unknown status";
   }
 }
