@@ -59,6 +59,13 @@ __device__ __forceinline__ uint32_t pick_from_set(uint32_t keep, bool mask_mode,
   return p0 | (p1 << 2);
 }
 
+// x[i] for a run-time i in 0..3 without indexing memory (keeps x in registers)
+__device__ __forceinline__ uint32_t sel4(const uint32_t (&x)[4], uint32_t i) {
+  const uint32_t lo = (i & 1u) ? x[1] : x[0];
+  const uint32_t hi = (i & 1u) ? x[3] : x[2];
+  return (i & 2u) ? hi : lo;
+}
+
 template <int CLS>
 __device__ __forceinline__ uint32_t pick_magnitude(const uint32_t (&x)[4]) {
   uint32_t k[4];
@@ -77,12 +84,15 @@ __device__ __forceinline__ uint32_t pick_magnitude(const uint32_t (&x)[4]) {
   return p0 | (p1 << 2);
 }
 
-// ESZ = element bytes (2 or 1); MODE = SP24_MODE_* value.
+// ESZ = element bytes (2 or 1); MODE = SP24_MODE_* value.  Each warp step covers kUnroll
+// groups of 32 consecutive chunks; all their loads are issued before any is used, so a
+// thread keeps kUnroll 16-byte loads (plus mask loads) in flight.
 template <int ESZ, int CLS, int MODE>
 __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
   constexpr int kElems = 16 / ESZ;   // elements per 16-byte chunk
   constexpr int kGroups = kElems / 4;  // groups per chunk
   constexpr int kLanesPerWord = 32 / kElems;
+  constexpr int kUnroll = 4;
   const int lane = threadIdx.x & 31;
   const int64_t cpr = a.K / kElems;  // chunks per row
   const int64_t total = a.M * cpr;
@@ -90,81 +100,94 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
   const int64_t warp_stride = (int64_t(gridDim.x) * blockDim.x) >> 5;
   bool any_flag = false;
 
-  for (int64_t base = warp_global * 32; base < total; base += warp_stride * 32) {
-    const int64_t c = base + lane;
-    const bool active = c < total;
-    const int64_t row = active ? c / cpr : 0;
-    const int64_t cc = active ? c - row * cpr : 0;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    uint32_t mbits[4] = {0, 0, 0, 0};
-    if (active) {
-      v = __ldcs(reinterpret_cast<const uint4*>(a.A + row * a.lda_bytes + cc * 16));
-      if constexpr (MODE == 1) {
-        if constexpr (kElems == 8) {
-          uint2 m = __ldcs(reinterpret_cast<const uint2*>(a.mask + row * a.ldm + cc * 8));
-          mbits[0] = m.x;
-          mbits[1] = m.y;
-        } else {
-          uint4 m = __ldcs(reinterpret_cast<const uint4*>(a.mask + row * a.ldm + cc * 16));
-          mbits[0] = m.x;
-          mbits[1] = m.y;
-          mbits[2] = m.z;
-          mbits[3] = m.w;
+  for (int64_t base = warp_global * 32 * kUnroll; base < total;
+       base += warp_stride * 32 * kUnroll) {
+    uint4 v[kUnroll];
+    uint32_t mbits[kUnroll][4];
+    int64_t row[kUnroll], cc[kUnroll];
+    bool active[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t c = base + u * 32 + lane;
+      active[u] = c < total;
+      row[u] = active[u] ? c / cpr : 0;
+      cc[u] = active[u] ? c - row[u] * cpr : 0;
+      v[u] = make_uint4(0, 0, 0, 0);
+      mbits[u][0] = mbits[u][1] = mbits[u][2] = mbits[u][3] = 0;
+      if (active[u]) {
+        v[u] = __ldcs(reinterpret_cast<const uint4*>(a.A + row[u] * a.lda_bytes + cc[u] * 16));
+        if constexpr (MODE == 1) {
+          if constexpr (kElems == 8) {
+            const uint2 m =
+                __ldcs(reinterpret_cast<const uint2*>(a.mask + row[u] * a.ldm + cc[u] * 8));
+            mbits[u][0] = m.x;
+            mbits[u][1] = m.y;
+          } else {
+            const uint4 m =
+                __ldcs(reinterpret_cast<const uint4*>(a.mask + row[u] * a.ldm + cc[u] * 16));
+            mbits[u][0] = m.x;
+            mbits[u][1] = m.y;
+            mbits[u][2] = m.z;
+            mbits[u][3] = m.w;
+          }
         }
       }
     }
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t out[2] = {0, 0};  // kept elements, packed
-    uint32_t nibs = 0;
 #pragma unroll
-    for (int g = 0; g < kGroups; ++g) {
-      uint32_t x[4];
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t out[2] = {0, 0};  // kept elements, packed
+      uint32_t nibs = 0;
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int e = 4 * g + p;  // element index within the chunk
-        if constexpr (ESZ == 2)
-          x[p] = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-        else
-          x[p] = (w[e >> 2] >> (8 * (e & 3))) & 0xFFu;
-      }
-      uint32_t nib;
-      bool flag = false;
-      if constexpr (MODE == 2) {
-        nib = pick_magnitude<CLS>(x);
-      } else {
-        uint32_t keep = 0;
+      for (int g = 0; g < kGroups; ++g) {
+        uint32_t x[4];
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
-          bool k;
-          if constexpr (MODE == 1) {
-            const int e = 4 * g + p;
-            k = ((mbits[e >> 2] >> (8 * (e & 3))) & 0xFFu) != 0u;
-          } else {
-            k = is_nonzero<CLS>(x[p]);
-          }
-          keep |= uint32_t(k) << p;
+          const int e = 4 * g + p;  // element index within the chunk
+          if constexpr (ESZ == 2)
+            x[p] = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+          else
+            x[p] = (w[e >> 2] >> (8 * (e & 3))) & 0xFFu;
         }
-        nib = pick_from_set(keep, MODE == 1, &flag);
-      }
-      any_flag |= (flag && active);
-      const uint32_t k0 = x[nib & 3u], k1 = x[nib >> 2];
-      if constexpr (ESZ == 2) {
-        out[g] = k0 | (k1 << 16);
-      } else {
-        out[g >> 1] |= (k0 | (k1 << 8)) << (16 * (g & 1));
-      }
-      nibs |= nib << (4 * g);
-    }
-    if (active) {
-      __stcs(reinterpret_cast<uint2*>(a.values + row * a.ldv_bytes + cc * 8),
-             make_uint2(out[0], out[1]));
-    }
-    // merge the nibbles of the lanes that share one index word
-    uint32_t word = nibs << ((4 * kGroups) * (lane % kLanesPerWord));
+        uint32_t nib;
+        bool flag = false;
+        if constexpr (MODE == 2) {
+          nib = pick_magnitude<CLS>(x);
+        } else {
+          uint32_t keep = 0;
 #pragma unroll
-    for (int o = 1; o < kLanesPerWord; o <<= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, o);
-    if (active && (lane % kLanesPerWord) == 0) {
-      a.index[row * a.ldi + (cc * kElems) / 32] = word;
+          for (int p = 0; p < 4; ++p) {
+            bool k;
+            if constexpr (MODE == 1) {
+              const int e = 4 * g + p;
+              k = ((mbits[u][e >> 2] >> (8 * (e & 3))) & 0xFFu) != 0u;
+            } else {
+              k = is_nonzero<CLS>(x[p]);
+            }
+            keep |= uint32_t(k) << p;
+          }
+          nib = pick_from_set(keep, MODE == 1, &flag);
+        }
+        any_flag |= (flag && active[u]);
+        const uint32_t k0 = sel4(x, nib & 3u), k1 = sel4(x, nib >> 2);
+        if constexpr (ESZ == 2) {
+          out[g] = k0 | (k1 << 16);
+        } else {
+          out[g >> 1] |= (k0 | (k1 << 8)) << (16 * (g & 1));
+        }
+        nibs |= nib << (4 * g);
+      }
+      if (active[u]) {
+        __stcs(reinterpret_cast<uint2*>(a.values + row[u] * a.ldv_bytes + cc[u] * 8),
+               make_uint2(out[0], out[1]));
+      }
+      // merge the nibbles of the lanes that share one index word
+      uint32_t word = nibs << ((4 * kGroups) * (lane % kLanesPerWord));
+#pragma unroll
+      for (int o = 1; o < kLanesPerWord; o <<= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, o);
+      if (active[u] && (lane % kLanesPerWord) == 0) {
+        a.index[row[u] * a.ldi + (cc[u] * kElems) / 32] = word;
+      }
     }
   }
   if (a.status != nullptr && __any_sync(0xFFFFFFFFu, any_flag) && lane == 0)
@@ -228,8 +251,8 @@ cudaError_t launch_compress(const CompressArgs& a, int dtype, int mode, int num_
                             cudaStream_t s) {
   const int esz = dtype_bytes(dtype);
   const int64_t chunks = a.M * (a.K / (16 / esz));
-  // each thread keeps one 16-byte load in flight per step; 8 resident blocks per SM
-  int64_t want = (chunks + 255) / 256;
+  // each thread covers 4 chunks per step; 8 resident blocks of 256 threads per SM
+  int64_t want = (chunks + 1023) / 1024;
   int64_t cap = int64_t(num_sms) * 8;
   const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
   switch (dtype) {

@@ -39,38 +39,44 @@ __device__ __forceinline__ uint32_t canon(const MetaArgs& a, int64_t row, int64_
   return a.index[row * a.ldi + w];
 }
 
-// one thread per image word; per (tile, stage): [mma j][128 lanes][4 words]
+// One thread per (tile, stage, lane): it reads the canonical words its lane needs and
+// writes the lane's 16-byte row of each of the stage's 4 MMA blocks (coalesced across the
+// lanes of a warp).
 template <bool kEightBit>
 __global__ void __launch_bounds__(256) meta_kernel(MetaArgs a) {
-  const int64_t total = a.mtiles * a.ksteps * kMmasPerStage * 128 * 4;
+  const int64_t total = a.mtiles * a.ksteps * 128;
   for (int64_t o = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; o < total;
        o += int64_t(gridDim.x) * blockDim.x) {
-    const int q = int(o & 3);                 // word within the lane's 16 bytes
-    const int lane = int((o >> 2) & 127);     // TMEM lane
-    const int j = int((o >> 9) & 3);          // MMA within the stage
-    const int64_t blk = o >> 11;              // (mtile, kstep)
+    const int lane = int(o & 127);            // TMEM lane
+    const int64_t blk = o >> 7;               // (mtile, kstep)
     const int64_t mt = blk / a.ksteps, ks = blk % a.ksteps;
-    uint32_t word = kPadWord;
+    uint4* out = reinterpret_cast<uint4*>(a.meta) + blk * (kMmasPerStage * 128) + lane;
     if constexpr (kEightBit) {
-      if (q < 2) word = canon(a, mt * 128 + lane, ks * 8 + j * 2 + q);
-    } else if (q == 0) {
-      const int64_t w = ks * 4 + j;           // canonical word (32 dense K)
+      const int64_t row = mt * 128 + lane;
+#pragma unroll
+      for (int j = 0; j < kMmasPerStage; ++j)
+        out[j * 128] = make_uint4(canon(a, row, ks * 8 + 2 * j), canon(a, row, ks * 8 + 2 * j + 1),
+                                  kPadWord, kPadWord);
+    } else {
       const int band = lane >> 4, l = lane & 15;
       const int64_t rA = mt * 128 + band * 16 + (l & 7);
       const int h = l >> 3;
-      const uint32_t lo = (canon(a, rA, w) >> (16 * h)) & 0xFFFFu;
-      const uint32_t hi = (canon(a, rA + 8, w) >> (16 * h)) & 0xFFFFu;
-      word = lo | (hi << 16);
+#pragma unroll
+      for (int j = 0; j < kMmasPerStage; ++j) {
+        const int64_t w = ks * 4 + j;         // canonical word (32 dense K) of MMA j
+        const uint32_t lo = (canon(a, rA, w) >> (16 * h)) & 0xFFFFu;
+        const uint32_t hi = (canon(a, rA + 8, w) >> (16 * h)) & 0xFFFFu;
+        out[j * 128] = make_uint4(lo | (hi << 16), kPadWord, kPadWord, kPadWord);
+      }
     }
-    a.meta[o] = word;
   }
 }
 
 }  // namespace
 
 cudaError_t launch_meta_prepare(const MetaArgs& a, int dtype, int num_sms, cudaStream_t s) {
-  const int64_t words = a.mtiles * a.ksteps * meta_stage_bytes(dtype) / 4;
-  int64_t want = (words + 255) / 256;
+  const int64_t threads = a.mtiles * a.ksteps * 128;
+  int64_t want = (threads + 255) / 256;
   int64_t cap = int64_t(num_sms) * 8;
   const int grid = int(want < cap ? (want > 0 ? want : 1) : cap);
   if (is_f8(dtype))
