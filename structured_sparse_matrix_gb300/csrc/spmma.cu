@@ -56,6 +56,7 @@ struct MmaParams {
   void* D;
   int64_t ldc, ldd;
   int32_t* status;
+  int c32, d32;  // C / D rows allow 32-byte vector accesses (base and pitch 32-byte aligned)
   int M, N, K;
   int mtiles, ntiles, num_kb;  // tiles of the variant (128 or 256 rows, 128 or 256 cols)
   uint64_t limit_ns;
@@ -85,61 +86,160 @@ struct Geo {
   static_assert(kSmemBytes <= 232448 - 256, "shared memory budget");
 };
 
-// Epilogue for one 32-column chunk of one output row: v += C (f32, nullable), cast, store.
-// Columns at or beyond N are not touched; full chunks use 16-byte vector accesses.
-template <int OUT>
-__device__ __forceinline__ void store_chunk(float (&v)[32], const MmaParams& p, int row, int col0) {
-  const bool full = col0 + 32 <= p.N;
-  if (p.C != nullptr) {
-    const float* crow = static_cast<const float*>(p.C) + int64_t(row) * p.ldc + col0;
-    if (full) {
+// Tile order: bands of kBandRows rows of D, each swept along N, so that the tiles in
+// flight at one time (about one per CTA pair) share a few row blocks of A and column
+// blocks of B that stay in L2 instead of streaming all of A for every column of tiles.
+constexpr int kBandRows = 2048;
+template <int kTileM>
+__device__ __forceinline__ void tile_coords(const MmaParams& p, int t, int& mt, int& nt) {
+  constexpr int kBand = kBandRows / kTileM;  // row tiles per band
+  const int band_tiles = kBand * p.ntiles;
+  const int g = t / band_tiles, r = t - g * band_tiles;
+  const int rest = p.mtiles - g * kBand;
+  const int gm = rest < kBand ? rest : kBand;  // the last band may be shorter
+  mt = g * kBand + r % gm;
+  nt = r / gm;
+}
+
+// Quad transpose (the four threads t with equal t/4 exchange values): thread q = t%4
+// holds, for j = 0..3, the two values at columns 8j + 2q and +1 of a 32-column row
+// segment in v[2j], v[2j+1]; afterwards it holds columns 8q .. 8q+7 in v[0..7].  Two
+// butterfly stages (partners q^1, then q^2), each swapping the two elements whose index
+// bit differs from the thread's.
+__device__ __forceinline__ void quad_transpose(float (&v)[8], int q) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const float4 cv = __ldcs(reinterpret_cast<const float4*>(crow + j));
-        v[j] += cv.x;
-        v[j + 1] += cv.y;
-        v[j + 2] += cv.z;
-        v[j + 3] += cv.w;
+  for (int bit = 1; bit <= 2; bit <<= 1) {
+    const bool up = (q & bit) != 0;
+#pragma unroll
+    for (int j0 = 0; j0 < 4; ++j0) {
+      if (j0 & bit) continue;
+      const int j1 = j0 | bit;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const float send = up ? v[2 * j0 + c] : v[2 * j1 + c];
+        const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, bit);
+        if (up)
+          v[2 * j0 + c] = recv;
+        else
+          v[2 * j1 + c] = recv;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void ld_f32x8(const float* src, bool v32, float (&c)[8]) {
+  if (v32) {
+    asm volatile("ld.global.cs.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3]), "=f"(c[4]), "=f"(c[5]),
+                   "=f"(c[6]), "=f"(c[7])
+                 : "l"(src));
+  } else {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(src));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(src) + 1);
+    c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
+    c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
+  }
+}
+
+// C (f32) at 8 consecutive columns of one output row; zeros beyond M, N or without C.
+__device__ __forceinline__ void load_c8(float (&c)[8], const MmaParams& p, int row, int col) {
+  if (p.C == nullptr || row >= p.M || col >= p.N) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c[j] = 0.f;
+    return;
+  }
+  const float* crow = static_cast<const float*>(p.C) + int64_t(row) * p.ldc + col;
+  if (col + 8 <= p.N) {
+    ld_f32x8(crow, p.c32 != 0, c);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c[j] = col + j < p.N ? crow[j] : 0.f;
+  }
+}
+
+// Cast and store 8 consecutive columns of one output row; columns at or beyond N are not
+// touched.  Each quad of threads covers one 32-column segment of a row, so a warp's
+// store is 8 whole 128-byte lines (f32 output).
+template <int OUT>
+__device__ __forceinline__ void store8(const float (&v)[8], const MmaParams& p, int row, int col) {
+  if (row >= p.M || col >= p.N) return;
+  const bool full = col + 8 <= p.N;
+  if constexpr (OUT == 0) {
+    float* d = static_cast<float*>(p.D) + int64_t(row) * p.ldd + col;
+    if (full) {
+      if (p.d32) {
+        asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(d), "f"(v[0]),
+                     "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                     : "memory");
+      } else {
+        __stcs(reinterpret_cast<float4*>(d), make_float4(v[0], v[1], v[2], v[3]));
+        __stcs(reinterpret_cast<float4*>(d) + 1, make_float4(v[4], v[5], v[6], v[7]));
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (col0 + j < p.N) v[j] += crow[j];
-    }
-  }
-  if constexpr (OUT == 0) {
-    float* drow = static_cast<float*>(p.D) + int64_t(row) * p.ldd + col0;
-    if (full) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        __stcs(reinterpret_cast<float4*>(drow + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (col0 + j < p.N) drow[j] = v[j];
+      for (int j = 0; j < 8; ++j)
+        if (col + j < p.N) d[j] = v[j];
     }
   } else {
-    __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.D) + int64_t(row) * p.ldd + col0;
+    __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + int64_t(row) * p.ldd + col;
     if (full) {
+      __nv_bfloat162 h[4];
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        __nv_bfloat162 h0 = __floats2bfloat162_rn(v[j], v[j + 1]);
-        __nv_bfloat162 h1 = __floats2bfloat162_rn(v[j + 2], v[j + 3]);
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(v[j + 4], v[j + 5]);
-        __nv_bfloat162 h3 = __floats2bfloat162_rn(v[j + 6], v[j + 7]);
-        uint4 u;
-        memcpy(&u.x, &h0, 4);
-        memcpy(&u.y, &h1, 4);
-        memcpy(&u.z, &h2, 4);
-        memcpy(&u.w, &h3, 4);
-        __stcs(reinterpret_cast<uint4*>(drow + j), u);
-      }
+      for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+      uint4 u;
+      memcpy(&u, h, 16);
+      __stcs(reinterpret_cast<uint4*>(d), u);
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (col0 + j < p.N) drow[j] = __float2bfloat16_rn(v[j]);
+      for (int j = 0; j < 8; ++j)
+        if (col + j < p.N) d[j] = __float2bfloat16_rn(v[j]);
     }
   }
+}
+
+// Four 32-column segments (columns col0 .. col0+127) of one output row from a .16x256b
+// fragment r (repetitions 0..15; row half e = 0 is lane t/4, e = 1 lane t/4 + 8): two
+// segments at a time, their C loads issued together, then each segment is transposed
+// across the quad, added to C and stored.
+template <int OUT>
+__device__ __forceinline__ void store_row128(const uint32_t* r, int e, const MmaParams& p,
+                                             int row, int col0, int q) {
+#pragma unroll
+  for (int g0 = 0; g0 < 4; g0 += 2) {
+    float c[2][8];
+#pragma unroll
+    for (int g = 0; g < 2; ++g) load_c8(c[g], p, row, col0 + 32 * (g0 + g) + 8 * q);
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = p.K > 0 ? __uint_as_float(r[4 * (4 * (g0 + g) + j) + 2 * e]) : 0.f;
+        v[2 * j + 1] = p.K > 0 ? __uint_as_float(r[4 * (4 * (g0 + g) + j) + 2 * e + 1]) : 0.f;
+      }
+      quad_transpose(v, q);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] += c[g][j];
+      store8<OUT>(v, p, row, col0 + 32 * (g0 + g) + 8 * q);
+    }
+  }
+}
+
+// Pull this thread's share of the C rows of a coming tile into L2 (the quad leader of
+// each row, one bulk prefetch of up to 512 bytes per row).
+__device__ __forceinline__ void prefetch_c_rows(const MmaParams& p, int row0, int col0, int q) {
+  if (p.C == nullptr || q != 0 || col0 >= p.N) return;
+  const int ncols = p.N - col0 < 128 ? p.N - col0 : 128;
+  const uint32_t bytes = uint32_t(ncols * 4) & ~15u;
+  if (bytes == 0) return;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int row = row0 + 16 * h + 8 * e;
+      if (row < p.M)
+        bulk_prefetch_l2(static_cast<const float*>(p.C) + int64_t(row) * p.ldc + col0, bytes);
+    }
 }
 
 // Integer epilogue for one 32-column chunk: D = sum + C (s32, nullable), wrapping.
@@ -242,7 +342,8 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
     if (lane == 0) {
       int q = 0;
       for (int t = unit; t < ntiles_total && !*abort; t += nunits) {
-        const int mt = t % p.mtiles, nt = t / p.mtiles;
+        int mt, nt;
+        tile_coords<G::kTileM>(p, t, mt, nt);
         const int mt128 = kPair ? mt * 2 + int(rank) : mt;  // this CTA's 128-row tile
         const int bcol = nt * G::kTileN + int(rank) * kBColsPerCta;
         for (int kb = 0; kb < p.num_kb; ++kb, ++q) {
@@ -373,7 +474,8 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
         kPair ? mapa(&acc_empty[0], 0) : smem_addr(&acc_empty[0]);
     int local = 0, ichunk = 0;
     for (int t = unit; t < ntiles_total; t += nunits, ++local) {
-      const int mt = t % p.mtiles, nt = t / p.mtiles;
+      int mt, nt;
+      tile_coords<G::kTileM>(p, t, mt, nt);
       const int abuf = kPair ? 0 : (local & 1);
       const int use = kPair ? local : (local >> 1);
       if constexpr (OUT != 2) {
@@ -423,38 +525,44 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
       } else if constexpr (kPair) {
         // drain this warp's 32 rows x 128 columns, free the accumulator, then store
         const int half = ew >> 2;
-        uint32_t r[4][32];
+        uint32_t r[2][64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(lane_base + uint32_t(half * 128 + c * 32), r[c]);
+        for (int h = 0; h < 2; ++h)
+          tc_ld_16x256b_x16(lane_base + (uint32_t(16 * h) << 16) + uint32_t(half * 128), r[h]);
         tc_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(abuf * sizeof(uint64_t)));
-        if (row < p.M) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int col0 = nt * G::kTileN + half * 128 + c * 32;
-            if (col0 < p.N) {
-              float v[32];
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = p.K > 0 ? __uint_as_float(r[c][j]) : 0.f;
-              store_chunk<OUT>(v, p, row, col0);
-            }
-          }
+        const int row0 = mt * G::kTileM + int(rank) * 128 + quad * 32 + (lane >> 2);
+        const int col0 = nt * G::kTileN + half * 128;
+        if (t + nunits < ntiles_total) {  // the next tile's C, needed one mainloop from now
+          int mt2, nt2;
+          tile_coords<G::kTileM>(p, t + nunits, mt2, nt2);
+          prefetch_c_rows(p, mt2 * G::kTileM + int(rank) * 128 + quad * 32 + (lane >> 2),
+                          nt2 * G::kTileN + half * 128, lane & 3);
         }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            store_row128<OUT>(r[h], e, p, row0 + 16 * h + 8 * e, col0, lane & 3);
       } else {
-#pragma unroll 1
-        for (int c = 0; c < G::kTileN / 32; ++c) {
-          uint32_t r[32];
-          tc_ld_32x32b_x32(lane_base + uint32_t(c * 32), r);
-          tc_wait_ld();
-          const int col0 = nt * G::kTileN + c * 32;
-          if (row >= p.M || col0 >= p.N) continue;
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = p.K > 0 ? __uint_as_float(r[j]) : 0.f;
-          store_chunk<OUT>(v, p, row, col0);
+        const int row0 = mt * G::kTileM + quad * 32 + (lane >> 2);
+        if (t + nunits < ntiles_total) {  // the next tile's C, needed one mainloop from now
+          int mt2, nt2;
+          tile_coords<G::kTileM>(p, t + nunits, mt2, nt2);
+          prefetch_c_rows(p, mt2 * G::kTileM + quad * 32 + (lane >> 2), nt2 * G::kTileN, lane & 3);
         }
+        uint32_t r[2][64];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tc_ld_16x256b_x16(lane_base + (uint32_t(16 * h) << 16), r[h]);
+        tc_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            store_row128<OUT>(r[h], e, p, row0 + 16 * h + 8 * e, nt * G::kTileN, lane & 3);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(abuf * sizeof(uint64_t)));
@@ -597,6 +705,9 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   p.ldc = ldc;
   p.ldd = ldd;
   p.status = status;
+  // 32-byte vector accesses need a 32-byte aligned base and pitch (the ABI promises 16)
+  p.c32 = (reinterpret_cast<uintptr_t>(C) % 32 == 0 && (ldc * 4) % 32 == 0) ? 1 : 0;
+  p.d32 = (reinterpret_cast<uintptr_t>(D) % 32 == 0 && (ldd * 4) % 32 == 0) ? 1 : 0;
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
