@@ -24,81 +24,163 @@ namespace {
 // element classes: how "zero" and "|x|" are read from the stored bits
 enum ElemClass { kFloat16 = 0, kFloat8 = 1, kSigned8 = 2, kUnsigned8 = 3 };
 
-template <int CLS>
-__device__ __forceinline__ uint32_t magnitude_key(uint32_t b) {
-  if constexpr (CLS == kFloat16) return b & 0x7FFFu;  // sign cleared: orders |x|
-  if constexpr (CLS == kFloat8) return b & 0x7Fu;
-  if constexpr (CLS == kSigned8) {
-    int v = static_cast<int8_t>(static_cast<uint8_t>(b));
-    return static_cast<uint32_t>(v < 0 ? -v : v);
-  }
-  return b & 0xFFu;
-}
-
-template <int CLS>
-__device__ __forceinline__ bool is_nonzero(uint32_t b) {
-  if constexpr (CLS == kFloat16) return (b & 0x7FFFu) != 0u;  // +0 and -0 are zero
-  if constexpr (CLS == kFloat8) return (b & 0x7Fu) != 0u;
-  return (b & 0xFFu) != 0u;
-}
-
-// Choose (p0, p1) for one group.  keep: 4-bit set of candidate positions (exact / mask
-// modes).  Returns the nibble and sets *flag when the group breaks the 2:4 rule.
-__device__ __forceinline__ uint32_t pick_from_set(uint32_t keep, bool mask_mode, bool* flag) {
-  const int n = __popc(keep);
-  *flag = mask_mode ? (n != 2) : (n > 2);
+// Selection rule of the exact and mask modes as a function of the 4-bit set of candidate
+// positions: more than two -> the two lowest; fewer than two -> add the lowest free
+// positions until there are two.  kPickLut holds the resulting nibble p0 | p1 << 2 for
+// every set (4 bits each); kFlagMask / kFlagExact have bit `set` on when the group
+// breaks the rule of that mode (mask: not exactly two; exact: more than two).
+constexpr uint32_t pick_rule(uint32_t keep) {
   uint32_t s = keep;
-  if (n > 2) {  // keep the two lowest
-    uint32_t lo = s & (0u - s);
-    uint32_t rest = s ^ lo;
+  int n = 0;
+  for (int p = 0; p < 4; ++p) n += (s >> p) & 1u;
+  if (n > 2) {
+    const uint32_t lo = s & (0u - s);
+    const uint32_t rest = s ^ lo;
     s = lo | (rest & (0u - rest));
   }
-  while (__popc(s) < 2) s |= (~s) & (s + 1u);  // add the lowest free position
-  const uint32_t p0 = __ffs(s) - 1;
-  const uint32_t p1 = 31 - __clz(s);
+  for (int p = 0; p < 4 && n < 2; ++p)
+    if (!((s >> p) & 1u)) {
+      s |= 1u << p;
+      ++n;
+    }
+  uint32_t p0 = 0, p1 = 0;
+  for (int p = 3; p >= 0; --p)
+    if ((s >> p) & 1u) p0 = uint32_t(p);
+  for (int p = 0; p < 4; ++p)
+    if ((s >> p) & 1u) p1 = uint32_t(p);
   return p0 | (p1 << 2);
 }
+constexpr uint64_t make_pick_lut() {
+  uint64_t r = 0;
+  for (uint32_t k = 0; k < 16; ++k) r |= uint64_t(pick_rule(k)) << (4 * k);
+  return r;
+}
+constexpr uint32_t make_flag_lut(bool mask_mode) {
+  uint32_t r = 0;
+  for (uint32_t k = 0; k < 16; ++k) {
+    const int n = int(k & 1u) + int((k >> 1) & 1u) + int((k >> 2) & 1u) + int((k >> 3) & 1u);
+    if (mask_mode ? n != 2 : n > 2) r |= 1u << k;
+  }
+  return r;
+}
+constexpr uint64_t kPickLut = make_pick_lut();
+constexpr uint32_t kFlagMask = make_flag_lut(true);
+constexpr uint32_t kFlagExact = make_flag_lut(false);
 
-// x[i] for a run-time i in 0..3 without indexing memory (keeps x in registers)
-__device__ __forceinline__ uint32_t sel4(const uint32_t (&x)[4], uint32_t i) {
-  const uint32_t lo = (i & 1u) ? x[1] : x[0];
-  const uint32_t hi = (i & 1u) ? x[3] : x[2];
-  return (i & 2u) ? hi : lo;
+// Byte lanes whose bit 7 flags "set" -> 4-bit set (bit i = byte i): move the flags to bit
+// 0 of each byte and sum the bytes, weighted 1, 2, 4, 8, with one multiply.
+__device__ __forceinline__ uint32_t gather_bit7(uint32_t t) {
+  return (((t >> 7) & 0x01010101u) * 0x01020408u) >> 24;
 }
 
+// Candidate set of one group from its mask word (4 bytes, non-zero = keep): adding 0x7F
+// to the low 7 bits of a byte carries into bit 7 unless they are zero.
+__device__ __forceinline__ uint32_t keep_from_mask(uint32_t m) {
+  return gather_bit7(((m & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | m);
+}
+
+// Candidate set of one group from its values: non-zero elements (+0 and -0 are zero for
+// the float types).  16-bit: the group is words w0 (elements 0, 1) and w1 (2, 3); the
+// same carry trick on 15-bit magnitudes sets bit 15 of each non-zero half.
+__device__ __forceinline__ uint32_t keep_nonzero16(uint32_t w0, uint32_t w1) {
+  const uint32_t y0 = (w0 & 0x7FFF7FFFu) + 0x7FFF7FFFu, y1 = (w1 & 0x7FFF7FFFu) + 0x7FFF7FFFu;
+  return ((y0 >> 15) & 1u) | ((y0 >> 30) & 2u) | ((y1 >> 13) & 4u) | ((y1 >> 28) & 8u);
+}
 template <int CLS>
-__device__ __forceinline__ uint32_t pick_magnitude(const uint32_t (&x)[4]) {
+__device__ __forceinline__ uint32_t keep_nonzero8(uint32_t w) {
+  if constexpr (CLS == kFloat8) return gather_bit7((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu);
+  return gather_bit7(((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w);
+}
+
+// The two kept elements of a 16-bit group (words w0, w1) packed as one word.
+__device__ __forceinline__ uint32_t pack16(uint32_t w0, uint32_t w1, uint32_t nib) {
+  const uint32_t p0 = nib & 3u, p1 = nib >> 2;
+  const uint32_t sel = (p0 * 0x22u + 0x10u) | ((p1 * 0x22u + 0x10u) << 8);
+  return __byte_perm(w0, w1, sel);
+}
+// The two kept bytes of an 8-bit group (word w) in the low 16 bits.
+__device__ __forceinline__ uint32_t pack8(uint32_t w, uint32_t nib) {
+  return __byte_perm(w, 0u, (nib & 3u) | ((nib >> 2) << 4) | 0x4400u) & 0xFFFFu;
+}
+
+// Magnitude mode: keep the two largest |x| of a group; equal magnitudes keep the lower
+// position.  With the positions ordered by (|x| descending, position ascending), p is
+// kept when fewer than two positions come before it, which is a function of the six
+// comparisons c_ab = (k_b > k_a), a < b.  They form a 6-bit index (bit 0 c01, 1 c02,
+// 2 c13, 3 c03, 4 c12, 5 c23) into kTopLut, the nibble p0 | p1 << 2 for each outcome.
+constexpr uint32_t top2_rule(uint32_t idx) {
+  const uint32_t c01 = idx & 1u, c02 = (idx >> 1) & 1u, c13 = (idx >> 2) & 1u,
+                 c03 = (idx >> 3) & 1u, c12 = (idx >> 4) & 1u, c23 = (idx >> 5) & 1u;
+  const uint32_t before[4] = {c01 + c02 + c03, (1u - c01) + c12 + c13,
+                              (1u - c02) + (1u - c12) + c23, (1u - c03) + (1u - c13) + (1u - c23)};
+  uint32_t keep = 0;
+  for (int p = 0; p < 4; ++p) keep |= (before[p] < 2u ? 1u : 0u) << p;
+  return pick_rule(keep);
+}
+constexpr uint64_t make_top_lut(int part) {
+  uint64_t r = 0;
+  for (uint32_t i = 0; i < 16; ++i) r |= uint64_t(top2_rule(uint32_t(part) * 16u + i)) << (4 * i);
+  return r;
+}
+constexpr uint64_t kTopLut0 = make_top_lut(0), kTopLut1 = make_top_lut(1),
+                   kTopLut2 = make_top_lut(2), kTopLut3 = make_top_lut(3);
+
+__device__ __forceinline__ uint32_t top_lookup(uint32_t lo3, uint32_t hi3) {
+  const uint32_t idx = lo3 | (hi3 << 3);
+  const uint64_t q = (idx & 32u) ? ((idx & 16u) ? kTopLut3 : kTopLut2)
+                                 : ((idx & 16u) ? kTopLut1 : kTopLut0);
+  return uint32_t(q >> (4 * (idx & 15u))) & 0xFu;
+}
+
+// Index into kTopLut from the four keys of a group (plain compares).
+__device__ __forceinline__ uint32_t top2_keys(uint32_t k0, uint32_t k1, uint32_t k2, uint32_t k3) {
+  const uint32_t lo3 = uint32_t(k1 > k0) | (uint32_t(k2 > k0) << 1) | (uint32_t(k3 > k1) << 2);
+  const uint32_t hi3 = uint32_t(k3 > k0) | (uint32_t(k2 > k1) << 1) | (uint32_t(k3 > k2) << 2);
+  return top_lookup(lo3, hi3);
+}
+
+// 16-bit group in words w0 (elements 0, 1) and w1 (2, 3); keys = bits without the sign.
+__device__ __forceinline__ uint32_t top2_16(uint32_t w0, uint32_t w1) {
+  return top2_keys(w0 & 0x7FFFu, (w0 >> 16) & 0x7FFFu, w1 & 0x7FFFu, (w1 >> 16) & 0x7FFFu);
+}
+
+// 8-bit group in one word: keys = |x| (FP8: bits without the sign; s8: absolute value,
+// so -128 gives 128; u8: the value).
+template <int CLS>
+__device__ __forceinline__ uint32_t top2_8(uint32_t w) {
   uint32_t k[4];
 #pragma unroll
-  for (int p = 0; p < 4; ++p) k[p] = magnitude_key<CLS>(x[p]);
-  int best = 0;
-#pragma unroll
-  for (int p = 1; p < 4; ++p)
-    if (k[p] > k[best]) best = p;  // strict: equal keys keep the lower position
-  int second = best == 0 ? 1 : 0;
-#pragma unroll
-  for (int p = 0; p < 4; ++p)
-    if (p != best && k[p] > k[second]) second = p;
-  const uint32_t p0 = best < second ? best : second;
-  const uint32_t p1 = best < second ? second : best;
-  return p0 | (p1 << 2);
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t b = (w >> (8 * p)) & 0xFFu;
+    if constexpr (CLS == kFloat8) {
+      k[p] = b & 0x7Fu;
+    } else if constexpr (CLS == kSigned8) {
+      const int v = int(b) - int((b & 0x80u) << 1);
+      k[p] = uint32_t(v < 0 ? -v : v);
+    } else {
+      k[p] = b;
+    }
+  }
+  return top2_keys(k[0], k[1], k[2], k[3]);
 }
 
 // ESZ = element bytes (2 or 1); MODE = SP24_MODE_* value.  Each warp step covers kUnroll
-// groups of 32 consecutive chunks; all their loads are issued before any is used, so a
+// runs of 32 consecutive chunks; all their loads are issued before any is used, so a
 // thread keeps kUnroll 16-byte loads (plus mask loads) in flight.
 template <int ESZ, int CLS, int MODE>
-__global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
+__global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
   constexpr int kElems = 16 / ESZ;   // elements per 16-byte chunk
   constexpr int kGroups = kElems / 4;  // groups per chunk
   constexpr int kLanesPerWord = 32 / kElems;
   constexpr int kUnroll = 4;
+  constexpr uint32_t kFlags = MODE == 1 ? kFlagMask : kFlagExact;
   const int lane = threadIdx.x & 31;
   const int64_t cpr = a.K / kElems;  // chunks per row
   const int64_t total = a.M * cpr;
+  const bool small = total < (int64_t(1) << 32);  // 32-bit chunk numbers suffice
   const int64_t warp_global = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t warp_stride = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  bool any_flag = false;
+  uint32_t any_flag = 0;
 
   for (int64_t base = warp_global * 32 * kUnroll; base < total;
        base += warp_stride * 32 * kUnroll) {
@@ -110,8 +192,14 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t c = base + u * 32 + lane;
       active[u] = c < total;
-      row[u] = active[u] ? c / cpr : 0;
-      cc[u] = active[u] ? c - row[u] * cpr : 0;
+      if (small) {
+        const uint32_t r = uint32_t(c) / uint32_t(cpr);
+        row[u] = r;
+        cc[u] = int64_t(uint32_t(c) - r * uint32_t(cpr));
+      } else {
+        row[u] = c / cpr;
+        cc[u] = c - row[u] * cpr;
+      }
       v[u] = make_uint4(0, 0, 0, 0);
       mbits[u][0] = mbits[u][1] = mbits[u][2] = mbits[u][3] = 0;
       if (active[u]) {
@@ -138,45 +226,33 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
       const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
       uint32_t out[2] = {0, 0};  // kept elements, packed
       uint32_t nibs = 0;
+      uint32_t flags = 0;
 #pragma unroll
       for (int g = 0; g < kGroups; ++g) {
-        uint32_t x[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int e = 4 * g + p;  // element index within the chunk
-          if constexpr (ESZ == 2)
-            x[p] = (w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-          else
-            x[p] = (w[e >> 2] >> (8 * (e & 3))) & 0xFFu;
-        }
         uint32_t nib;
-        bool flag = false;
         if constexpr (MODE == 2) {
-          nib = pick_magnitude<CLS>(x);
+          if constexpr (ESZ == 2)
+            nib = top2_16(w[2 * g], w[2 * g + 1]);
+          else
+            nib = top2_8<CLS>(w[g]);
         } else {
-          uint32_t keep = 0;
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            bool k;
-            if constexpr (MODE == 1) {
-              const int e = 4 * g + p;
-              k = ((mbits[u][e >> 2] >> (8 * (e & 3))) & 0xFFu) != 0u;
-            } else {
-              k = is_nonzero<CLS>(x[p]);
-            }
-            keep |= uint32_t(k) << p;
-          }
-          nib = pick_from_set(keep, MODE == 1, &flag);
+          uint32_t keep;
+          if constexpr (MODE == 1)
+            keep = keep_from_mask(mbits[u][g]);
+          else if constexpr (ESZ == 2)
+            keep = keep_nonzero16(w[2 * g], w[2 * g + 1]);
+          else
+            keep = keep_nonzero8<CLS>(w[g]);
+          nib = uint32_t(kPickLut >> (4 * keep)) & 0xFu;
+          flags |= kFlags >> keep;
         }
-        any_flag |= (flag && active[u]);
-        const uint32_t k0 = sel4(x, nib & 3u), k1 = sel4(x, nib >> 2);
-        if constexpr (ESZ == 2) {
-          out[g] = k0 | (k1 << 16);
-        } else {
-          out[g >> 1] |= (k0 | (k1 << 8)) << (16 * (g & 1));
-        }
+        if constexpr (ESZ == 2)
+          out[g] = pack16(w[2 * g], w[2 * g + 1], nib);
+        else
+          out[g >> 1] |= pack8(w[g], nib) << (16 * (g & 1));
         nibs |= nib << (4 * g);
       }
+      if (active[u]) any_flag |= flags & 1u;
       if (active[u]) {
         __stcs(reinterpret_cast<uint2*>(a.values + row[u] * a.ldv_bytes + cc[u] * 8),
                make_uint2(out[0], out[1]));
@@ -190,7 +266,7 @@ __global__ void __launch_bounds__(256) compress_kernel(CompressArgs a) {
       }
     }
   }
-  if (a.status != nullptr && __any_sync(0xFFFFFFFFu, any_flag) && lane == 0)
+  if (a.status != nullptr && __any_sync(0xFFFFFFFFu, any_flag != 0u) && lane == 0)
     atomicOr(a.status, kDevNot24);
 }
 
@@ -222,13 +298,15 @@ __global__ void __launch_bounds__(256) decompress_kernel(DecompressArgs a) {
         k0 = h & 0xFFu;
         k1 = h >> 8;
       }
-      const int e0 = 4 * g + p0, e1 = 4 * g + p1;
-      if constexpr (ESZ == 2) {
-        o[e0 >> 1] |= k0 << (16 * (e0 & 1));
-        o[e1 >> 1] |= k1 << (16 * (e1 & 1));
-      } else {
-        o[e0 >> 2] |= k0 << (8 * (e0 & 3));
-        o[e1 >> 2] |= k1 << (8 * (e1 & 3));
+      // element 4g + p gets k0 at p0, k1 at p1, zero elsewhere (static register indices)
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint32_t v = uint32_t(p) == p0 ? k0 : (uint32_t(p) == p1 ? k1 : 0u);
+        const int e = 4 * g + p;
+        if constexpr (ESZ == 2)
+          o[e >> 1] |= v << (16 * (e & 1));
+        else
+          o[e >> 2] |= v << (8 * (e & 3));
       }
     }
     *reinterpret_cast<uint4*>(a.A + row * a.lda_bytes + cc * 16) = make_uint4(o[0], o[1], o[2], o[3]);

@@ -39,6 +39,16 @@ __device__ __forceinline__ uint32_t canon(const MetaArgs& a, int64_t row, int64_
   return a.index[row * a.ldi + w];
 }
 
+// Canonical words w0 .. w0+3 of one row: one 16-byte load when they are all inside the
+// index and 16-byte aligned, else word by word with padding.
+__device__ __forceinline__ uint4 canon4(const MetaArgs& a, int64_t row, int64_t w0) {
+  const uint32_t* p = a.index + row * a.ldi + w0;
+  if (row < a.M && w0 + 4 <= a.K / 32 && (reinterpret_cast<uintptr_t>(p) & 15u) == 0)
+    return __ldg(reinterpret_cast<const uint4*>(p));
+  return make_uint4(canon(a, row, w0), canon(a, row, w0 + 1), canon(a, row, w0 + 2),
+                    canon(a, row, w0 + 3));
+}
+
 // One thread per (tile, stage, lane): it reads the canonical words its lane needs and
 // writes the lane's 16-byte row of each of the stage's 4 MMA blocks (coalesced across the
 // lanes of a warp).
@@ -50,23 +60,26 @@ __global__ void __launch_bounds__(256) meta_kernel(MetaArgs a) {
     const int lane = int(o & 127);            // TMEM lane
     const int64_t blk = o >> 7;               // (mtile, kstep)
     const int64_t mt = blk / a.ksteps, ks = blk % a.ksteps;
-    uint4* out = reinterpret_cast<uint4*>(a.meta) + blk * (kMmasPerStage * 128) + lane;
     if constexpr (kEightBit) {
       const int64_t row = mt * 128 + lane;
-#pragma unroll
-      for (int j = 0; j < kMmasPerStage; ++j)
-        out[j * 128] = make_uint4(canon(a, row, ks * 8 + 2 * j), canon(a, row, ks * 8 + 2 * j + 1),
-                                  kPadWord, kPadWord);
+      uint4* out = reinterpret_cast<uint4*>(a.meta) + blk * (kMmasPerStage * 128) + lane;
+      const uint4 c0 = canon4(a, row, ks * 8), c1 = canon4(a, row, ks * 8 + 4);
+      out[0 * 128] = make_uint4(c0.x, c0.y, kPadWord, kPadWord);
+      out[1 * 128] = make_uint4(c0.z, c0.w, kPadWord, kPadWord);
+      out[2 * 128] = make_uint4(c1.x, c1.y, kPadWord, kPadWord);
+      out[3 * 128] = make_uint4(c1.z, c1.w, kPadWord, kPadWord);
     } else {
       const int band = lane >> 4, l = lane & 15;
       const int64_t rA = mt * 128 + band * 16 + (l & 7);
       const int h = l >> 3;
+      uint4* out = reinterpret_cast<uint4*>(a.meta) + blk * (kMmasPerStage * 128) + lane;
+      const uint4 lo4 = canon4(a, rA, ks * 4), hi4 = canon4(a, rA + 8, ks * 4);
+      const uint32_t lo[4] = {lo4.x, lo4.y, lo4.z, lo4.w}, hi[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
 #pragma unroll
-      for (int j = 0; j < kMmasPerStage; ++j) {
-        const int64_t w = ks * 4 + j;         // canonical word (32 dense K) of MMA j
-        const uint32_t lo = (canon(a, rA, w) >> (16 * h)) & 0xFFFFu;
-        const uint32_t hi = (canon(a, rA + 8, w) >> (16 * h)) & 0xFFFFu;
-        out[j * 128] = make_uint4(lo | (hi << 16), kPadWord, kPadWord, kPadWord);
+      for (int j = 0; j < kMmasPerStage; ++j) {  // MMA j reads canonical word ks * 4 + j
+        const uint32_t l16 = (lo[j] >> (16 * h)) & 0xFFFFu;
+        const uint32_t h16 = (hi[j] >> (16 * h)) & 0xFFFFu;
+        out[j * 128] = make_uint4(l16 | (h16 << 16), kPadWord, kPadWord, kPadWord);
       }
     }
   }
