@@ -40,10 +40,8 @@
 namespace sp24 {
 namespace {
 
-constexpr int kStages = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = 128 * 128;  // one stage of compressed A: 128 rows x 128 bytes
-constexpr int kBColsPerCta = 128;   // B columns staged by each CTA per stage
 constexpr int kSlotCols = 16;       // TMEM columns per MMA metadata slot (aligned)
 // Integer mode: 8-bit integers widened to bf16 are exact, every product |a b| <= 255 * 128,
 // so 512 non-zero products (1024 dense K = 8 bf16 stages) sum to less than 2^24 and the
@@ -57,33 +55,41 @@ struct MmaParams {
   int64_t ldc, ldd;
   int32_t* status;
   int c32, d32;  // C / D rows allow 32-byte vector accesses (base and pitch 32-byte aligned)
+  int batoms;    // B boxes loaded per stage and CTA (the narrow variant skips empty ones)
   int M, N, K;
   int mtiles, ntiles, num_kb;  // tiles of the variant (128 or 256 rows, 128 or 256 cols)
   uint64_t limit_ns;
 };
 
-template <int ESZ, bool kPair>
+// Variants: pair (256 x 256 tiles on a CTA pair), single (128 x 128 tiles) and narrow
+// (128 x 32 tiles for N <= 32: B staged in 32-byte swizzle atoms, so a stage holds only
+// the columns that exist and seven stages fit in shared memory).
+template <int ESZ, bool kPair, bool kNarrow = false>
 struct Geo {
   static constexpr int kStageK = ESZ == 2 ? 128 : 256;       // dense K per stage
   static constexpr int kMmaK = ESZ == 2 ? 32 : 64;            // dense K per MMA
   static constexpr int kMmas = kStageK / kMmaK;               // 4
   static constexpr int kMetaBytes = kMmas * kMetaBlockBytes;  // 8 KB per stage
-  static constexpr int kAtomN = 128 / ESZ;                    // B columns per 128 bytes
-  static constexpr int kAtoms = kBColsPerCta / kAtomN;
-  static constexpr int kAtomBytes = kStageK * 128;            // one B box
-  static constexpr int kBBytes = kAtoms * kAtomBytes;         // 32 KB
+  static constexpr int kTileM = kPair ? 256 : 128;
+  static constexpr int kTileN = kPair ? 256 : (kNarrow ? 32 : 128);
+  static constexpr int kBCols = kPair ? 128 : kTileN;         // B columns staged per CTA
+  static constexpr int kAtomInner = kNarrow ? 32 : 128;       // bytes of a B atom row
+  static constexpr int kSwzCode = kNarrow ? 6 : 2;            // descriptor: 32B / 128B
+  static constexpr int kAtomN = kAtomInner / ESZ;             // B columns per atom
+  static constexpr int kAtoms = kBCols / kAtomN;
+  static constexpr int kAtomBytes = kStageK * kAtomInner;     // one B box
+  static constexpr int kBBytes = kAtoms * kAtomBytes;
+  static constexpr int kStages = kNarrow ? 7 : 4;
   static constexpr int kStageBytes = kABytes + kBBytes + kMetaBytes;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
-  static constexpr uint32_t kTx = uint32_t(kStageBytes) * (kPair ? 2 : 1);
-  static constexpr int kTileM = kPair ? 256 : 128;
-  static constexpr int kTileN = kPair ? 256 : 128;
   static constexpr int kAccBufs = kPair ? 1 : 2;
-  static constexpr int kAccCols = kAccBufs * kTileN;          // 256 in both variants
+  static constexpr int kAccCols = kAccBufs * kTileN;
   static constexpr uint32_t kMetaCol = kAccCols;              // slot set s at + s * 64
   static constexpr int kEpiWarps = kPair ? 8 : 4;
-  static constexpr int kThreads = 32 * (2 + kEpiWarps);       // 192 or 320
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);       // 320 or 192
   static_assert(kAccCols + kStages * kMmas * kSlotCols <= int(kTmemCols), "TMEM budget");
-  static_assert(kSmemBytes <= 232448 - 256, "shared memory budget");
+  static_assert(kSmemBytes <= 232448 - 512, "shared memory budget");
+  static_assert(kAtoms >= 1, "B atoms");
 };
 
 // Tile order: bands of kBandRows rows of D, each swept along N, so that the tiles in
@@ -197,20 +203,21 @@ __device__ __forceinline__ void store8(const float (&v)[8], const MmaParams& p, 
   }
 }
 
-// Four 32-column segments (columns col0 .. col0+127) of one output row from a .16x256b
-// fragment r (repetitions 0..15; row half e = 0 is lane t/4, e = 1 lane t/4 + 8): two
-// segments at a time, their C loads issued together, then each segment is transposed
-// across the quad, added to C and stored.
-template <int OUT>
-__device__ __forceinline__ void store_row128(const uint32_t* r, int e, const MmaParams& p,
-                                             int row, int col0, int q) {
+// kSeg 32-column segments (columns col0 .. col0 + 32 kSeg - 1) of one output row from a
+// .16x256b fragment r (repetitions 0 .. 4 kSeg - 1; row half e = 0 is lane t/4, e = 1
+// lane t/4 + 8): up to two segments at a time, their C loads issued together, then each
+// segment is transposed across the quad, added to C and stored.
+template <int OUT, int kSeg>
+__device__ __forceinline__ void store_row(const uint32_t* r, int e, const MmaParams& p, int row,
+                                          int col0, int q) {
+  constexpr int kBatch = kSeg < 2 ? kSeg : 2;
 #pragma unroll
-  for (int g0 = 0; g0 < 4; g0 += 2) {
-    float c[2][8];
+  for (int g0 = 0; g0 < kSeg; g0 += kBatch) {
+    float c[kBatch][8];
 #pragma unroll
-    for (int g = 0; g < 2; ++g) load_c8(c[g], p, row, col0 + 32 * (g0 + g) + 8 * q);
+    for (int g = 0; g < kBatch; ++g) load_c8(c[g], p, row, col0 + 32 * (g0 + g) + 8 * q);
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
+    for (int g = 0; g < kBatch; ++g) {
       float v[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -226,10 +233,11 @@ __device__ __forceinline__ void store_row128(const uint32_t* r, int e, const Mma
 }
 
 // Pull this thread's share of the C rows of a coming tile into L2 (the quad leader of
-// each row, one bulk prefetch of up to 512 bytes per row).
-__device__ __forceinline__ void prefetch_c_rows(const MmaParams& p, int row0, int col0, int q) {
+// each row, one bulk prefetch of up to `cols` columns per row).
+__device__ __forceinline__ void prefetch_c_rows(const MmaParams& p, int row0, int col0, int q,
+                                                int cols) {
   if (p.C == nullptr || q != 0 || col0 >= p.N) return;
-  const int ncols = p.N - col0 < 128 ? p.N - col0 : 128;
+  const int ncols = p.N - col0 < cols ? p.N - col0 : cols;
   const uint32_t bytes = uint32_t(ncols * 4) & ~15u;
   if (bytes == 0) return;
 #pragma unroll
@@ -281,12 +289,13 @@ __device__ __forceinline__ void store_chunk_s32(const uint32_t* v, const MmaPara
 
 // OUT: 0 = f32 output, 1 = bf16 output, 2 = s32 output (integer mode, single variant).
 // C (nullable) is f32 for float outputs, s32 for integer mode.
-template <int ESZ, int OUT, bool kPair>
-__global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
+template <int ESZ, int OUT, bool kPair, bool kNarrow>
+__global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow>::kThreads, 1)
     spmma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmM, const MmaParams p,
                  const uint32_t idesc) {
-  using G = Geo<ESZ, kPair>;
+  using G = Geo<ESZ, kPair, kNarrow>;
+  constexpr int kStages = G::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
@@ -345,11 +354,13 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
         int mt, nt;
         tile_coords<G::kTileM>(p, t, mt, nt);
         const int mt128 = kPair ? mt * 2 + int(rank) : mt;  // this CTA's 128-row tile
-        const int bcol = nt * G::kTileN + int(rank) * kBColsPerCta;
+        const int bcol = nt * G::kTileN + int(rank) * G::kBCols;
+        const uint32_t tx =
+            uint32_t(kABytes + p.batoms * G::kAtomBytes + G::kMetaBytes) * (kPair ? 2u : 1u);
         for (int kb = 0; kb < p.num_kb; ++kb, ++q) {
           const int s = q % kStages;
           if (!mbar_wait(&empty_bar[s], ((q / kStages) & 1) ^ 1u, abort, p.limit_ns)) break;
-          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], G::kTx);
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], tx);
           const int kx = kb * (G::kStageK / 2);
           const int mrow = (mt128 * p.num_kb + kb) * (G::kMetaBytes / 128);
           if constexpr (kPair) {
@@ -357,14 +368,16 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
             tma_load_2d_pair(sA + s * kABytes, &tmA, fb, kx, mt128 * 128);
 #pragma unroll
             for (int a = 0; a < G::kAtoms; ++a)
-              tma_load_2d_pair(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, fb,
+              if (a < p.batoms)
+                tma_load_2d_pair(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, fb,
                                bcol + a * G::kAtomN, kb * G::kStageK);
             tma_load_2d_pair(sM + s * G::kMetaBytes, &tmM, fb, 0, mrow);
           } else {
             tma_load_2d(sA + s * kABytes, &tmA, &full_bar[s], kx, mt128 * 128);
 #pragma unroll
             for (int a = 0; a < G::kAtoms; ++a)
-              tma_load_2d(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, &full_bar[s],
+              if (a < p.batoms)
+                tma_load_2d(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, &full_bar[s],
                           bcol + a * G::kAtomN, kb * G::kStageK);
             tma_load_2d(sM + s * G::kMetaBytes, &tmM, &full_bar[s], 0, mrow);
           }
@@ -380,7 +393,8 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (rank == 0 && lane == 0) {
       const uint64_t adesc_hi = smem_desc_hi(16, 1024, 2);
-      const uint64_t bdesc_hi = smem_desc_hi(G::kAtomBytes, 1024, 2);
+      // B is MN-major: LBO = next atom along N, SBO = next 8 rows of K
+      const uint64_t bdesc_hi = smem_desc_hi(G::kAtomBytes, 8 * G::kAtomInner, G::kSwzCode);
       const uint64_t mdesc_hi = smem_desc_hi(0, 128, 0);
       int q = 0, local = 0, chunk = 0;
       for (int t = unit; t < ntiles_total && !*abort; t += nunits, ++local) {
@@ -432,7 +446,7 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
           for (int j = 0; j < G::kMmas; ++j) {
             if (k0 + j * G::kMmaK < p.K) {
               const uint64_t ad = smem_desc(a_saddr + 32 * j, adesc_hi);
-              const uint64_t bd = smem_desc(b_saddr + j * G::kMmaK * 128, bdesc_hi);
+              const uint64_t bd = smem_desc(b_saddr + j * G::kMmaK * G::kAtomInner, bdesc_hi);
               const uint32_t acc = (first > 0 || j > 0) ? 1u : 0u;
               if constexpr (kPair)
                 tc_mma_sp_pair<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, idesc, acc);
@@ -539,30 +553,36 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair>::kThreads, 1)
           int mt2, nt2;
           tile_coords<G::kTileM>(p, t + nunits, mt2, nt2);
           prefetch_c_rows(p, mt2 * G::kTileM + int(rank) * 128 + quad * 32 + (lane >> 2),
-                          nt2 * G::kTileN + half * 128, lane & 3);
+                          nt2 * G::kTileN + half * 128, lane & 3, 128);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            store_row128<OUT>(r[h], e, p, row0 + 16 * h + 8 * e, col0, lane & 3);
+            store_row<OUT, 4>(r[h], e, p, row0 + 16 * h + 8 * e, col0, lane & 3);
       } else {
         const int row0 = mt * G::kTileM + quad * 32 + (lane >> 2);
         if (t + nunits < ntiles_total) {  // the next tile's C, needed one mainloop from now
           int mt2, nt2;
           tile_coords<G::kTileM>(p, t + nunits, mt2, nt2);
-          prefetch_c_rows(p, mt2 * G::kTileM + quad * 32 + (lane >> 2), nt2 * G::kTileN, lane & 3);
+          prefetch_c_rows(p, mt2 * G::kTileM + quad * 32 + (lane >> 2), nt2 * G::kTileN, lane & 3,
+                          G::kTileN);
         }
-        uint32_t r[2][64];
+        constexpr int kSeg = G::kTileN / 32;
+        uint32_t r[2][16 * kSeg];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          tc_ld_16x256b_x16(lane_base + (uint32_t(16 * h) << 16), r[h]);
+        for (int h = 0; h < 2; ++h) {
+          if constexpr (kSeg == 4)
+            tc_ld_16x256b_x16(lane_base + (uint32_t(16 * h) << 16), r[h]);
+          else
+            tc_ld_16x256b_x4(lane_base + (uint32_t(16 * h) << 16), r[h]);
+        }
         tc_wait_ld();
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            store_row128<OUT>(r[h], e, p, row0 + 16 * h + 8 * e, nt * G::kTileN, lane & 3);
+            store_row<OUT, kSeg>(r[h], e, p, row0 + 16 * h + 8 * e, nt * G::kTileN, lane & 3);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(abuf * sizeof(uint64_t)));
@@ -618,10 +638,10 @@ bool make_tmap(CUtensorMap* m, const void* base, int esz, uint64_t cols, uint64_
   return r == CUDA_SUCCESS;
 }
 
-template <int ESZ, int OUT, bool kPair>
+template <int ESZ, int OUT, bool kPair, bool kNarrow = false>
 int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const void* B,
         int64_t ldb, uint32_t idesc, int num_sms, cudaStream_t s) {
-  using G = Geo<ESZ, kPair>;
+  using G = Geo<ESZ, kPair, kNarrow>;
   p.mtiles = (p.M + G::kTileM - 1) / G::kTileM;
   p.ntiles = (p.N + G::kTileN - 1) / G::kTileN;
   CUtensorMap tA, tB, tM;
@@ -633,7 +653,7 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
                    128 / ESZ, 128, CU_TENSOR_MAP_SWIZZLE_128B))
       return 4;
     if (!make_tmap(&tB, B, ESZ, uint64_t(p.N), uint64_t(p.K), uint64_t(ldb) * ESZ, G::kAtomN,
-                   G::kStageK, CU_TENSOR_MAP_SWIZZLE_128B))
+                   G::kStageK, kNarrow ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B))
       return 4;
     // the compact metadata image as rows of 128 bytes; one (tile, stage) block per box
     const uint64_t mrows = uint64_t(meta_mtiles(p.M)) * p.num_kb * (G::kMetaBytes / 128);
@@ -641,7 +661,9 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
                    CU_TENSOR_MAP_SWIZZLE_NONE))
       return 4;
   }
-  auto kern = spmma_kernel<ESZ, OUT, kPair>;
+  // the narrow variant loads only the B atoms that hold columns below N
+  p.batoms = kNarrow ? (p.N + G::kAtomN - 1) / G::kAtomN : G::kAtoms;
+  auto kern = spmma_kernel<ESZ, OUT, kPair, kNarrow>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) !=
       cudaSuccess)
     return 4;
@@ -680,6 +702,11 @@ int dispatch(const MmaParams& p, const void* values, int64_t ldv, const void* me
   if (p.N > 128)  // wide outputs: 256 x 256 tiles on CTA pairs
     return run<ESZ, OUT, true>(p, values, ldv, meta, B, ldb, idesc_sparse_f32(at, bt, 256, 256),
                                num_sms, s);
+  if (p.N <= 32) {  // skinny outputs: 128 x 32 tiles, MMA N = N rounded up to 16
+    const uint32_t n_mma = uint32_t((p.N + 15) / 16 * 16);
+    return run<ESZ, OUT, false, true>(p, values, ldv, meta, B, ldb,
+                                      idesc_sparse_f32(at, bt, 128, n_mma), num_sms, s);
+  }
   return run<ESZ, OUT, false>(p, values, ldv, meta, B, ldb, idesc_sparse_f32(at, bt, 128, 128),
                               num_sms, s);
 }

@@ -24,10 +24,20 @@ def test_config1_bit_exact():
 
 @pytest.mark.parametrize("ta", FLOAT_TYPES)
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (200, 192, 320), (257, 64, 96),
-                                   (64, 304, 512), (1, 16, 32), (384, 400, 1056)])
+                                   (64, 304, 512), (1, 16, 32), (384, 400, 1056),
+                                   (200, 16, 384), (257, 32, 1056), (130, 48, 256)])
 def test_small_ragged_shapes(ta, M, N, K):
     c = inputs.case(ta, ta, M, N, K, seed=M + N + K, tc="f32")
     run_case(c, mode="mask")
+
+
+@pytest.mark.parametrize("ta", ["f16", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(130, 24, 256), (64, 8, 128), (300, 16, 2080)])
+def test_skinny_outputs(ta, M, N, K):
+    # N <= 32 runs on 128 x 32 tiles that stage only the B columns below N
+    c = inputs.case(ta, ta, M, N, K, seed=M + N + K, tc="f32")
+    run_case(c, mode="mask")
+    run_case(dict(c, C=None, tc=None), mode="mask", out_dtype=torch.bfloat16)
 
 
 @pytest.mark.parametrize("ta", FLOAT_TYPES)
