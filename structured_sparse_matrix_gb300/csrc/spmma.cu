@@ -61,18 +61,20 @@ struct MmaParams {
   uint64_t limit_ns;
 };
 
-// Variants: pair (256 x 256 tiles on a CTA pair), single (128 x 128 tiles) and narrow
-// (128 x 32 tiles for N <= 32: B staged in 32-byte swizzle atoms, so a stage holds only
-// the columns that exist and seven stages fit in shared memory).
-template <int ESZ, bool kPair, bool kNarrow = false>
+// Variants: pair (256 x 256 tiles on a CTA pair), pair with 256 x 128 tiles and
+// double-buffered accumulators (the integer path, whose chunked accumulation switches
+// buffers every 8 stages), single (128 x 128 tiles) and narrow (128 x 32 tiles for
+// N <= 32: B staged in 32-byte swizzle atoms, so a stage holds only the columns that
+// exist and seven stages fit in shared memory).
+template <int ESZ, bool kPair, bool kNarrow = false, bool kHalfN = false>
 struct Geo {
   static constexpr int kStageK = ESZ == 2 ? 128 : 256;       // dense K per stage
   static constexpr int kMmaK = ESZ == 2 ? 32 : 64;            // dense K per MMA
   static constexpr int kMmas = kStageK / kMmaK;               // 4
   static constexpr int kMetaBytes = kMmas * kMetaBlockBytes;  // 8 KB per stage
   static constexpr int kTileM = kPair ? 256 : 128;
-  static constexpr int kTileN = kPair ? 256 : (kNarrow ? 32 : 128);
-  static constexpr int kBCols = kPair ? 128 : kTileN;         // B columns staged per CTA
+  static constexpr int kTileN = kPair ? (kHalfN ? 128 : 256) : (kNarrow ? 32 : 128);
+  static constexpr int kBCols = kPair ? kTileN / 2 : kTileN;  // B columns staged per CTA
   static constexpr int kAtomInner = kNarrow ? 32 : 128;       // bytes of a B atom row
   static constexpr int kSwzCode = kNarrow ? 6 : 2;            // descriptor: 32B / 128B
   static constexpr int kAtomN = kAtomInner / ESZ;             // B columns per atom
@@ -82,7 +84,7 @@ struct Geo {
   static constexpr int kStages = kNarrow ? 7 : 4;
   static constexpr int kStageBytes = kABytes + kBBytes + kMetaBytes;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
-  static constexpr int kAccBufs = kPair ? 1 : 2;
+  static constexpr int kAccBufs = (kPair && !kHalfN) ? 1 : 2;
   static constexpr int kAccCols = kAccBufs * kTileN;
   static constexpr uint32_t kMetaCol = kAccCols;              // slot set s at + s * 64
   static constexpr int kEpiWarps = kPair ? 8 : 4;
@@ -289,12 +291,12 @@ __device__ __forceinline__ void store_chunk_s32(const uint32_t* v, const MmaPara
 
 // OUT: 0 = f32 output, 1 = bf16 output, 2 = s32 output (integer mode, single variant).
 // C (nullable) is f32 for float outputs, s32 for integer mode.
-template <int ESZ, int OUT, bool kPair, bool kNarrow>
-__global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow>::kThreads, 1)
+template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN>
+__global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
     spmma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmM, const MmaParams p,
                  const uint32_t idesc) {
-  using G = Geo<ESZ, kPair, kNarrow>;
+  using G = Geo<ESZ, kPair, kNarrow, kHalfN>;
   constexpr int kStages = G::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -402,8 +404,8 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow>::kThreads, 1)
         int abuf = 0;
         uint32_t d_tmem = tmem;
         if constexpr (OUT != 2) {
-          abuf = kPair ? 0 : (local & 1);
-          const int use = kPair ? local : (local >> 1);  // earlier uses of this buffer
+          abuf = G::kAccBufs == 1 ? 0 : (local & 1);
+          const int use = G::kAccBufs == 1 ? local : (local >> 1);  // earlier uses of abuf
           if (!mbar_wait(&acc_empty[abuf], (use & 1) ^ 1u, abort, p.limit_ns)) break;
           tc_fence_after();
           d_tmem = tmem + uint32_t(abuf * G::kTileN);
@@ -460,7 +462,10 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow>::kThreads, 1)
             tc_commit(&empty_bar[s]);
           if constexpr (OUT == 2) {
             if (kc == kIntChunkStages - 1 || kb == p.num_kb - 1) {  // chunk done
-              tc_commit(&acc_full[abuf]);
+              if constexpr (kPair)
+                tc_commit_pair_mc(&acc_full[abuf], 3);
+              else
+                tc_commit(&acc_full[abuf]);
               ++chunk;
             }
           }
@@ -490,8 +495,8 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow>::kThreads, 1)
     for (int t = unit; t < ntiles_total; t += nunits, ++local) {
       int mt, nt;
       tile_coords<G::kTileM>(p, t, mt, nt);
-      const int abuf = kPair ? 0 : (local & 1);
-      const int use = kPair ? local : (local >> 1);
+      const int abuf = G::kAccBufs == 1 ? 0 : (local & 1);
+      const int use = G::kAccBufs == 1 ? local : (local >> 1);
       if constexpr (OUT != 2) {
         if (!mbar_wait(&acc_full[abuf], use & 1, abort, p.limit_ns)) break;
         tc_fence_after();
@@ -499,12 +504,14 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow>::kThreads, 1)
       const int row = mt * G::kTileM + int(rank) * 128 + quad * 32 + lane;
       const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16) + uint32_t(abuf * G::kTileN);
       if constexpr (OUT == 2) {
-        // integer mode: one f32 chunk per 1024 dense K, summed exactly in int32
-        // (single variant: 4 epilogue warps, each thread one row x 128 columns)
+        // integer mode: one f32 chunk per 1024 dense K, summed exactly in int32; each
+        // thread owns one row x kIntCols columns (single: 128, pair 256 x 128: 64)
         (void)abuf;
-        uint32_t sum[128];
+        constexpr int kIntCols = G::kTileN * 4 / G::kEpiWarps;
+        const int cbase = (ew >> 2) * kIntCols;  // this warp's first column in the tile
+        uint32_t sum[kIntCols];
 #pragma unroll
-        for (int j = 0; j < 128; ++j) sum[j] = 0u;
+        for (int j = 0; j < kIntCols; ++j) sum[j] = 0u;
         const int nch = (p.num_kb + kIntChunkStages - 1) / kIntChunkStages;
         bool ok = true;
         for (int c = 0; c < nch; ++c, ++ichunk) {
@@ -514,9 +521,10 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow>::kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t base = tmem + (uint32_t(quad * 32) << 16) + uint32_t(b * G::kTileN);
+          const uint32_t base =
+              tmem + (uint32_t(quad * 32) << 16) + uint32_t(b * G::kTileN + cbase);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q4 = 0; q4 < kIntCols / 32; ++q4) {
             uint32_t r[32];
             tc_ld_32x32b_x32(base + uint32_t(q4 * 32), r);
             tc_wait_ld();
@@ -531,8 +539,8 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow>::kThreads, 1)
         if (!ok) break;
         if (row < p.M) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int col0 = nt * G::kTileN + c * 32;
+          for (int c = 0; c < kIntCols / 32; ++c) {
+            const int col0 = nt * G::kTileN + cbase + c * 32;
             if (col0 < p.N) store_chunk_s32(&sum[c * 32], p, row, col0);
           }
         }
@@ -638,10 +646,10 @@ bool make_tmap(CUtensorMap* m, const void* base, int esz, uint64_t cols, uint64_
   return r == CUDA_SUCCESS;
 }
 
-template <int ESZ, int OUT, bool kPair, bool kNarrow = false>
+template <int ESZ, int OUT, bool kPair, bool kNarrow = false, bool kHalfN = false>
 int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const void* B,
         int64_t ldb, uint32_t idesc, int num_sms, cudaStream_t s) {
-  using G = Geo<ESZ, kPair, kNarrow>;
+  using G = Geo<ESZ, kPair, kNarrow, kHalfN>;
   p.mtiles = (p.M + G::kTileM - 1) / G::kTileM;
   p.ntiles = (p.N + G::kTileN - 1) / G::kTileN;
   CUtensorMap tA, tB, tM;
@@ -663,7 +671,7 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
   }
   // the narrow variant loads only the B atoms that hold columns below N
   p.batoms = kNarrow ? (p.N + G::kAtomN - 1) / G::kAtomN : G::kAtoms;
-  auto kern = spmma_kernel<ESZ, OUT, kPair, kNarrow>;
+  auto kern = spmma_kernel<ESZ, OUT, kPair, kNarrow, kHalfN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) !=
       cudaSuccess)
     return 4;
@@ -743,7 +751,8 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   p.limit_ns = 1000000000ull;  // 1 s per wait
   if (is_i8(ta)) {
     // integers: widen both operands to bf16 (exact) and run the bf16 tensor path with
-    // chunked integer accumulation; 128 x 128 tiles with double-buffered accumulators
+    // chunked integer accumulation; 256 x 128 tiles on CTA pairs with double-buffered
+    // accumulators
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uint8_t* wa = ws;
     uint8_t* wb = ws + (M * (K / 2) * 2 + 255) / 256 * 256;
@@ -754,8 +763,8 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
         return 4;
     }
     // kind::f16 with bf16 operands: type code 1 for A and B
-    return run<2, 2, false>(p, wa, K / 2, meta, wb, ldbw, idesc_sparse_f32(1, 1, 128, 128),
-                            num_sms, s);
+    return run<2, 2, true, false, true>(p, wa, K / 2, meta, wb, ldbw,
+                                        idesc_sparse_f32(1, 1, 256, 128), num_sms, s);
   }
   const int esz = dtype_bytes(ta);
   // kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2
