@@ -154,7 +154,8 @@ size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t
  *
  * ta, tb, tc, td supported combinations (anything else: SP24_ERR_UNSUPPORTED):
  *   (F16, F16) and (BF16, BF16)     -> f32 accumulate, tc in {F32, none}, td in {F32, BF16}
- *   (E4M3, E4M3) and (E5M2, E5M2)   -> f32 accumulate, tc in {F32, none}, td in {F32, BF16}
+ *   (E4M3, E4M3), (E5M2, E5M2),
+ *   (E4M3, E5M2) and (E5M2, E4M3)   -> f32 accumulate, tc in {F32, none}, td in {F32, BF16}
  *   (S8, S8) and (U8, S8)           -> exact integer result, tc in {S32, none}, td = S32,
  *                                      32-bit two's-complement wrap, no clamp
  * "none" for tc means C == NULL (treated as zero); tc is then ignored.

@@ -183,7 +183,9 @@ sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
   const bool f8 = is_f8(ta);
   const bool i8 = is_i8(ta);
   if (f16ish || f8) {
-    if (tb != ta) return SP24_ERR_UNSUPPORTED;
+    // 16-bit: A and B of one type; FP8: any mix of E4M3 and E5M2 (kind::f8f6f4 takes
+    // separate A and B type fields)
+    if (f16ish ? tb != ta : !is_f8(tb)) return SP24_ERR_UNSUPPORTED;
     if (C != nullptr && tc != SP24_F32) return SP24_ERR_UNSUPPORTED;
     if (td != SP24_F32 && td != SP24_BF16) return SP24_ERR_UNSUPPORTED;
   } else if (i8) {

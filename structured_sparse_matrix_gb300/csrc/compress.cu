@@ -164,6 +164,46 @@ __device__ __forceinline__ uint32_t top2_8(uint32_t w) {
   return top2_keys(k[0], k[1], k[2], k[3]);
 }
 
+// One 16-byte chunk of a row (8 16-bit or 16 8-bit elements = 2 or 4 groups): the kept
+// elements packed into 8 bytes, the groups' nibbles (4 bits each, group g at 4g) and the
+// mode's rule-break flag in bit 0 of `flags`.  m: the chunk's mask bytes (mask mode).
+template <int ESZ, int CLS, int MODE>
+__device__ __forceinline__ void compress_chunk(const uint4& v, const uint32_t (&m)[4], uint2& vals,
+                                               uint32_t& nibs, uint32_t& flags) {
+  constexpr int kGroups = (16 / ESZ) / 4;
+  constexpr uint32_t kFlags = MODE == 1 ? kFlagMask : kFlagExact;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[2] = {0, 0};
+  nibs = 0;
+  flags = 0;
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    uint32_t nib;
+    if constexpr (MODE == 2) {
+      if constexpr (ESZ == 2)
+        nib = top2_16(w[2 * g], w[2 * g + 1]);
+      else
+        nib = top2_8<CLS>(w[g]);
+    } else {
+      uint32_t keep;
+      if constexpr (MODE == 1)
+        keep = keep_from_mask(m[g]);
+      else if constexpr (ESZ == 2)
+        keep = keep_nonzero16(w[2 * g], w[2 * g + 1]);
+      else
+        keep = keep_nonzero8<CLS>(w[g]);
+      nib = uint32_t(kPickLut >> (4 * keep)) & 0xFu;
+      flags |= kFlags >> keep;
+    }
+    if constexpr (ESZ == 2)
+      out[g] = pack16(w[2 * g], w[2 * g + 1], nib);
+    else
+      out[g >> 1] |= pack8(w[g], nib) << (16 * (g & 1));
+    nibs |= nib << (4 * g);
+  }
+  vals = make_uint2(out[0], out[1]);
+}
+
 // ESZ = element bytes (2 or 1); MODE = SP24_MODE_* value.  Each warp step covers kUnroll
 // runs of 32 consecutive chunks; all their loads are issued before any is used, so a
 // thread keeps kUnroll 16-byte loads (plus mask loads) in flight.
@@ -173,7 +213,6 @@ __global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
   constexpr int kGroups = kElems / 4;  // groups per chunk
   constexpr int kLanesPerWord = 32 / kElems;
   constexpr int kUnroll = 4;
-  constexpr uint32_t kFlags = MODE == 1 ? kFlagMask : kFlagExact;
   const int lane = threadIdx.x & 31;
   const int64_t cpr = a.K / kElems;  // chunks per row
   const int64_t total = a.M * cpr;
@@ -223,40 +262,12 @@ __global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-      uint32_t out[2] = {0, 0};  // kept elements, packed
-      uint32_t nibs = 0;
-      uint32_t flags = 0;
-#pragma unroll
-      for (int g = 0; g < kGroups; ++g) {
-        uint32_t nib;
-        if constexpr (MODE == 2) {
-          if constexpr (ESZ == 2)
-            nib = top2_16(w[2 * g], w[2 * g + 1]);
-          else
-            nib = top2_8<CLS>(w[g]);
-        } else {
-          uint32_t keep;
-          if constexpr (MODE == 1)
-            keep = keep_from_mask(mbits[u][g]);
-          else if constexpr (ESZ == 2)
-            keep = keep_nonzero16(w[2 * g], w[2 * g + 1]);
-          else
-            keep = keep_nonzero8<CLS>(w[g]);
-          nib = uint32_t(kPickLut >> (4 * keep)) & 0xFu;
-          flags |= kFlags >> keep;
-        }
-        if constexpr (ESZ == 2)
-          out[g] = pack16(w[2 * g], w[2 * g + 1], nib);
-        else
-          out[g >> 1] |= pack8(w[g], nib) << (16 * (g & 1));
-        nibs |= nib << (4 * g);
-      }
+      uint2 vals;
+      uint32_t nibs, flags;
+      compress_chunk<ESZ, CLS, MODE>(v[u], mbits[u], vals, nibs, flags);
       if (active[u]) any_flag |= flags & 1u;
-      if (active[u]) {
-        __stcs(reinterpret_cast<uint2*>(a.values + row[u] * a.ldv_bytes + cc[u] * 8),
-               make_uint2(out[0], out[1]));
-      }
+      if (active[u])
+        __stcs(reinterpret_cast<uint2*>(a.values + row[u] * a.ldv_bytes + cc[u] * 8), vals);
       // merge the nibbles of the lanes that share one index word
       uint32_t word = nibs << ((4 * kGroups) * (lane % kLanesPerWord));
 #pragma unroll

@@ -93,7 +93,8 @@ def _mma(ta=BF16, tb=BF16, tc=F32, td=F32, M=128, N=128, K=128, values=FAKE, ldv
 
 def test_mma_argument_checks():
     assert _mma(ta=F16, tb=BF16) == UNSUPPORTED
-    assert _mma(ta=E4M3, tb=E5M2) == UNSUPPORTED
+    assert _mma(ta=E4M3, tb=BF16) == UNSUPPORTED
+    assert _mma(ta=BF16, tb=E4M3) == UNSUPPORTED
     assert _mma(td=S32) == UNSUPPORTED
     assert _mma(tc=S32) == UNSUPPORTED
     assert _mma(ta=F32, tb=F32) == UNSUPPORTED

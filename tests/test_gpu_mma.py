@@ -47,6 +47,16 @@ def test_no_C_and_bf16_output(ta):
     run_case(c, mode="mask", out_dtype=torch.bfloat16)
 
 
+@pytest.mark.parametrize("ta,tb", [("e4m3", "e5m2"), ("e5m2", "e4m3")])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (200, 304, 512), (130, 16, 768),
+                                   (384, 400, 1280)])
+def test_mixed_fp8_operands(ta, tb, M, N, K):
+    # kind::f8f6f4 takes separate A and B types: E4M3 x E5M2 and E5M2 x E4M3
+    c = inputs.case(ta, tb, M, N, K, seed=M + 3 * N + K, tc="f32")
+    run_case(c, mode="mask")
+    run_case(dict(c, C=None, tc=None), mode="mask", out_dtype=torch.bfloat16)
+
+
 @pytest.mark.parametrize("ta", ["f16", "e4m3"])
 def test_every_single_pattern(ta):
     # one pattern everywhere, for each of the six: exercises every metadata nibble value
