@@ -193,6 +193,29 @@ sp24_status sp24_diag_wait_timeout(int32_t *d_status, uint64_t limit_ns, void *s
 #define SP24_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
 /*
+ * sp24_mma_strided_batched -- `batch` independent products of one shape in one launch
+ * (e.g. the same layer for several sequences, or experts of equal size):
+ *   D_b = expand(values_b, meta_b) * B_b + C_b,  b = 0 .. batch-1,
+ * where operand X of problem b starts at X + b * stride_X.  The tiles of all problems
+ * are scheduled together, so small problems fill the GPU.  Float operands only (the
+ * pairs sp24_mma takes for 16-bit and FP8 types); everything else as in sp24_mma for each
+ * problem (sizes, leading dimensions, alignment, tc / td, status bits).
+ * stride_values, stride_b : elements of ta / tb between problems' values and B.
+ * stride_meta : bytes between problems' metadata images, >= sp24_meta_bytes(ta, M, K).
+ * stride_c, stride_d : elements between problems' C and D; D blocks must not overlap
+ *   (stride_d >= M * ldd).  Every stride times its element size is a multiple of 16 bytes.
+ * batch == 0: nothing is enqueued; batch == 1 is sp24_mma without a workspace.
+ */
+sp24_status sp24_mma_strided_batched(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc,
+                                     sp24_dtype td, int64_t batch, int64_t M, int64_t N,
+                                     int64_t K, const void *values, int64_t ldv,
+                                     int64_t stride_values, const void *meta,
+                                     int64_t stride_meta, const void *B, int64_t ldb,
+                                     int64_t stride_b, const void *C, int64_t ldc,
+                                     int64_t stride_c, void *D, int64_t ldd, int64_t stride_d,
+                                     int32_t *d_status, void *stream);
+
+/*
  * sp24_mma_i8_noalloc -- the 8-bit integer form of sp24_mma without a workspace argument.
  * The source pages have no counterpart; this entry point exists for callers that cannot
  * allocate device memory at the point of the call: for example a plugin inside a host

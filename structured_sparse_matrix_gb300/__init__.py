@@ -20,7 +20,8 @@ import torch
 
 from . import _build
 
-__all__ = ["lib", "compress", "decompress", "meta_bytes", "meta_prepare", "mma", "workspace_bytes",
+__all__ = ["lib", "compress", "decompress", "meta_bytes", "meta_prepare", "mma", "mma_batched",
+           "workspace_bytes",
            "SparseMatrix", "Sp24Error", "DEV_NOT_2_4", "DEV_TIMEOUT", "DTYPE_CODES"]
 
 DTYPE_CODES = {
@@ -33,7 +34,7 @@ DEV_TIMEOUT = 2
 
 # every symbol include/sp24.h declares
 EXPORTS = ("sp24_compress", "sp24_decompress", "sp24_meta_bytes", "sp24_meta_prepare",
-           "sp24_mma_workspace_bytes", "sp24_mma", "sp24_mma_i8_noalloc",
+           "sp24_mma_workspace_bytes", "sp24_mma", "sp24_mma_strided_batched", "sp24_mma_i8_noalloc",
            "sp24_diag_wait_timeout", "sp24_status_string", "sp24_version")
 
 _lock = threading.Lock()
@@ -71,6 +72,10 @@ def lib():
             L.sp24_mma.restype = i32
             L.sp24_mma.argtypes = [i32, i32, i32, i32, i64, i64, i64, p, i64, p, p, i64, p, i64,
                                    p, i64, p, ctypes.c_size_t, p, p]
+            L.sp24_mma_strided_batched.restype = i32
+            L.sp24_mma_strided_batched.argtypes = [i32, i32, i32, i32, i64, i64, i64, i64, p, i64,
+                                                   i64, p, i64, p, i64, i64, p, i64, i64, p,
+                                                   i64, i64, p, p]
             L.sp24_mma_i8_noalloc.restype = i32
             L.sp24_mma_i8_noalloc.argtypes = [i32, i32, i32, i32, i64, i64, i64, p, i64, p, p,
                                               i64, p, i64, p, i64, p, p]
@@ -177,6 +182,29 @@ def mma(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor, C: torch.Tens
         _ld(C) if C is not None else N, _ptr(out), _ld(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream)))
+    return out
+
+
+def mma_batched(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor,
+                C: torch.Tensor | None = None, out_dtype=torch.float32,
+                out: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """D[b] = expand(values[b], meta[b]) @ B[b] + C[b] for every b, in one launch.
+
+    values: (batch, M, K/2), meta: (batch, sp24_meta_bytes) uint8, B: (batch, K, N),
+    C / out: (batch, M, N); float operands only.  Rows of each matrix must be contiguous
+    in their last dimension (the leading dimension is stride(1))."""
+    batch, M = values.shape[0], values.shape[1]
+    K, N = B.shape[1], B.shape[2]
+    if out is None:
+        out = torch.empty((batch, M, N), dtype=out_dtype, device=B.device)
+    tc = _code(C.dtype) if C is not None else _code(torch.float32)
+    _check("sp24_mma_strided_batched", lib().sp24_mma_strided_batched(
+        _code(values.dtype), _code(B.dtype), tc, _code(out.dtype), batch, M, N, K,
+        _ptr(values), values.stride(1), values.stride(0), _ptr(meta),
+        meta.stride(0) * meta.element_size(), _ptr(B), B.stride(1), B.stride(0), _ptr(C),
+        C.stride(1) if C is not None else N, C.stride(0) if C is not None else 0,
+        _ptr(out), out.stride(1), out.stride(0), _ptr(status), _stream(stream)))
     return out
 
 

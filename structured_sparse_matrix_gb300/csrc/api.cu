@@ -217,6 +217,58 @@ sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
   return static_cast<sp24_status>(rc);
 }
 
+sp24_status sp24_mma_strided_batched(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc,
+                                     sp24_dtype td, int64_t batch, int64_t M, int64_t N,
+                                     int64_t K, const void* values, int64_t ldv,
+                                     int64_t stride_values, const void* meta,
+                                     int64_t stride_meta, const void* B, int64_t ldb,
+                                     int64_t stride_b, const void* C, int64_t ldc,
+                                     int64_t stride_c, void* D, int64_t ldd, int64_t stride_d,
+                                     int32_t* d_status, void* stream) {
+  const bool f16ish = (ta == SP24_F16 || ta == SP24_BF16);
+  if (!(f16ish || is_f8(ta))) return SP24_ERR_UNSUPPORTED;  // float operands only
+  if (f16ish ? tb != ta : !is_f8(tb)) return SP24_ERR_UNSUPPORTED;
+  if (C != nullptr && tc != SP24_F32) return SP24_ERR_UNSUPPORTED;
+  if (td != SP24_F32 && td != SP24_BF16) return SP24_ERR_UNSUPPORTED;
+  if (batch < 0 || M < 0 || N < 0 || K < 0 || (K % 32) != 0) return SP24_ERR_INVALID_ARG;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return SP24_ERR_INVALID_ARG;
+  if (batch == 0 || M == 0 || N == 0) return SP24_OK;
+  // every tile of the launch is numbered with an int
+  if ((M + 127) / 128 * ((N + 31) / 32) * batch > INT32_MAX / 2) return SP24_ERR_INVALID_ARG;
+  if (!D || (K > 0 && (!values || !meta || !B))) return SP24_ERR_INVALID_ARG;
+  if (ldd < N || (C && ldc < N) || (K > 0 && (ldv < K / 2 || ldb < N))) return SP24_ERR_INVALID_ARG;
+  const int esz = dtype_bytes(ta);
+  const int dsz = dtype_bytes(td);
+  if (batch > 1) {
+    // D of different problems must not overlap; the operands are only read
+    if (stride_d < M * ldd) return SP24_ERR_INVALID_ARG;
+    if (C && stride_c < 0) return SP24_ERR_INVALID_ARG;
+    if (K > 0 && (stride_values < 0 || stride_b < 0 ||
+                  size_t(stride_meta) < sp24_meta_bytes(ta, M, K)))
+      return SP24_ERR_INVALID_ARG;
+    if ((stride_d * dsz) % 16 || (C && (stride_c * 4) % 16)) return SP24_ERR_ALIGN;
+    if (K > 0 && ((stride_values * esz) % 16 || (stride_b * esz) % 16 || stride_meta % 16))
+      return SP24_ERR_ALIGN;
+  }
+  if (!aligned16(D) || (ldd * dsz) % 16) return SP24_ERR_ALIGN;
+  if (C && (!aligned16(C) || (ldc * 4) % 16)) return SP24_ERR_ALIGN;
+  if (K > 0 && (!aligned16(values) || !aligned16(meta) || !aligned16(B) || (ldv * esz) % 16 ||
+                (ldb * esz) % 16))
+    return SP24_ERR_ALIGN;
+  int sms = 0;
+  if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
+  BatchArgs ba;
+  ba.count = batch;
+  ba.stride_values = stride_values;
+  ba.stride_meta = stride_meta;
+  ba.stride_b = stride_b;
+  ba.stride_c = stride_c;
+  ba.stride_d = stride_d;
+  const int rc = launch_spmma(ta, tb, tc, td, M, N, K, values, ldv, meta, B, ldb, C, ldc, D, ldd,
+                              nullptr, d_status, sms, static_cast<cudaStream_t>(stream), &ba);
+  return static_cast<sp24_status>(rc);
+}
+
 sp24_status sp24_diag_wait_timeout(int32_t* d_status, uint64_t limit_ns, void* stream) {
   if (!d_status) return SP24_ERR_INVALID_ARG;
   int sms = 0;

@@ -74,11 +74,19 @@ cudaError_t launch_widen(const void* src, int64_t ld_src, void* dst, int64_t ld_
 int64_t int_ws_ldb(int64_t N);
 size_t int_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
-// returns 0 on success, else an sp24_status value
+// A strided batch of equal-shape problems: problem b's operands start at values +
+// b * stride_values, meta + b * stride_meta (bytes), B + b * stride_b, C + b * stride_c,
+// D + b * stride_d (elements of each operand's type).
+struct BatchArgs {
+  int64_t count;
+  int64_t stride_values, stride_meta, stride_b, stride_c, stride_d;
+};
+
+// returns 0 on success, else an sp24_status value; batch == nullptr: one problem
 int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K,
                  const void* values, int64_t ldv, const void* meta, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd, void* workspace,
-                 int32_t* status, int num_sms, cudaStream_t s);
+                 int32_t* status, int num_sms, cudaStream_t s, const BatchArgs* batch = nullptr);
 
 // device properties of the current device, cached; returns false if not sm_103
 bool current_device(int* num_sms);

@@ -58,6 +58,8 @@ struct MmaParams {
   int batoms;    // B boxes loaded per stage and CTA (the narrow variant skips empty ones)
   int M, N, K;
   int mtiles, ntiles, num_kb;  // tiles of the variant (128 or 256 rows, 128 or 256 cols)
+  int batch;                   // problems of equal shape; problem b's C / D start at
+  int64_t stride_c, stride_d;  // C + b * stride_c, D + b * stride_d (elements)
   uint64_t limit_ns;
 };
 
@@ -98,6 +100,18 @@ struct Geo {
 // flight at one time (about one per CTA pair) share a few row blocks of A and column
 // blocks of B that stay in L2 instead of streaming all of A for every column of tiles.
 constexpr int kBandRows = 2048;
+template <int kTileM>
+__device__ __forceinline__ void tile_coords(const MmaParams& p, int t, int& mt, int& nt);
+
+// Tile t of the whole launch: problem b = t / (tiles of one problem), then the tile's
+// (row tile, column tile) inside it.
+template <int kTileM>
+__device__ __forceinline__ void batch_tile(const MmaParams& p, int t, int& b, int& mt, int& nt) {
+  const int per = p.mtiles * p.ntiles;
+  b = t / per;
+  tile_coords<kTileM>(p, t - b * per, mt, nt);
+}
+
 template <int kTileM>
 __device__ __forceinline__ void tile_coords(const MmaParams& p, int t, int& mt, int& nt) {
   constexpr int kBand = kBandRows / kTileM;  // row tiles per band
@@ -150,13 +164,14 @@ __device__ __forceinline__ void ld_f32x8(const float* src, bool v32, float (&c)[
 }
 
 // C (f32) at 8 consecutive columns of one output row; zeros beyond M, N or without C.
-__device__ __forceinline__ void load_c8(float (&c)[8], const MmaParams& p, int row, int col) {
+__device__ __forceinline__ void load_c8(float (&c)[8], const MmaParams& p, int row, int col,
+                                        int64_t cofs) {
   if (p.C == nullptr || row >= p.M || col >= p.N) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) c[j] = 0.f;
     return;
   }
-  const float* crow = static_cast<const float*>(p.C) + int64_t(row) * p.ldc + col;
+  const float* crow = static_cast<const float*>(p.C) + cofs + int64_t(row) * p.ldc + col;
   if (col + 8 <= p.N) {
     ld_f32x8(crow, p.c32 != 0, c);
   } else {
@@ -169,11 +184,12 @@ __device__ __forceinline__ void load_c8(float (&c)[8], const MmaParams& p, int r
 // touched.  Each quad of threads covers one 32-column segment of a row, so a warp's
 // store is 8 whole 128-byte lines (f32 output).
 template <int OUT>
-__device__ __forceinline__ void store8(const float (&v)[8], const MmaParams& p, int row, int col) {
+__device__ __forceinline__ void store8(const float (&v)[8], const MmaParams& p, int row, int col,
+                                       int64_t dofs) {
   if (row >= p.M || col >= p.N) return;
   const bool full = col + 8 <= p.N;
   if constexpr (OUT == 0) {
-    float* d = static_cast<float*>(p.D) + int64_t(row) * p.ldd + col;
+    float* d = static_cast<float*>(p.D) + dofs + int64_t(row) * p.ldd + col;
     if (full) {
       if (p.d32) {
         asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(d), "f"(v[0]),
@@ -189,7 +205,7 @@ __device__ __forceinline__ void store8(const float (&v)[8], const MmaParams& p, 
         if (col + j < p.N) d[j] = v[j];
     }
   } else {
-    __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + int64_t(row) * p.ldd + col;
+    __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + dofs + int64_t(row) * p.ldd + col;
     if (full) {
       __nv_bfloat162 h[4];
 #pragma unroll
@@ -211,13 +227,13 @@ __device__ __forceinline__ void store8(const float (&v)[8], const MmaParams& p, 
 // segment is transposed across the quad, added to C and stored.
 template <int OUT, int kSeg>
 __device__ __forceinline__ void store_row(const uint32_t* r, int e, const MmaParams& p, int row,
-                                          int col0, int q) {
+                                          int col0, int q, int64_t cofs, int64_t dofs) {
   constexpr int kBatch = kSeg < 2 ? kSeg : 2;
 #pragma unroll
   for (int g0 = 0; g0 < kSeg; g0 += kBatch) {
     float c[kBatch][8];
 #pragma unroll
-    for (int g = 0; g < kBatch; ++g) load_c8(c[g], p, row, col0 + 32 * (g0 + g) + 8 * q);
+    for (int g = 0; g < kBatch; ++g) load_c8(c[g], p, row, col0 + 32 * (g0 + g) + 8 * q, cofs);
 #pragma unroll
     for (int g = 0; g < kBatch; ++g) {
       float v[8];
@@ -229,7 +245,7 @@ __device__ __forceinline__ void store_row(const uint32_t* r, int e, const MmaPar
       quad_transpose(v, q);
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] += c[g][j];
-      store8<OUT>(v, p, row, col0 + 32 * (g0 + g) + 8 * q);
+      store8<OUT>(v, p, row, col0 + 32 * (g0 + g) + 8 * q, dofs);
     }
   }
 }
@@ -237,7 +253,7 @@ __device__ __forceinline__ void store_row(const uint32_t* r, int e, const MmaPar
 // Pull this thread's share of the C rows of a coming tile into L2 (the quad leader of
 // each row, one bulk prefetch of up to `cols` columns per row).
 __device__ __forceinline__ void prefetch_c_rows(const MmaParams& p, int row0, int col0, int q,
-                                                int cols) {
+                                                int cols, int64_t cofs) {
   if (p.C == nullptr || q != 0 || col0 >= p.N) return;
   const int ncols = p.N - col0 < cols ? p.N - col0 : cols;
   const uint32_t bytes = uint32_t(ncols * 4) & ~15u;
@@ -248,7 +264,8 @@ __device__ __forceinline__ void prefetch_c_rows(const MmaParams& p, int row0, in
     for (int e = 0; e < 2; ++e) {
       const int row = row0 + 16 * h + 8 * e;
       if (row < p.M)
-        bulk_prefetch_l2(static_cast<const float*>(p.C) + int64_t(row) * p.ldc + col0, bytes);
+        bulk_prefetch_l2(static_cast<const float*>(p.C) + cofs + int64_t(row) * p.ldc + col0,
+                         bytes);
     }
 }
 
@@ -312,7 +329,7 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kABytes;
   uint8_t* sM = sB + kStages * G::kBBytes;
-  const int ntiles_total = p.mtiles * p.ntiles;
+  const int ntiles_total = p.mtiles * p.ntiles * p.batch;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -353,8 +370,8 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
     if (lane == 0) {
       int q = 0;
       for (int t = unit; t < ntiles_total && !*abort; t += nunits) {
-        int mt, nt;
-        tile_coords<G::kTileM>(p, t, mt, nt);
+        int b, mt, nt;
+        batch_tile<G::kTileM>(p, t, b, mt, nt);
         const int mt128 = kPair ? mt * 2 + int(rank) : mt;  // this CTA's 128-row tile
         const int bcol = nt * G::kTileN + int(rank) * G::kBCols;
         const uint32_t tx =
@@ -367,21 +384,21 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
           const int mrow = (mt128 * p.num_kb + kb) * (G::kMetaBytes / 128);
           if constexpr (kPair) {
             const uint32_t fb = mapa(&full_bar[s], 0);
-            tma_load_2d_pair(sA + s * kABytes, &tmA, fb, kx, mt128 * 128);
+            tma_load_3d_pair(sA + s * kABytes, &tmA, fb, kx, mt128 * 128, b);
 #pragma unroll
             for (int a = 0; a < G::kAtoms; ++a)
               if (a < p.batoms)
-                tma_load_2d_pair(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, fb,
-                               bcol + a * G::kAtomN, kb * G::kStageK);
-            tma_load_2d_pair(sM + s * G::kMetaBytes, &tmM, fb, 0, mrow);
+                tma_load_3d_pair(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, fb,
+                                 bcol + a * G::kAtomN, kb * G::kStageK, b);
+            tma_load_3d_pair(sM + s * G::kMetaBytes, &tmM, fb, 0, mrow, b);
           } else {
-            tma_load_2d(sA + s * kABytes, &tmA, &full_bar[s], kx, mt128 * 128);
+            tma_load_3d(sA + s * kABytes, &tmA, &full_bar[s], kx, mt128 * 128, b);
 #pragma unroll
             for (int a = 0; a < G::kAtoms; ++a)
               if (a < p.batoms)
-                tma_load_2d(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, &full_bar[s],
-                          bcol + a * G::kAtomN, kb * G::kStageK);
-            tma_load_2d(sM + s * G::kMetaBytes, &tmM, &full_bar[s], 0, mrow);
+                tma_load_3d(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, &full_bar[s],
+                            bcol + a * G::kAtomN, kb * G::kStageK, b);
+            tma_load_3d(sM + s * G::kMetaBytes, &tmM, &full_bar[s], 0, mrow, b);
           }
         }
       }
@@ -493,8 +510,9 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
         kPair ? mapa(&acc_empty[0], 0) : smem_addr(&acc_empty[0]);
     int local = 0, ichunk = 0;
     for (int t = unit; t < ntiles_total; t += nunits, ++local) {
-      int mt, nt;
-      tile_coords<G::kTileM>(p, t, mt, nt);
+      int b, mt, nt;
+      batch_tile<G::kTileM>(p, t, b, mt, nt);
+      const int64_t cofs = b * p.stride_c, dofs = b * p.stride_d;
       const int abuf = G::kAccBufs == 1 ? 0 : (local & 1);
       const int use = G::kAccBufs == 1 ? local : (local >> 1);
       if constexpr (OUT != 2) {
@@ -558,23 +576,23 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
         const int row0 = mt * G::kTileM + int(rank) * 128 + quad * 32 + (lane >> 2);
         const int col0 = nt * G::kTileN + half * 128;
         if (t + nunits < ntiles_total) {  // the next tile's C, needed one mainloop from now
-          int mt2, nt2;
-          tile_coords<G::kTileM>(p, t + nunits, mt2, nt2);
+          int b2, mt2, nt2;
+          batch_tile<G::kTileM>(p, t + nunits, b2, mt2, nt2);
           prefetch_c_rows(p, mt2 * G::kTileM + int(rank) * 128 + quad * 32 + (lane >> 2),
-                          nt2 * G::kTileN + half * 128, lane & 3, 128);
+                          nt2 * G::kTileN + half * 128, lane & 3, 128, b2 * p.stride_c);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            store_row<OUT, 4>(r[h], e, p, row0 + 16 * h + 8 * e, col0, lane & 3);
+            store_row<OUT, 4>(r[h], e, p, row0 + 16 * h + 8 * e, col0, lane & 3, cofs, dofs);
       } else {
         const int row0 = mt * G::kTileM + quad * 32 + (lane >> 2);
         if (t + nunits < ntiles_total) {  // the next tile's C, needed one mainloop from now
-          int mt2, nt2;
-          tile_coords<G::kTileM>(p, t + nunits, mt2, nt2);
+          int b2, mt2, nt2;
+          batch_tile<G::kTileM>(p, t + nunits, b2, mt2, nt2);
           prefetch_c_rows(p, mt2 * G::kTileM + quad * 32 + (lane >> 2), nt2 * G::kTileN, lane & 3,
-                          G::kTileN);
+                          G::kTileN, b2 * p.stride_c);
         }
         constexpr int kSeg = G::kTileN / 32;
         uint32_t r[2][16 * kSeg];
@@ -590,7 +608,8 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            store_row<OUT, kSeg>(r[h], e, p, row0 + 16 * h + 8 * e, nt * G::kTileN, lane & 3);
+            store_row<OUT, kSeg>(r[h], e, p, row0 + 16 * h + 8 * e, nt * G::kTileN, lane & 3,
+                                 cofs, dofs);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(abuf * sizeof(uint64_t)));
@@ -626,29 +645,35 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 2-D tensor map over a row-major matrix: inner extent `cols` elements of `esz` bytes,
-// `rows` rows, row pitch `pitch_bytes`; box = box_cols x box_rows.
+// 3-D tensor map over `batch` row-major matrices: inner extent `cols` elements of `esz`
+// bytes, `rows` rows, row pitch `pitch_bytes`, matrix pitch `batch_bytes`; box =
+// box_cols x box_rows x 1.
 bool make_tmap(CUtensorMap* m, const void* base, int esz, uint64_t cols, uint64_t rows,
                uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows,
-               CUtensorMapSwizzle swz) {
+               CUtensorMapSwizzle swz, uint64_t batch, uint64_t batch_bytes) {
   auto enc = get_encode();
   if (!enc) return false;
   const CUtensorMapDataType dt = esz == 4   ? CU_TENSOR_MAP_DATA_TYPE_UINT32
                                  : esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
                                             : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {pitch_bytes};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+  cuuint64_t dims[3] = {cols, rows, batch};
+  cuuint64_t strides[2] = {pitch_bytes, batch > 1 ? batch_bytes : rows * pitch_bytes};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
+// Per-problem strides of the operands of a batched call (bytes).
+struct BatchStrides {
+  int64_t values, meta, b;
+};
+
 template <int ESZ, int OUT, bool kPair, bool kNarrow = false, bool kHalfN = false>
 int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const void* B,
-        int64_t ldb, uint32_t idesc, int num_sms, cudaStream_t s) {
+        int64_t ldb, uint32_t idesc, int num_sms, cudaStream_t s, const BatchStrides& bs) {
   using G = Geo<ESZ, kPair, kNarrow, kHalfN>;
   p.mtiles = (p.M + G::kTileM - 1) / G::kTileM;
   p.ntiles = (p.N + G::kTileN - 1) / G::kTileN;
@@ -657,16 +682,18 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
   memset(&tB, 0, sizeof(tB));
   memset(&tM, 0, sizeof(tM));
   if (p.K > 0) {  // with K == 0 no stage is loaded and the maps are never read
+    const uint64_t nb = uint64_t(p.batch);
     if (!make_tmap(&tA, values, ESZ, uint64_t(p.K / 2), uint64_t(p.M), uint64_t(ldv) * ESZ,
-                   128 / ESZ, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+                   128 / ESZ, 128, CU_TENSOR_MAP_SWIZZLE_128B, nb, uint64_t(bs.values)))
       return 4;
     if (!make_tmap(&tB, B, ESZ, uint64_t(p.N), uint64_t(p.K), uint64_t(ldb) * ESZ, G::kAtomN,
-                   G::kStageK, kNarrow ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B))
+                   G::kStageK, kNarrow ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B,
+                   nb, uint64_t(bs.b)))
       return 4;
     // the compact metadata image as rows of 128 bytes; one (tile, stage) block per box
     const uint64_t mrows = uint64_t(meta_mtiles(p.M)) * p.num_kb * (G::kMetaBytes / 128);
     if (!make_tmap(&tM, meta, 4, 32, mrows, 128, 32, G::kMetaBytes / 128,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+                   CU_TENSOR_MAP_SWIZZLE_NONE, nb, uint64_t(bs.meta)))
       return 4;
   }
   // the narrow variant loads only the B atoms that hold columns below N
@@ -686,7 +713,7 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int tiles = p.mtiles * p.ntiles;
+  const int tiles = p.mtiles * p.ntiles * p.batch;
   int units = num_sms;
   if (kPair) {
     cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
@@ -706,17 +733,18 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
 
 template <int ESZ, int OUT>
 int dispatch(const MmaParams& p, const void* values, int64_t ldv, const void* meta,
-             const void* B, int64_t ldb, uint32_t at, uint32_t bt, int num_sms, cudaStream_t s) {
+             const void* B, int64_t ldb, uint32_t at, uint32_t bt, int num_sms, cudaStream_t s,
+             const BatchStrides& bs) {
   if (p.N > 128)  // wide outputs: 256 x 256 tiles on CTA pairs
     return run<ESZ, OUT, true>(p, values, ldv, meta, B, ldb, idesc_sparse_f32(at, bt, 256, 256),
-                               num_sms, s);
+                               num_sms, s, bs);
   if (p.N <= 32) {  // skinny outputs: 128 x 32 tiles, MMA N = N rounded up to 16
     const uint32_t n_mma = uint32_t((p.N + 15) / 16 * 16);
     return run<ESZ, OUT, false, true>(p, values, ldv, meta, B, ldb,
-                                      idesc_sparse_f32(at, bt, 128, n_mma), num_sms, s);
+                                      idesc_sparse_f32(at, bt, 128, n_mma), num_sms, s, bs);
   }
   return run<ESZ, OUT, false>(p, values, ldv, meta, B, ldb, idesc_sparse_f32(at, bt, 128, 128),
-                              num_sms, s);
+                              num_sms, s, bs);
 }
 
 }  // namespace
@@ -732,9 +760,21 @@ size_t int_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K,
                  const void* values, int64_t ldv, const void* meta, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd, void* workspace,
-                 int32_t* status, int num_sms, cudaStream_t s) {
+                 int32_t* status, int num_sms, cudaStream_t s, const BatchArgs* batch) {
   (void)tc;
   MmaParams p;
+  memset(&p, 0, sizeof(p));
+  BatchStrides bs{0, 0, 0};
+  p.batch = 1;
+  if (batch != nullptr && batch->count > 1) {
+    const int esz = dtype_bytes(ta);
+    p.batch = int(batch->count);
+    bs.values = batch->stride_values * esz;
+    bs.meta = batch->stride_meta;
+    bs.b = batch->stride_b * esz;
+    p.stride_c = batch->stride_c;
+    p.stride_d = batch->stride_d;
+  }
   p.C = C;
   p.D = D;
   p.ldc = ldc;
@@ -764,7 +804,7 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
     }
     // kind::f16 with bf16 operands: type code 1 for A and B
     return run<2, 2, true, false, true>(p, wa, K / 2, meta, wb, ldbw,
-                                        idesc_sparse_f32(1, 1, 256, 128), num_sms, s);
+                                        idesc_sparse_f32(1, 1, 256, 128), num_sms, s, bs);
   }
   const int esz = dtype_bytes(ta);
   // kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2
@@ -772,10 +812,10 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   const uint32_t bt = (tb == kBF16 || tb == kE5M2) ? 1u : 0u;
   const bool out_bf16 = td == kBF16;
   if (esz == 2)
-    return out_bf16 ? dispatch<2, 1>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s)
-                    : dispatch<2, 0>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s);
-  return out_bf16 ? dispatch<1, 1>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s)
-                  : dispatch<1, 0>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s);
+    return out_bf16 ? dispatch<2, 1>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s, bs)
+                    : dispatch<2, 0>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s, bs);
+  return out_bf16 ? dispatch<1, 1>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s, bs)
+                  : dispatch<1, 0>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s, bs);
 }
 
 }  // namespace sp24

@@ -122,6 +122,31 @@ def test_mma_argument_checks():
     assert _mma(N=0) == OK
 
 
+def _bmma(ta=BF16, tb=BF16, tc=F32, td=F32, batch=3, M=128, N=128, K=128, sv=None, sm=None,
+          sb=None, sc=None, sd=None, C=FAKE, D=FAKE):
+    M_, N_, K_ = M, N, K
+    sv = M_ * K_ // 2 if sv is None else sv
+    sm = sp.lib().sp24_meta_bytes(ta, M_, K_) if sm is None else sm
+    sb = K_ * N_ if sb is None else sb
+    sc = M_ * N_ if sc is None else sc
+    sd = M_ * N_ if sd is None else sd
+    return sp.lib().sp24_mma_strided_batched(ta, tb, tc, td, batch, M, N, K, FAKE, K // 2, sv,
+                                             FAKE, sm, FAKE, N, sb, C, N, sc, D, N, sd, None,
+                                             None)
+
+
+def test_batched_argument_checks():
+    assert _bmma(ta=S8, tb=S8, tc=S32, td=S32) == UNSUPPORTED   # float operands only
+    assert _bmma(ta=F16, tb=BF16) == UNSUPPORTED
+    assert _bmma(batch=-1) == INVALID
+    assert _bmma(batch=0) == OK                                   # nothing to do
+    assert _bmma(sd=128 * 128 - 4) == INVALID                     # D blocks overlap
+    assert _bmma(sm=1024) == INVALID                              # smaller than one image
+    assert _bmma(sv=128 * 64 + 4) == ALIGN                        # 8200-byte stride
+    assert _bmma(sd=128 * 128 + 2) == ALIGN
+    assert _bmma(D=None) == INVALID
+
+
 def test_meta_prepare_argument_checks():
     L = sp.lib()
     assert L.sp24_meta_prepare(F32, 64, 128, FAKE, 4, FAKE, None) == UNSUPPORTED

@@ -92,6 +92,41 @@ def test_padded_leading_dimensions_and_ragged_N(ta):
     assert np.all(Dh[:, N:] == 7.0), "wrote past N"
 
 
+@pytest.mark.parametrize("ta,tb,M,N,K", [("bf16", "bf16", 200, 304, 384),   # pair tiles
+                                        ("f16", "f16", 130, 96, 256),     # single tiles
+                                        ("e4m3", "e5m2", 257, 16, 512),   # narrow tiles
+                                        ("bf16", "bf16", 64, 272, 0)])    # K = 0: D = C
+def test_strided_batch(ta, tb, M, N, K):
+    # four problems of one shape in one launch, each against the oracle, and bit for bit
+    # equal to four single calls (same tiles, same accumulation order)
+    cases = [inputs.case(ta, tb, M, N, K, seed=500 + i, tc="f32") for i in range(4)]
+    Kc = max(K, 32)
+    vals, metas = [], []
+    for c in cases:
+        if K > 0:
+            v, ix = sp.compress(dev(c["A"]), mode="mask", mask=dev(c["mask"]))
+            vals.append(v)
+            metas.append(sp.meta_prepare(ix, c["A"].dtype, M, K))
+        else:
+            vals.append(torch.zeros((M, Kc // 2), dtype=c["A"].dtype, device="cuda"))
+            metas.append(torch.zeros(16, dtype=torch.uint8, device="cuda"))
+    V = torch.stack(vals)
+    MT = torch.stack(metas)
+    Bs = torch.stack([dev(c["B"]) for c in cases])
+    Cs = torch.stack([dev(c["C"]) for c in cases])
+    D = sp.mma_batched(V, MT, Bs, Cs)
+    singles = [sp.mma(vals[i], metas[i], Bs[i], Cs[i]) for i in range(4)]
+    torch.cuda.synchronize()
+    for i, c in enumerate(cases):
+        assert torch.equal(D[i], singles[i]), f"problem {i} differs from the single call"
+        if K == 0:
+            assert torch.equal(D[i], Cs[i])
+            continue
+        v, ix, _ = oracle.compress(inputs.bits(c["A"]), ta, "mask", mask=c["mask"].numpy())
+        R, S = oracle.mma_f64(v, ix, inputs.bits(c["B"]), c["C"].numpy(), ta, tb, K)
+        check_float(D[i].cpu().numpy(), R, S, False, f"batched problem {i}")
+
+
 def test_identity_B_returns_A_plus_C():
     # the pages' verification idiom: with B = I the product is A itself
     M, K = 256, 256
