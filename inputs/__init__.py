@@ -105,6 +105,26 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.numpy()
 
 
+def gen_nibbles(shape, g: torch.Generator) -> np.ndarray:
+    """Uniform 4-bit patterns (0..15), one per byte: the oracle's 4-bit layout."""
+    return torch.randint(0, 16, shape, generator=g).numpy().astype(np.uint8)
+
+
+def pack4(nibbles) -> np.ndarray:
+    """Two 4-bit elements per byte, element 2i in the low nibble (the library's storage)."""
+    a = np.asarray(nibbles, dtype=np.uint8)
+    return (a[..., 0::2] & 0xF) | ((a[..., 1::2] & 0xF) << 4)
+
+
+def unpack4(packed) -> np.ndarray:
+    """Inverse of pack4: one 4-bit element per byte."""
+    a = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(a.shape[:-1] + (2 * a.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = a & 0xF
+    out[..., 1::2] = a >> 4
+    return out
+
+
 def case(ta: str, tb: str, M: int, N: int, K: int, *, seed: int = 0, tc: str | None = None,
          dist: str = "normal", mask: str = "random", b_dist: str | None = None,
          c_dist: str | None = None) -> dict:

@@ -26,9 +26,11 @@ _HDR = os.path.join(_HERE, "sp24_oracle.h")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
-DTYPES = {"f16": 0, "bf16": 1, "e4m3": 2, "e5m2": 3, "s8": 4, "u8": 5, "f32": 6, "s32": 7}
+DTYPES = {"f16": 0, "bf16": 1, "e4m3": 2, "e5m2": 3, "s8": 4, "u8": 5, "f32": 6, "s32": 7,
+          "s4": 8, "u4": 9}  # 4-bit: one element per byte, pattern in the low nibble
 MODES = {"exact": 0, "mask": 1, "magnitude": 2}
-ELEM_BYTES = {"f16": 2, "bf16": 2, "e4m3": 1, "e5m2": 1, "s8": 1, "u8": 1, "f32": 4, "s32": 4}
+ELEM_BYTES = {"f16": 2, "bf16": 2, "e4m3": 1, "e5m2": 1, "s8": 1, "u8": 1, "f32": 4, "s32": 4,
+              "s4": 1, "u4": 1}
 FLAG_NOT_2_4 = 1
 
 _lock = threading.Lock()
@@ -190,7 +192,7 @@ def mma_f64(values, index, B, C, ta: str, tb: str, K: int, tc: str = "f32", rows
 
 
 def mma_i64(values, index, B, C, ta: str, tb: str, K: int, rows=None) -> np.ndarray:
-    """Exact int64 D = expand(values, index) @ B + C for s8/u8 operands."""
+    """Exact int64 D = expand(values, index) @ B + C for s8/u8/s4/u4 operands."""
     values, B = _c(values), _c(B)
     index = _c(np.asarray(index, dtype=np.uint32))
     C = _c(C)

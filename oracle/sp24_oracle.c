@@ -35,6 +35,8 @@ int or_elem_bytes(int dtype)
     case OR_E5M2:
     case OR_S8:
     case OR_U8:
+    case OR_S4: /* one element per byte in the oracle's arrays */
+    case OR_U4:
         return 1;
     case OR_F32:
     case OR_S32:
@@ -88,6 +90,10 @@ double or_decode(int dtype, uint32_t bits)
         return (double)(int8_t)(uint8_t)bits;
     case OR_U8:
         return (double)(uint8_t)bits;
+    case OR_S4: /* 4-bit two's complement: -8 .. 7 ("iu4" with the sign flag set) */
+        return (double)((int)(bits & 0xfu) - (int)((bits & 0x8u) << 1));
+    case OR_U4:
+        return (double)(bits & 0xfu);
     case OR_F32:
         return dec_float(bits, 8, 23, 127, 1);
     case OR_S32:
@@ -340,14 +346,16 @@ int or_mma_f64(int ta, int tb, int64_t M, int64_t N, int64_t K, const void *valu
     return 0;
 }
 
-/* Integer form: s8/u8 operands (a_neg / b_neg pick signed or unsigned, "Common
- * parameters"), exact int64 sums, C of type s32 or absent. */
+static int is_int_ab(int t) { return t == OR_S8 || t == OR_U8 || t == OR_S4 || t == OR_U4; }
+
+/* Integer form: 8- or 4-bit operands (a_neg / b_neg pick signed or unsigned, "Common
+ * parameters"; 4-bit is the pages' iu4), exact int64 sums, C of type s32 or absent. */
 int or_mma_i64(int ta, int tb, int64_t M, int64_t N, int64_t K, const void *values,
                int64_t ldv, const uint32_t *index, int64_t ldi, const void *B,
                int64_t ldb, const void *C, int64_t ldc, const int64_t *rows,
                int64_t nrows, int64_t *D)
 {
-    if ((ta != OR_S8 && ta != OR_U8) || (tb != OR_S8 && tb != OR_U8))
+    if (!is_int_ab(ta) || !is_int_ab(tb))
         return -1;
     (void)M;
 #pragma omp parallel
@@ -366,8 +374,8 @@ int or_mma_i64(int ta, int tb, int64_t M, int64_t N, int64_t K, const void *valu
                 int p0 = (int)(nib & 3u), p1 = (int)(nib >> 2);
                 uint32_t v0 = load_bits(values, 1, i * ldv + 2 * g);
                 uint32_t v1 = load_bits(values, 1, i * ldv + 2 * g + 1);
-                arow[4 * g + p0] = ta == OR_S8 ? (int64_t)(int8_t)v0 : (int64_t)v0;
-                arow[4 * g + p1] = ta == OR_S8 ? (int64_t)(int8_t)v1 : (int64_t)v1;
+                arow[4 * g + p0] = (int64_t)or_decode(ta, v0);
+                arow[4 * g + p1] = (int64_t)or_decode(ta, v1);
             }
             for (int64_t k = 0; k < K; ++k) {
                 int64_t a = arow[k];
@@ -375,7 +383,7 @@ int or_mma_i64(int ta, int tb, int64_t M, int64_t N, int64_t K, const void *valu
                     continue;
                 const uint8_t *brow = (const uint8_t *)B + k * ldb;
                 for (int64_t j = 0; j < N; ++j) {
-                    int64_t b = tb == OR_S8 ? (int64_t)(int8_t)brow[j] : (int64_t)brow[j];
+                    int64_t b = (int64_t)or_decode(tb, brow[j]);
                     drow[j] += a * b;
                 }
             }

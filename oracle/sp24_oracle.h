@@ -36,7 +36,10 @@ enum {
     OR_S8 = 4,    /* signed 8-bit integer   (a_neg / b_neg = true)       */
     OR_U8 = 5,    /* unsigned 8-bit integer (a_neg / b_neg = false)      */
     OR_F32 = 6,   /* IEEE binary32 (C operand only)                      */
-    OR_S32 = 7    /* 32-bit two's complement (C operand only)            */
+    OR_S32 = 7,   /* 32-bit two's complement (C operand only)            */
+    OR_S4 = 8,    /* signed 4-bit integer (the pages' iu4 with a_neg / b_neg set),
+                     one element per byte here, pattern in the low nibble */
+    OR_U4 = 9     /* unsigned 4-bit integer, stored like OR_S4            */
 };
 
 /* compression modes */
@@ -96,7 +99,7 @@ int or_mma_f64(int ta, int tb, int64_t M, int64_t N, int64_t K, const void *valu
                int64_t ldb, int tc, const void *C, int64_t ldc, const int64_t *rows,
                int64_t nrows, double *D, double *S);
 
-/* Integer variant: exact int64 sums for S8/U8 operands (C of type OR_S32 or NULL). */
+/* Integer variant: exact int64 sums for S8/U8/S4/U4 operands (C of type OR_S32 or NULL). */
 int or_mma_i64(int ta, int tb, int64_t M, int64_t N, int64_t K, const void *values,
                int64_t ldv, const uint32_t *index, int64_t ldi, const void *B,
                int64_t ldb, const void *C, int64_t ldc, const int64_t *rows,

@@ -74,6 +74,15 @@ def test_decode_integers():
     assert np.array_equal(oracle.decode("u8", b), b.astype(np.float64))
 
 
+def test_decode_4bit_integers_closed_form():
+    # the pages' iu4: a 4-bit field, two's complement when the sign flag is set
+    n = np.arange(16, dtype=np.uint8)
+    assert list(oracle.decode("s4", n)) == [0, 1, 2, 3, 4, 5, 6, 7, -8, -7, -6, -5, -4, -3, -2, -1]
+    assert list(oracle.decode("u4", n)) == list(range(16))
+    # only the low nibble of the stored byte is the element
+    assert oracle.decode("s4", [0xF8])[0] == -8.0 and oracle.decode("u4", [0x37])[0] == 7.0
+
+
 # --- bf16 rounding: pinned to torch's float32 -> bfloat16 (RNE) and to tie cases -------
 
 def test_round_bf16_matches_torch_on_float32_values():
@@ -156,6 +165,19 @@ def test_round_trip_exact_mode(dtype):
     _check_index_matches_mask(index, m.numpy())
 
 
+@pytest.mark.parametrize("dtype", ["s4", "u4"])
+def test_round_trip_exact_mode_4bit(dtype):
+    M, K = 24, 96
+    m = inputs.keep_mask(M, K, inputs.gen(11)).numpy()
+    A = inputs.gen_nibbles((M, K), inputs.gen(13))
+    A[A == 0] = 1                      # kept values non-zero: exactly two per group
+    A[~m] = 0
+    values, index, flags = oracle.compress(A, dtype, "exact")
+    assert not flags.any()
+    assert np.array_equal(oracle.decompress(values, index, dtype, K), A)
+    _check_index_matches_mask(index, m)
+
+
 def _check_index_matches_mask(index, mask):
     M, K = mask.shape
     for i in range(M):
@@ -221,6 +243,24 @@ def test_magnitude_prune_brute_force_all_small_tuples():
                 # every dropped |x| <= every kept |x|; at equality the dropped is higher
                 assert abs(t[d]) < abs(t[k]) or (abs(t[d]) == abs(t[k]) and d > k), (t, nib)
         assert values[0, 2 * g] == A[0, 4 * g + p0] and values[0, 2 * g + 1] == A[0, 4 * g + p1]
+
+
+def test_magnitude_prune_brute_force_all_s4_groups():
+    # every group of four 4-bit two's-complement values (16^4): dropped |x| <= kept |x|,
+    # ties drop the higher position; -8 has magnitude 8, the largest
+    tuples = np.array(list(itertools.product(range(16), repeat=4)), dtype=np.uint8)
+    A = tuples.reshape(1, -1)
+    values, index, _ = oracle.compress(A, "s4", "magnitude")
+    mag = np.abs(oracle.decode("s4", tuples))
+    nib = (index[0][np.arange(len(tuples)) // 8] >> (4 * (np.arange(len(tuples)) % 8))) & 0xF
+    p0, p1 = nib & 3, nib >> 2
+    assert np.all(p0 < p1)
+    for g in range(len(tuples)):
+        kept = {int(p0[g]), int(p1[g])}
+        for d in set(range(4)) - kept:
+            for k in kept:
+                assert mag[g, d] < mag[g, k] or (mag[g, d] == mag[g, k] and d > k)
+    assert np.array_equal(values[0, 0::2], A[0, 4 * np.arange(len(tuples)) + p0])
 
 
 def test_magnitude_prune_matches_sorted_selection_bf16():
@@ -303,6 +343,28 @@ def test_integer_extremes_exact():
         values, index, _ = oracle.compress(A, ta, "mask", mask=m)
         D = oracle.mma_i64(values, index, Bi.astype(np.int8), None, ta, "s8", K)
         assert np.array_equal(D, Ai @ Bi)
+
+
+@pytest.mark.parametrize("ta", ["s4", "u4"])
+def test_mma_i64_4bit_matches_integer_dense_product(ta):
+    M, N, K = 33, 17, 128
+    m = inputs.keep_mask(M, K, inputs.gen(21)).numpy()
+    A = inputs.gen_nibbles((M, K), inputs.gen(22))
+    A[~m] = 0
+    B = inputs.gen_nibbles((K, N), inputs.gen(23))
+    C = np.random.default_rng(24).integers(-2**20, 2**20, (M, N)).astype(np.int32)
+    values, index, _ = oracle.compress(A, ta, "mask", mask=m)
+    D = oracle.mma_i64(values, index, B, C, ta, "s4", K)
+    # the same product written with numpy's own 4-bit decoding
+    Ai = A.astype(np.int64) - (16 * (A >= 8) if ta == "s4" else 0)
+    Bi = B.astype(np.int64) - 16 * (B >= 8)
+    assert np.array_equal(D, C.astype(np.int64) + Ai @ Bi)
+    # extremes: every kept a at -8 (or 15) and every b = -8
+    Ae = np.where(m, 8 if ta == "s4" else 15, 0).astype(np.uint8)
+    v2, i2, _ = oracle.compress(Ae, ta, "mask", mask=m)
+    D2 = oracle.mma_i64(v2, i2, np.full((K, N), 8, np.uint8), None, ta, "s4", K)
+    aval = -8 if ta == "s4" else 15
+    assert np.array_equal(D2, (m * aval).astype(np.int64) @ np.full((K, N), -8))
 
 
 def test_row_subset_equals_full_rows():
