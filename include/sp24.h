@@ -44,7 +44,11 @@ extern "C" {
 /* Element types.  F16 = IEEE binary16, BF16 = bfloat16, E4M3 = OCP FP8 E4M3 (the
  * pages' "FP8"), E5M2 = OCP FP8 E5M2 (the pages' "BF8"), S8 / U8 = signed / unsigned
  * 8-bit integers (the a_neg / b_neg choice of "RDNA4 dense WMMA builtins", "Common
- * parameters"), F32 / S32 = accumulator and output types. */
+ * parameters"), F32 / S32 = accumulator and output types, S4 / U4 = signed (-8..7) /
+ * unsigned (0..15) 4-bit integers ("RDNA4 sparse WMMA builtins", "INT4 and UINT4
+ * inputs").  4-bit elements are stored two per byte, element 2i in the low nibble and
+ * 2i+1 in the high nibble; their leading dimensions still count elements (a row pitch
+ * of ld elements is ld/2 bytes). */
 typedef enum sp24_dtype {
     SP24_F16 = 0,
     SP24_BF16 = 1,
@@ -53,7 +57,9 @@ typedef enum sp24_dtype {
     SP24_S8 = 4,
     SP24_U8 = 5,
     SP24_F32 = 6,
-    SP24_S32 = 7
+    SP24_S32 = 7,
+    SP24_S4 = 8,
+    SP24_U4 = 9
 } sp24_dtype;
 
 typedef enum sp24_status {
@@ -92,7 +98,7 @@ typedef enum sp24_mode {
  * (the nibble order is the one the CDNA example's literal 0x88 fixes for positions 0
  * and 2: the lower position in the low two bits).
  *
- * t      : SP24_F16, SP24_BF16, SP24_E4M3, SP24_E5M2, SP24_S8 or SP24_U8.
+ * t      : SP24_F16, SP24_BF16, SP24_E4M3, SP24_E5M2, SP24_S8, SP24_U8, SP24_S4 or SP24_U4.
  * M, K   : rows and dense columns of A; K % 32 == 0 (one index word per 32 columns).
  * A      : device, M x K elements of type t, leading dimension lda >= K.
  * mask   : device, M x K bytes (ldm >= K), used only in SP24_MODE_MASK, else ignored.
@@ -102,8 +108,9 @@ typedef enum sp24_mode {
  * adds the lowest free positions, with more than two it keeps the two lowest and sets
  * SP24_DEV_NOT_2_4.  MASK keeps the marked positions by the same rules and sets
  * SP24_DEV_NOT_2_4 unless exactly two are marked.  MAGNITUDE never flags.
- * Alignment: A, values and mask 16-byte aligned; lda*size(t), ldv*size(t) and ldm
- * multiples of 16 bytes; index 4-byte aligned.  Otherwise SP24_ERR_ALIGN.
+ * Alignment: A, values and mask 16-byte aligned; the row pitches of A and values (lda
+ * and ldv elements of t) and ldm multiples of 16 bytes (for S4 / U4: lda and ldv
+ * multiples of 32); index 4-byte aligned.  Otherwise SP24_ERR_ALIGN.
  */
 sp24_status sp24_compress(sp24_dtype t, int64_t M, int64_t K, const void *A, int64_t lda,
                           const uint8_t *mask, int64_t ldm, sp24_mode mode, void *values,
@@ -133,8 +140,8 @@ size_t sp24_meta_bytes(sp24_dtype t, int64_t M, int64_t K);
  * the K step; pad groups get the valid pattern {0,1} and their values are zero, so they
  * add nothing.  The image is a format private to sp24_mma (sp24_meta_bytes() gives its
  * size); the canonical index stays the interchange format.
- * 8-bit integer types use the layout of the 16-bit types (their product runs on the
- * bf16 tensor path).
+ * 8- and 4-bit integer types use the layout of the 16-bit types (their product runs on
+ * the bf16 tensor path).
  * index : device, M x K/32 words, ldi >= K/32, 4-byte aligned.
  * meta  : device, sp24_meta_bytes(t, M, K) bytes, 16-byte aligned.
  */
@@ -143,8 +150,8 @@ sp24_status sp24_meta_prepare(sp24_dtype t, int64_t M, int64_t K, const uint32_t
 
 /*
  * sp24_mma_workspace_bytes -- device workspace sp24_mma needs for (ta, tb, M, N, K): for
- * 8-bit integer operands the bytes of both operands widened to bf16 (A_c: M x K/2, B:
- * K x N with the row pitch rounded up to 8 elements); 0 for float operands.
+ * integer operands the bytes of both operands widened to bf16 (A_c: M x K/2, B: K x N
+ * with the row pitch rounded up to 8 elements); 0 for float operands.
  */
 size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t N, int64_t K);
 
@@ -158,6 +165,7 @@ size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t
  *   (E4M3, E5M2) and (E5M2, E4M3)   -> f32 accumulate, tc in {F32, none}, td in {F32, BF16}
  *   (S8, S8) and (U8, S8)           -> exact integer result, tc in {S32, none}, td = S32,
  *                                      32-bit two's-complement wrap, no clamp
+ *   (S4 or U4, S4 or U4)            -> the same, for 4-bit operands (any sign mix)
  * "none" for tc means C == NULL (treated as zero); tc is then ignored.
  * M, N, K : D is M x N; K is the dense depth, K % 32 == 0.
  * values  : device, M x K/2 of ta (ldv >= K/2), from sp24_compress.
@@ -167,10 +175,11 @@ size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t
  * workspace, workspace_bytes : device scratch of at least sp24_mma_workspace_bytes(),
  *           16-byte aligned, owned by the caller and used only by this call's kernels
  *           (integer operands only; NULL / 0 otherwise).
+ * Leading dimensions count elements, also for 4-bit types (two per byte).
  * Accumulation: floats in f32 on the tensor cores; a BF16 D is the f32 result rounded to
  * nearest-even.  Integers are widened to bf16 (exact) and accumulated in f32 in chunks of
  * 1024 dense K (every chunk sum is an exact integer below 2^24), the chunks then summed in
- * int32: the result is exact.
+ * int32: the result is exact.  (A u8 x u8 chunk sum could pass 2^24, hence B = S8.)
  * Alignment: values, meta, B, C, D 16-byte aligned, every row pitch a multiple of 16 bytes.
  * Device status: SP24_DEV_TIMEOUT if a pipeline wait gave up (D is then invalid).
  */

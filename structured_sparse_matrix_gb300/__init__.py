@@ -9,6 +9,11 @@ missing or no sm_103 device is current, calls raise.
     values, index = compress(A, mode="mask", mask=keep)     # A: M x K on cuda
     meta = meta_prepare(index, A.dtype, M, K)
     D = mma(values, meta, B, C, out_dtype=torch.float32)     # D = A_sp @ B + C
+
+4-bit integer operands ("s4", "u4") travel as uint8 tensors holding two elements per
+byte (element 2i in the low nibble); the functions take them with ``elem="s4"`` (or
+``a_elem`` / ``b_elem`` for ``mma``), and their shapes count bytes along the packed
+dimension (A: M x K/2 bytes, values: M x K/4 bytes, B: K x N/2 bytes).
 """
 from __future__ import annotations
 
@@ -28,6 +33,10 @@ DTYPE_CODES = {
     torch.float16: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2, torch.float8_e5m2: 3,
     torch.int8: 4, torch.uint8: 5, torch.float32: 6, torch.int32: 7,
 }
+# 4-bit types have no torch dtype: they are named by string
+NAMED_CODES = {"f16": 0, "bf16": 1, "e4m3": 2, "e5m2": 3, "s8": 4, "u8": 5, "f32": 6, "s32": 7,
+               "s4": 8, "u4": 9}
+PACKED4 = ("s4", "u4")
 MODES = {"exact": 0, "mask": 1, "magnitude": 2}
 DEV_NOT_2_4 = 1
 DEV_TIMEOUT = 2
@@ -103,22 +112,47 @@ def _ptr(t):
 
 
 def _code(dtype):
+    if isinstance(dtype, str):
+        if dtype not in NAMED_CODES:
+            raise TypeError(f"unsupported element type {dtype!r}")
+        return NAMED_CODES[dtype]
     if dtype not in DTYPE_CODES:
         raise TypeError(f"unsupported element type {dtype}")
     return DTYPE_CODES[dtype]
 
 
-def _ld(t):
+def _ld(t, elem=None):
+    """Leading dimension in elements (4-bit types: two per byte of a uint8 tensor)."""
     if t.dim() != 2 or t.stride(1) != 1:
         raise ValueError("expected a 2-D row-major tensor (unit column stride)")
-    return t.stride(0)
+    return t.stride(0) * (2 if elem in PACKED4 else 1)
+
+
+def _elem_code(t, elem):
+    """Element code of tensor t, read as 4-bit elements when elem is "s4" / "u4"."""
+    if elem is None:
+        return _code(t.dtype)
+    if elem not in PACKED4:
+        raise ValueError(f"elem must be None, 's4' or 'u4', not {elem!r}")
+    if t.dtype != torch.uint8:
+        raise TypeError("4-bit operands travel as uint8 tensors (two elements per byte)")
+    return _code(elem)
 
 
 def compress(A: torch.Tensor, mode: str = "exact", mask: torch.Tensor | None = None,
-             status: torch.Tensor | None = None, stream=None):
-    """Dense M x K (2:4 along K) -> (values M x K/2, index M x K/32 int32 words)."""
-    M, K = A.shape
-    values = torch.empty((M, K // 2), dtype=A.dtype, device=A.device)
+             status: torch.Tensor | None = None, stream=None, elem: str | None = None):
+    """Dense M x K (2:4 along K) -> (values M x K/2, index M x K/32 int32 words).
+
+    elem="s4" / "u4": A is M x K/2 packed bytes and values M x K/4 packed bytes."""
+    t = _elem_code(A, elem)
+    per = 2 if elem in PACKED4 else 1
+    M, K = A.shape[0], A.shape[1] * per
+    vcols = K // 2 // per
+    if per == 2:  # K/4 bytes a row: pad the pitch to 16 bytes (K = 32 gives 8)
+        values = torch.empty((M, (vcols + 15) // 16 * 16), dtype=A.dtype,
+                             device=A.device)[:, :vcols]
+    else:
+        values = torch.empty((M, vcols), dtype=A.dtype, device=A.device)
     index = torch.empty((M, K // 32), dtype=torch.int32, device=A.device)
     m = None
     ldm = K
@@ -128,17 +162,21 @@ def compress(A: torch.Tensor, mode: str = "exact", mask: torch.Tensor | None = N
         m = mask.to(torch.uint8) if mask.dtype != torch.uint8 else mask
         ldm = _ld(m)
     _check("sp24_compress", lib().sp24_compress(
-        _code(A.dtype), M, K, _ptr(A), _ld(A), _ptr(m), ldm, MODES[mode], _ptr(values),
-        _ld(values), _ptr(index), _ld(index), _ptr(status), _stream(stream)))
+        t, M, K, _ptr(A), _ld(A, elem), _ptr(m), ldm, MODES[mode], _ptr(values),
+        _ld(values, elem), _ptr(index), _ld(index), _ptr(status), _stream(stream)))
     return values, index
 
 
-def decompress(values: torch.Tensor, index: torch.Tensor, K: int, stream=None) -> torch.Tensor:
+def decompress(values: torch.Tensor, index: torch.Tensor, K: int, stream=None,
+               elem: str | None = None) -> torch.Tensor:
+    """The dense M x K operand (elem="s4" / "u4": M x K/2 packed bytes)."""
+    t = _elem_code(values, elem)
+    per = 2 if elem in PACKED4 else 1
     M = values.shape[0]
-    A = torch.empty((M, K), dtype=values.dtype, device=values.device)
+    A = torch.empty((M, K // per), dtype=values.dtype, device=values.device)
     _check("sp24_decompress", lib().sp24_decompress(
-        _code(values.dtype), M, K, _ptr(values), _ld(values), _ptr(index), _ld(index), _ptr(A),
-        _ld(A), _stream(stream)))
+        t, M, K, _ptr(values), _ld(values, elem), _ptr(index), _ld(index), _ptr(A),
+        _ld(A, elem), _stream(stream)))
     return A
 
 
@@ -155,30 +193,35 @@ def meta_prepare(index: torch.Tensor, dtype, M: int, K: int, stream=None) -> tor
 
 
 def workspace_bytes(a_dtype, b_dtype, M: int, N: int, K: int) -> int:
-    """Device workspace sp24_mma needs (non-zero only for 8-bit integer operands)."""
+    """Device workspace sp24_mma needs (non-zero only for integer operands); the types
+    are torch dtypes or names ("s4", "u4", ...)."""
     return int(lib().sp24_mma_workspace_bytes(_code(a_dtype), _code(b_dtype), M, N, K))
 
 
 def mma(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
         out_dtype=None, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-        status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        status: torch.Tensor | None = None, stream=None, a_elem: str | None = None,
+        b_elem: str | None = None) -> torch.Tensor:
     """D = expand(values, meta) @ B + C  (values M x K/2, B K x N, C/D M x N).
 
-    Float operands give f32 (default) or bf16 output; 8-bit integer operands give int32."""
+    Float operands give f32 (default) or bf16 output; integer operands give int32.
+    a_elem / b_elem = "s4" / "u4": that operand is packed 4-bit (values M x K/4 bytes,
+    B K x N/2 bytes)."""
+    ta, tb = _elem_code(values, a_elem), _elem_code(B, b_elem)
     M = values.shape[0]
-    K, N = B.shape
+    K, N = B.shape[0], B.shape[1] * (2 if b_elem in PACKED4 else 1)
     integer = values.dtype in (torch.int8, torch.uint8)
     if out is None:
         if out_dtype is None:
             out_dtype = torch.int32 if integer else torch.float32
         out = torch.empty((M, N), dtype=out_dtype, device=B.device)
     tc = _code(C.dtype) if C is not None else _code(out.dtype if integer else torch.float32)
-    ws_bytes = workspace_bytes(values.dtype, B.dtype, M, N, K)
+    ws_bytes = int(lib().sp24_mma_workspace_bytes(ta, tb, M, N, K))
     if ws_bytes and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=B.device)
     _check("sp24_mma", lib().sp24_mma(
-        _code(values.dtype), _code(B.dtype), tc, _code(out.dtype), M, N, K,
-        _ptr(values), _ld(values), _ptr(meta), _ptr(B), _ld(B), _ptr(C),
+        ta, tb, tc, _code(out.dtype), M, N, K,
+        _ptr(values), _ld(values, a_elem), _ptr(meta), _ptr(B), _ld(B, b_elem), _ptr(C),
         _ld(C) if C is not None else N, _ptr(out), _ld(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream)))

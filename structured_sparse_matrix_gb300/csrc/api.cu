@@ -88,20 +88,19 @@ sp24_status sp24_compress(sp24_dtype t, int64_t M, int64_t K, const void* A, int
   if (!A || !values || !index || (mode == SP24_MODE_MASK && !mask)) return SP24_ERR_INVALID_ARG;
   if (lda < K || ldv < K / 2 || ldi < K / 32 || (mode == SP24_MODE_MASK && ldm < K))
     return SP24_ERR_INVALID_ARG;
-  const int esz = dtype_bytes(t);
   if (!aligned16(A) || !aligned16(values) || (reinterpret_cast<uintptr_t>(index) & 3u) ||
-      (lda * esz) % 16 || (ldv * esz) % 16)
+      !ld_ok16(t, lda) || !ld_ok16(t, ldv))
     return SP24_ERR_ALIGN;
   if (mode == SP24_MODE_MASK && (!aligned16(mask) || ldm % 16)) return SP24_ERR_ALIGN;
   int sms = 0;
   if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
   CompressArgs a;
   a.A = static_cast<const uint8_t*>(A);
-  a.lda_bytes = lda * esz;
+  a.lda_bytes = ld_bytes(t, lda);
   a.mask = mask;
   a.ldm = ldm;
   a.values = static_cast<uint8_t*>(values);
-  a.ldv_bytes = ldv * esz;
+  a.ldv_bytes = ld_bytes(t, ldv);
   a.index = index;
   a.ldi = ldi;
   a.M = M;
@@ -120,19 +119,18 @@ sp24_status sp24_decompress(sp24_dtype t, int64_t M, int64_t K, const void* valu
   if (M == 0 || K == 0) return SP24_OK;
   if (!A || !values || !index) return SP24_ERR_INVALID_ARG;
   if (lda < K || ldv < K / 2 || ldi < K / 32) return SP24_ERR_INVALID_ARG;
-  const int esz = dtype_bytes(t);
   if (!aligned16(A) || !aligned16(values) || (reinterpret_cast<uintptr_t>(index) & 3u) ||
-      (lda * esz) % 16 || (ldv * esz) % 16)
+      !ld_ok16(t, lda) || !ld_ok16(t, ldv))
     return SP24_ERR_ALIGN;
   int sms = 0;
   if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
   DecompressArgs a;
   a.values = static_cast<const uint8_t*>(values);
-  a.ldv_bytes = ldv * esz;
+  a.ldv_bytes = ld_bytes(t, ldv);
   a.index = index;
   a.ldi = ldi;
   a.A = static_cast<uint8_t*>(A);
-  a.lda_bytes = lda * esz;
+  a.lda_bytes = ld_bytes(t, lda);
   a.M = M;
   a.K = K;
   if (launch_decompress(a, t, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -170,8 +168,9 @@ sp24_status sp24_meta_prepare(sp24_dtype t, int64_t M, int64_t K, const uint32_t
 }
 
 size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t N, int64_t K) {
-  if (!is_i8(ta) || tb != SP24_S8 || M < 0 || N < 0 || K < 0) return 0;
-  return int_workspace_bytes(M, N, K);
+  if (M < 0 || N < 0 || K < 0) return 0;
+  if ((is_i8(ta) && tb == SP24_S8) || (is_i4(ta) && is_i4(tb))) return int_workspace_bytes(M, N, K);
+  return 0;
 }
 
 sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td, int64_t M,
@@ -181,15 +180,17 @@ sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
                      void* stream) {
   const bool f16ish = (ta == SP24_F16 || ta == SP24_BF16);
   const bool f8 = is_f8(ta);
-  const bool i8 = is_i8(ta);
+  const bool integer = is_int(ta);
   if (f16ish || f8) {
     // 16-bit: A and B of one type; FP8: any mix of E4M3 and E5M2 (kind::f8f6f4 takes
     // separate A and B type fields)
     if (f16ish ? tb != ta : !is_f8(tb)) return SP24_ERR_UNSUPPORTED;
     if (C != nullptr && tc != SP24_F32) return SP24_ERR_UNSUPPORTED;
     if (td != SP24_F32 && td != SP24_BF16) return SP24_ERR_UNSUPPORTED;
-  } else if (i8) {
-    if (tb != SP24_S8) return SP24_ERR_UNSUPPORTED;
+  } else if (integer) {
+    // 8-bit: B signed (u8 x u8 products could leave an f32 chunk sum inexact); 4-bit: any
+    // mix of signed and unsigned
+    if (is_i8(ta) ? tb != SP24_S8 : !is_i4(tb)) return SP24_ERR_UNSUPPORTED;
     if (C != nullptr && tc != SP24_S32) return SP24_ERR_UNSUPPORTED;
     if (td != SP24_S32) return SP24_ERR_UNSUPPORTED;
   } else {
@@ -200,16 +201,15 @@ sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
   if (M == 0 || N == 0) return SP24_OK;
   if (!D || (K > 0 && (!values || !meta || !B))) return SP24_ERR_INVALID_ARG;
   if (ldd < N || (C && ldc < N) || (K > 0 && (ldv < K / 2 || ldb < N))) return SP24_ERR_INVALID_ARG;
-  if (i8 && K > 0 && (!workspace || workspace_bytes < int_workspace_bytes(M, N, K)))
+  if (integer && K > 0 && (!workspace || workspace_bytes < int_workspace_bytes(M, N, K)))
     return SP24_ERR_INVALID_ARG;
-  const int esz = dtype_bytes(ta);
   const int dsz = dtype_bytes(td);
   if (!aligned16(D) || (ldd * dsz) % 16) return SP24_ERR_ALIGN;
   if (C && (!aligned16(C) || (ldc * 4) % 16)) return SP24_ERR_ALIGN;
-  if (K > 0 && (!aligned16(values) || !aligned16(meta) || !aligned16(B) || (ldv * esz) % 16 ||
-                (ldb * esz) % 16))
+  if (K > 0 && (!aligned16(values) || !aligned16(meta) || !aligned16(B) || !ld_ok16(ta, ldv) ||
+                !ld_ok16(tb, ldb)))
     return SP24_ERR_ALIGN;
-  if (i8 && K > 0 && !aligned16(workspace)) return SP24_ERR_ALIGN;
+  if (integer && K > 0 && !aligned16(workspace)) return SP24_ERR_ALIGN;
   int sms = 0;
   if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
   const int rc = launch_spmma(ta, tb, tc, td, M, N, K, values, ldv, meta, B, ldb, C, ldc, D, ldd,

@@ -7,11 +7,13 @@
 //   index[i][g/8] bits 4(g%8)..+3  = p0 | p1 << 2
 //
 // Layout of the work: one thread owns one 16-byte chunk of a row of A (8 elements of a
-// 16-bit type = 2 groups, or 16 elements of an 8-bit type = 4 groups).  A warp owns 32
-// consecutive chunks, so every load of A and every store of values is a fully
-// coalesced 16- / 8-byte vector access; the 4 (16-bit) or 2 (8-bit) lanes that share
-// one 32-element index word merge their nibbles with two / one xor-shuffles.  The
-// kernel is HBM-bound: it streams A (+ mask) once and writes values + index once.
+// 16-bit type = 2 groups, 16 elements of an 8-bit type = 4 groups, or 32 elements of a
+// 4-bit type = 8 groups, two per byte with element 2i in the low nibble as in "INT4 and
+// UINT4 inputs").  A warp owns 32 consecutive chunks, so every load of A and every store
+// of values is a fully coalesced 16- / 8-byte vector access; the 4 (16-bit) or 2 (8-bit)
+// lanes that share one 32-element index word merge their nibbles with two / one
+// xor-shuffles (a 4-bit chunk fills a word alone).  The kernel is HBM-bound: it streams
+// A (+ mask) once and writes values + index once.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -22,7 +24,8 @@ namespace sp24 {
 namespace {
 
 // element classes: how "zero" and "|x|" are read from the stored bits
-enum ElemClass { kFloat16 = 0, kFloat8 = 1, kSigned8 = 2, kUnsigned8 = 3 };
+enum ElemClass { kFloat16 = 0, kFloat8 = 1, kSigned8 = 2, kUnsigned8 = 3, kSigned4 = 4,
+                 kUnsigned4 = 5 };
 
 // Selection rule of the exact and mask modes as a function of the 4-bit set of candidate
 // positions: more than two -> the two lowest; fewer than two -> add the lowest free
@@ -92,6 +95,17 @@ __device__ __forceinline__ uint32_t keep_nonzero8(uint32_t w) {
   return gather_bit7(((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w);
 }
 
+// 4-bit group: four nibbles in the low 16 bits of x.  Non-zero nibbles by the same carry
+// trick (bit 3 of each nibble), gathered into a 4-bit set with one multiply.
+__device__ __forceinline__ uint32_t keep_nonzero4(uint32_t x) {
+  const uint32_t t = ((x & 0x7777u) + 0x7777u) | x;
+  return ((((t >> 3) & 0x1111u) * 0x1248u) >> 12) & 0xFu;
+}
+// The two kept nibbles of a 4-bit group as one byte (p0 low, p1 high).
+__device__ __forceinline__ uint32_t pack4(uint32_t x, uint32_t nib) {
+  return ((x >> (4 * (nib & 3u))) & 0xFu) | (((x >> (4 * (nib >> 2))) & 0xFu) << 4);
+}
+
 // The two kept elements of a 16-bit group (words w0, w1) packed as one word.
 __device__ __forceinline__ uint32_t pack16(uint32_t w0, uint32_t w1, uint32_t nib) {
   const uint32_t p0 = nib & 3u, p1 = nib >> 2;
@@ -144,6 +158,23 @@ __device__ __forceinline__ uint32_t top2_16(uint32_t w0, uint32_t w1) {
   return top2_keys(w0 & 0x7FFFu, (w0 >> 16) & 0x7FFFu, w1 & 0x7FFFu, (w1 >> 16) & 0x7FFFu);
 }
 
+// 4-bit group in the low 16 bits: keys = |x| (s4: two's complement, so -8 gives 8).
+template <int CLS>
+__device__ __forceinline__ uint32_t top2_4(uint32_t x) {
+  uint32_t k[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t n = (x >> (4 * p)) & 0xFu;
+    if constexpr (CLS == kSigned4) {
+      const int v = int(n) - int((n & 8u) << 1);
+      k[p] = uint32_t(v < 0 ? -v : v);
+    } else {
+      k[p] = n;
+    }
+  }
+  return top2_keys(k[0], k[1], k[2], k[3]);
+}
+
 // 8-bit group in one word: keys = |x| (FP8: bits without the sign; s8: absolute value,
 // so -128 gives 128; u8: the value).
 template <int CLS>
@@ -164,13 +195,14 @@ __device__ __forceinline__ uint32_t top2_8(uint32_t w) {
   return top2_keys(k[0], k[1], k[2], k[3]);
 }
 
-// One 16-byte chunk of a row (8 16-bit or 16 8-bit elements = 2 or 4 groups): the kept
-// elements packed into 8 bytes, the groups' nibbles (4 bits each, group g at 4g) and the
-// mode's rule-break flag in bit 0 of `flags`.  m: the chunk's mask bytes (mask mode).
-template <int ESZ, int CLS, int MODE>
-__device__ __forceinline__ void compress_chunk(const uint4& v, const uint32_t (&m)[4], uint2& vals,
+// One 16-byte chunk of a row (8 16-bit, 16 8-bit or 32 4-bit elements = 2, 4 or 8
+// groups; EB = element bits): the kept elements packed into 8 bytes, the groups' nibbles
+// (4 bits each, group g at 4g) and the mode's rule-break flag in bit 0 of `flags`.
+// m: the chunk's mask bytes (mask mode), one word per group.
+template <int EB, int CLS, int MODE>
+__device__ __forceinline__ void compress_chunk(const uint4& v, const uint32_t (&m)[8], uint2& vals,
                                                uint32_t& nibs, uint32_t& flags) {
-  constexpr int kGroups = (16 / ESZ) / 4;
+  constexpr int kGroups = (128 / EB) / 4;
   constexpr uint32_t kFlags = MODE == 1 ? kFlagMask : kFlagExact;
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t out[2] = {0, 0};
@@ -179,37 +211,45 @@ __device__ __forceinline__ void compress_chunk(const uint4& v, const uint32_t (&
 #pragma unroll
   for (int g = 0; g < kGroups; ++g) {
     uint32_t nib;
+    uint32_t x4 = 0;  // 4-bit: the group's four nibbles
+    if constexpr (EB == 4) x4 = (w[g >> 1] >> (16 * (g & 1))) & 0xFFFFu;
     if constexpr (MODE == 2) {
-      if constexpr (ESZ == 2)
+      if constexpr (EB == 16)
         nib = top2_16(w[2 * g], w[2 * g + 1]);
-      else
+      else if constexpr (EB == 8)
         nib = top2_8<CLS>(w[g]);
+      else
+        nib = top2_4<CLS>(x4);
     } else {
       uint32_t keep;
       if constexpr (MODE == 1)
         keep = keep_from_mask(m[g]);
-      else if constexpr (ESZ == 2)
+      else if constexpr (EB == 16)
         keep = keep_nonzero16(w[2 * g], w[2 * g + 1]);
-      else
+      else if constexpr (EB == 8)
         keep = keep_nonzero8<CLS>(w[g]);
+      else
+        keep = keep_nonzero4(x4);
       nib = uint32_t(kPickLut >> (4 * keep)) & 0xFu;
       flags |= kFlags >> keep;
     }
-    if constexpr (ESZ == 2)
+    if constexpr (EB == 16)
       out[g] = pack16(w[2 * g], w[2 * g + 1], nib);
-    else
+    else if constexpr (EB == 8)
       out[g >> 1] |= pack8(w[g], nib) << (16 * (g & 1));
+    else
+      out[g >> 2] |= pack4(x4, nib) << (8 * (g & 3));
     nibs |= nib << (4 * g);
   }
   vals = make_uint2(out[0], out[1]);
 }
 
-// ESZ = element bytes (2 or 1); MODE = SP24_MODE_* value.  Each warp step covers kUnroll
-// runs of 32 consecutive chunks; all their loads are issued before any is used, so a
-// thread keeps kUnroll 16-byte loads (plus mask loads) in flight.
-template <int ESZ, int CLS, int MODE>
+// EB = element bits (16, 8 or 4); MODE = SP24_MODE_* value.  Each warp step covers
+// kUnroll runs of 32 consecutive chunks; all their loads are issued before any is used,
+// so a thread keeps kUnroll 16-byte loads (plus mask loads) in flight.
+template <int EB, int CLS, int MODE>
 __global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
-  constexpr int kElems = 16 / ESZ;   // elements per 16-byte chunk
+  constexpr int kElems = 128 / EB;   // elements per 16-byte chunk
   constexpr int kGroups = kElems / 4;  // groups per chunk
   constexpr int kLanesPerWord = 32 / kElems;
   constexpr int kUnroll = 4;
@@ -224,7 +264,7 @@ __global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
   for (int64_t base = warp_global * 32 * kUnroll; base < total;
        base += warp_stride * 32 * kUnroll) {
     uint4 v[kUnroll];
-    uint32_t mbits[kUnroll][4];
+    uint32_t mbits[kUnroll][8];
     int64_t row[kUnroll], cc[kUnroll];
     bool active[kUnroll];
 #pragma unroll
@@ -240,7 +280,8 @@ __global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
         cc[u] = c - row[u] * cpr;
       }
       v[u] = make_uint4(0, 0, 0, 0);
-      mbits[u][0] = mbits[u][1] = mbits[u][2] = mbits[u][3] = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) mbits[u][q] = 0;
       if (active[u]) {
         v[u] = __ldcs(reinterpret_cast<const uint4*>(a.A + row[u] * a.lda_bytes + cc[u] * 16));
         if constexpr (MODE == 1) {
@@ -250,12 +291,15 @@ __global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
             mbits[u][0] = m.x;
             mbits[u][1] = m.y;
           } else {
-            const uint4 m =
-                __ldcs(reinterpret_cast<const uint4*>(a.mask + row[u] * a.ldm + cc[u] * 16));
-            mbits[u][0] = m.x;
-            mbits[u][1] = m.y;
-            mbits[u][2] = m.z;
-            mbits[u][3] = m.w;
+#pragma unroll
+            for (int h = 0; h < kElems / 16; ++h) {  // 16 mask bytes per load
+              const uint4 m = __ldcs(reinterpret_cast<const uint4*>(
+                  a.mask + row[u] * a.ldm + cc[u] * kElems + 16 * h));
+              mbits[u][4 * h + 0] = m.x;
+              mbits[u][4 * h + 1] = m.y;
+              mbits[u][4 * h + 2] = m.z;
+              mbits[u][4 * h + 3] = m.w;
+            }
           }
         }
       }
@@ -264,14 +308,16 @@ __global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
     for (int u = 0; u < kUnroll; ++u) {
       uint2 vals;
       uint32_t nibs, flags;
-      compress_chunk<ESZ, CLS, MODE>(v[u], mbits[u], vals, nibs, flags);
+      compress_chunk<EB, CLS, MODE>(v[u], mbits[u], vals, nibs, flags);
       if (active[u]) any_flag |= flags & 1u;
       if (active[u])
         __stcs(reinterpret_cast<uint2*>(a.values + row[u] * a.ldv_bytes + cc[u] * 8), vals);
       // merge the nibbles of the lanes that share one index word
       uint32_t word = nibs << ((4 * kGroups) * (lane % kLanesPerWord));
+      if constexpr (kLanesPerWord > 1) {
 #pragma unroll
-      for (int o = 1; o < kLanesPerWord; o <<= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, o);
+        for (int o = 1; o < kLanesPerWord; o <<= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, o);
+      }
       if (active[u] && (lane % kLanesPerWord) == 0) {
         a.index[row[u] * a.ldi + (cc[u] * kElems) / 32] = word;
       }
@@ -282,9 +328,9 @@ __global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
 }
 
 // expand(values, index): one thread writes one 16-byte chunk of dense A.
-template <int ESZ>
+template <int EB>
 __global__ void __launch_bounds__(256) decompress_kernel(DecompressArgs a) {
-  constexpr int kElems = 16 / ESZ;
+  constexpr int kElems = 128 / EB;
   constexpr int kGroups = kElems / 4;
   const int64_t cpr = a.K / kElems;
   const int64_t total = a.M * cpr;
@@ -301,35 +347,41 @@ __global__ void __launch_bounds__(256) decompress_kernel(DecompressArgs a) {
       const uint32_t nib = (nibs >> (4 * g)) & 0xFu;
       const uint32_t p0 = nib & 3u, p1 = nib >> 2;
       uint32_t k0, k1;
-      if constexpr (ESZ == 2) {
+      if constexpr (EB == 16) {
         k0 = kv[g] & 0xFFFFu;
         k1 = kv[g] >> 16;
-      } else {
+      } else if constexpr (EB == 8) {
         const uint32_t h = (kv[g >> 1] >> (16 * (g & 1))) & 0xFFFFu;
         k0 = h & 0xFFu;
         k1 = h >> 8;
+      } else {
+        const uint32_t b = (kv[g >> 2] >> (8 * (g & 3))) & 0xFFu;
+        k0 = b & 0xFu;
+        k1 = b >> 4;
       }
       // element 4g + p gets k0 at p0, k1 at p1, zero elsewhere (static register indices)
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         const uint32_t v = uint32_t(p) == p0 ? k0 : (uint32_t(p) == p1 ? k1 : 0u);
         const int e = 4 * g + p;
-        if constexpr (ESZ == 2)
+        if constexpr (EB == 16)
           o[e >> 1] |= v << (16 * (e & 1));
-        else
+        else if constexpr (EB == 8)
           o[e >> 2] |= v << (8 * (e & 3));
+        else
+          o[e >> 3] |= v << (4 * (e & 7));
       }
     }
     *reinterpret_cast<uint4*>(a.A + row * a.lda_bytes + cc * 16) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
-template <int ESZ, int CLS>
+template <int EB, int CLS>
 cudaError_t launch_compress_cls(const CompressArgs& a, int mode, int grid, cudaStream_t s) {
   switch (mode) {
-    case 0: compress_kernel<ESZ, CLS, 0><<<grid, 256, 0, s>>>(a); break;
-    case 1: compress_kernel<ESZ, CLS, 1><<<grid, 256, 0, s>>>(a); break;
-    default: compress_kernel<ESZ, CLS, 2><<<grid, 256, 0, s>>>(a); break;
+    case 0: compress_kernel<EB, CLS, 0><<<grid, 256, 0, s>>>(a); break;
+    case 1: compress_kernel<EB, CLS, 1><<<grid, 256, 0, s>>>(a); break;
+    default: compress_kernel<EB, CLS, 2><<<grid, 256, 0, s>>>(a); break;
   }
   return cudaGetLastError();
 }
@@ -338,32 +390,35 @@ cudaError_t launch_compress_cls(const CompressArgs& a, int mode, int grid, cudaS
 
 cudaError_t launch_compress(const CompressArgs& a, int dtype, int mode, int num_sms,
                             cudaStream_t s) {
-  const int esz = dtype_bytes(dtype);
-  const int64_t chunks = a.M * (a.K / (16 / esz));
+  const int64_t chunks = a.M * (a.K / (128 / elem_bits(dtype)));
   // each thread covers 4 chunks per step; 8 resident blocks of 256 threads per SM
   int64_t want = (chunks + 1023) / 1024;
   int64_t cap = int64_t(num_sms) * 8;
   const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
   switch (dtype) {
     case kF16:
-    case kBF16: return launch_compress_cls<2, kFloat16>(a, mode, grid, s);
+    case kBF16: return launch_compress_cls<16, kFloat16>(a, mode, grid, s);
     case kE4M3:
-    case kE5M2: return launch_compress_cls<1, kFloat8>(a, mode, grid, s);
-    case kS8: return launch_compress_cls<1, kSigned8>(a, mode, grid, s);
-    default: return launch_compress_cls<1, kUnsigned8>(a, mode, grid, s);
+    case kE5M2: return launch_compress_cls<8, kFloat8>(a, mode, grid, s);
+    case kS8: return launch_compress_cls<8, kSigned8>(a, mode, grid, s);
+    case kU8: return launch_compress_cls<8, kUnsigned8>(a, mode, grid, s);
+    case kS4: return launch_compress_cls<4, kSigned4>(a, mode, grid, s);
+    default: return launch_compress_cls<4, kUnsigned4>(a, mode, grid, s);
   }
 }
 
 cudaError_t launch_decompress(const DecompressArgs& a, int dtype, int num_sms, cudaStream_t s) {
-  const int esz = dtype_bytes(dtype);
-  const int64_t chunks = a.M * (a.K / (16 / esz));
+  const int eb = elem_bits(dtype);
+  const int64_t chunks = a.M * (a.K / (128 / eb));
   int64_t want = (chunks + 255) / 256;
   int64_t cap = int64_t(num_sms) * 8;
   const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
-  if (esz == 2)
-    decompress_kernel<2><<<grid, 256, 0, s>>>(a);
+  if (eb == 16)
+    decompress_kernel<16><<<grid, 256, 0, s>>>(a);
+  else if (eb == 8)
+    decompress_kernel<8><<<grid, 256, 0, s>>>(a);
   else
-    decompress_kernel<1><<<grid, 256, 0, s>>>(a);
+    decompress_kernel<4><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

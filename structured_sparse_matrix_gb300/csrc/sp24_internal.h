@@ -8,24 +8,38 @@
 namespace sp24 {
 
 // element codes: identical to sp24_dtype in include/sp24.h
-enum : int { kF16 = 0, kBF16 = 1, kE4M3 = 2, kE5M2 = 3, kS8 = 4, kU8 = 5, kF32 = 6, kS32 = 7 };
+enum : int {
+  kF16 = 0, kBF16 = 1, kE4M3 = 2, kE5M2 = 3, kS8 = 4, kU8 = 5, kF32 = 6, kS32 = 7,
+  kS4 = 8, kU4 = 9
+};
 
-inline int dtype_bytes(int t) {
+// bits per element (4-bit types: two per byte, element 2i in the low nibble)
+inline int elem_bits(int t) {
   switch (t) {
-    case kF16: case kBF16: return 2;
-    case kE4M3: case kE5M2: case kS8: case kU8: return 1;
-    case kF32: case kS32: return 4;
+    case kF16: case kBF16: return 16;
+    case kE4M3: case kE5M2: case kS8: case kU8: return 8;
+    case kF32: case kS32: return 32;
+    case kS4: case kU4: return 4;
     default: return 0;
   }
 }
-inline bool is_ab_type(int t) { return t >= kF16 && t <= kU8; }
+// bytes of a whole-byte type (0 for 4-bit types)
+inline int dtype_bytes(int t) { return elem_bits(t) >= 8 ? elem_bits(t) / 8 : 0; }
+// row pitch in bytes of `ld` elements; ld_ok16: that pitch is a whole number of 16-byte
+// units (for 4-bit types this also makes ld even)
+inline int64_t ld_bytes(int t, int64_t ld) { return ld * elem_bits(t) / 8; }
+inline bool ld_ok16(int t, int64_t ld) { return (ld * elem_bits(t)) % 128 == 0; }
+inline bool is_ab_type(int t) { return (t >= kF16 && t <= kU8) || t == kS4 || t == kU4; }
 inline bool is_f8(int t) { return t == kE4M3 || t == kE5M2; }
 inline bool is_i8(int t) { return t == kS8 || t == kU8; }
+inline bool is_i4(int t) { return t == kS4 || t == kU4; }
+inline bool is_int(int t) { return is_i8(t) || is_i4(t); }
+inline bool is_signed_int(int t) { return t == kS8 || t == kS4; }
 
 // ---- sparse-GEMM K-step geometry (one pipeline stage) shared by meta.cu and spmma.cu
 // 16-bit operands: 128 dense K per stage = 4 MMAs of K=32, metadata one TMEM column
 // per MMA; FP8 operands: 256 dense K per stage = 4 MMAs of K=64, two columns per MMA.
-// 8-bit integers run widened to bf16 on the 16-bit path, so they use its geometry.
+// 8- and 4-bit integers run widened to bf16 on the 16-bit path, so they use its geometry.
 // In both cases a stage of compressed A is 128 rows x 128 bytes, and the stage's
 // metadata is one [128 lanes][4 words] block per MMA (the MMA's words first), the
 // source of one tcgen05.cp.128x128b into the MMA's column-aligned TMEM slot.
@@ -63,9 +77,10 @@ struct MetaArgs {
 cudaError_t launch_compress(const CompressArgs& a, int dtype, int mode, int num_sms, cudaStream_t s);
 cudaError_t launch_decompress(const DecompressArgs& a, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_meta_prepare(const MetaArgs& a, int dtype, int num_sms, cudaStream_t s);
-// rows x cols 8-bit integers (pitch ld_src bytes) -> bfloat16 (pitch ld_dst elements)
+// rows x cols 8- or 4-bit integers (`bits`; pitch ld_src bytes) -> bfloat16 (pitch
+// ld_dst elements)
 cudaError_t launch_widen(const void* src, int64_t ld_src, void* dst, int64_t ld_dst,
-                         int64_t rows, int64_t cols, bool is_signed, int num_sms,
+                         int64_t rows, int64_t cols, bool is_signed, int bits, int num_sms,
                          cudaStream_t s);
 
 // Integer operands are widened to bf16 into a caller-provided workspace: A_c (M x K/2)

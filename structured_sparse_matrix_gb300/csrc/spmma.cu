@@ -767,11 +767,10 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   BatchStrides bs{0, 0, 0};
   p.batch = 1;
   if (batch != nullptr && batch->count > 1) {
-    const int esz = dtype_bytes(ta);
     p.batch = int(batch->count);
-    bs.values = batch->stride_values * esz;
+    bs.values = ld_bytes(ta, batch->stride_values);
     bs.meta = batch->stride_meta;
-    bs.b = batch->stride_b * esz;
+    bs.b = ld_bytes(tb, batch->stride_b);
     p.stride_c = batch->stride_c;
     p.stride_d = batch->stride_d;
   }
@@ -789,7 +788,7 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   p.mtiles = p.ntiles = 0;
   p.num_kb = int((K + stage_k(ta) - 1) / stage_k(ta));
   p.limit_ns = 1000000000ull;  // 1 s per wait
-  if (is_i8(ta)) {
+  if (is_int(ta)) {
     // integers: widen both operands to bf16 (exact) and run the bf16 tensor path with
     // chunked integer accumulation; 256 x 128 tiles on CTA pairs with double-buffered
     // accumulators
@@ -798,8 +797,10 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
     uint8_t* wb = ws + (M * (K / 2) * 2 + 255) / 256 * 256;
     const int64_t ldbw = int_ws_ldb(N);
     if (K > 0) {
-      if (launch_widen(values, ldv, wa, K / 2, M, K / 2, ta == kS8, num_sms, s) != cudaSuccess ||
-          launch_widen(B, ldb, wb, ldbw, K, N, tb == kS8, num_sms, s) != cudaSuccess)
+      if (launch_widen(values, ld_bytes(ta, ldv), wa, K / 2, M, K / 2, is_signed_int(ta),
+                       elem_bits(ta), num_sms, s) != cudaSuccess ||
+          launch_widen(B, ld_bytes(tb, ldb), wb, ldbw, K, N, is_signed_int(tb), elem_bits(tb),
+                       num_sms, s) != cudaSuccess)
         return 4;
     }
     // kind::f16 with bf16 operands: type code 1 for A and B

@@ -161,3 +161,38 @@ def test_no_device_means_no_cpu_fallback():
     assert _compress() == NODEV
     assert _mma() == NODEV
     assert sp.lib().sp24_diag_wait_timeout(FAKE, 1000, None) == NODEV
+
+
+S4, U4 = 8, 9
+
+
+def test_four_bit_argument_checks():
+    L = sp.lib()
+    # the 16-bit metadata layout (the product runs widened to bf16)
+    assert L.sp24_meta_bytes(S4, 4096, 4096) == L.sp24_meta_bytes(BF16, 4096, 4096)
+    assert L.sp24_meta_bytes(U4, 129, 160) == 2 * 2 * 8192
+    # pitches count elements: lda = 144 is 72 bytes, ldv = 80 is 40 bytes
+    assert _compress(t=S4, lda=144) == ALIGN
+    assert _compress(t=U4, ldv=80) == ALIGN
+    assert _compress(t=S4, ldv=48) == INVALID
+    assert _compress(t=U4, M=0) == OK
+    assert L.sp24_decompress(S4, 64, 128, FAKE, 80, FAKE, 4, FAKE, 128, None) == ALIGN
+    # products: both operands 4-bit (any sign mix), integer C and D
+    assert _mma(ta=S4, tb=S8, tc=S32, td=S32) == UNSUPPORTED
+    assert _mma(ta=S8, tb=S4, tc=S32, td=S32) == UNSUPPORTED
+    assert _mma(ta=U4, tb=U4, tc=S32, td=F32) == UNSUPPORTED
+    assert _mma(ta=S4, tb=U4, tc=F32, td=S32) == UNSUPPORTED
+    need = L.sp24_mma_workspace_bytes(S4, U4, 128, 128, 128)
+    assert need == L.sp24_mma_workspace_bytes(S8, S8, 128, 128, 128)
+    assert L.sp24_mma_workspace_bytes(S4, S8, 128, 128, 128) == 0
+    assert _mma(ta=S4, tb=U4, tc=S32, td=S32) == INVALID           # needs the workspace
+    assert _mma(ta=U4, tb=S4, tc=S32, td=S32, ws=FAKE, ws_bytes=need, ldb=144) == ALIGN
+    assert _mma(ta=U4, tb=S4, tc=S32, td=S32, ws=FAKE, ws_bytes=need, ldv=80) == ALIGN
+    assert _bmma(ta=S4, tb=S4, tc=S32, td=S32) == UNSUPPORTED
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
+def test_four_bit_valid_calls_reach_the_device_check():
+    need = sp.lib().sp24_mma_workspace_bytes(S4, S4, 128, 128, 128)
+    assert _compress(t=S4) == NODEV
+    assert _mma(ta=S4, tb=S4, tc=S32, td=S32, ws=FAKE, ws_bytes=need) == NODEV
