@@ -78,6 +78,8 @@ def lib():
             L.or_decode_array.argtypes = [i32, p, i64, p]
             L.or_round_bf16_array.restype = None
             L.or_round_bf16_array.argtypes = [p, i64, p]
+            L.or_round_f16_array.restype = None
+            L.or_round_f16_array.argtypes = [p, i64, p]
             L.or_wrap_i32_array.restype = None
             L.or_wrap_i32_array.argtypes = [p, i64, p]
             L.or_num_threads.restype = i32
@@ -117,6 +119,15 @@ def round_bf16(x) -> np.ndarray:
     flat = np.ascontiguousarray(arr.ravel())
     out = np.empty(flat.size, dtype=np.uint16)
     lib().or_round_bf16_array(_ptr(flat), flat.size, _ptr(out))
+    return out.reshape(arr.shape)
+
+
+def round_f16(x) -> np.ndarray:
+    """IEEE binary16 bit patterns of x rounded to nearest, ties to even."""
+    arr = np.asarray(x, dtype=np.float64)
+    flat = np.ascontiguousarray(arr.ravel())
+    out = np.empty(flat.size, dtype=np.uint16)
+    lib().or_round_f16_array(_ptr(flat), flat.size, _ptr(out))
     return out.reshape(arr.shape)
 
 

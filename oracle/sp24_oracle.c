@@ -129,6 +129,32 @@ uint16_t or_round_bf16(double x)
     return (uint16_t)(sign | (u >> 16));
 }
 
+uint16_t or_round_f16(double x)
+{
+    if (isnan(x))
+        return 0x7e00u;
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double ax = fabs(x);
+    if (ax == 0.0)
+        return sign;
+    /* quantum of the binary16 binade holding ax: 11 significant bits, min exponent -14 */
+    int e;
+    frexp(ax, &e);
+    int ue = e - 1;
+    if (ue < -14)
+        ue = -14; /* subnormal range has the fixed quantum 2^-24 */
+    double q = ldexp(1.0, ue - 10);
+    double y = rint(ax / q) * q; /* ties to even */
+    if (y >= 65536.0)
+        return sign | 0x7c00u; /* overflow to infinity (65520 and above) */
+    if (y < ldexp(1.0, -14))   /* subnormal (or the smallest normal reached by rounding) */
+        return (uint16_t)(sign | (uint16_t)(y / ldexp(1.0, -24)));
+    frexp(y, &e);
+    ue = e - 1;
+    uint32_t frac = (uint32_t)(y / ldexp(1.0, ue - 10)) - 1024u; /* 10 fraction bits */
+    return (uint16_t)(sign | (uint16_t)((uint32_t)(ue + 15) << 10) | (uint16_t)frac);
+}
+
 int32_t or_wrap_i32(int64_t x)
 {
     uint32_t u = (uint32_t)((uint64_t)x & 0xffffffffu);
@@ -150,6 +176,12 @@ void or_round_bf16_array(const double *src, int64_t n, uint16_t *dst)
 {
     for (int64_t i = 0; i < n; ++i)
         dst[i] = or_round_bf16(src[i]);
+}
+
+void or_round_f16_array(const double *src, int64_t n, uint16_t *dst)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = or_round_f16(src[i]);
 }
 
 void or_wrap_i32_array(const int64_t *src, int64_t n, int32_t *dst)
@@ -297,13 +329,15 @@ static int valid_ab(int t) { return t >= OR_F16 && t <= OR_U8; }
 
 /* D = expand(A, index) * B + C ("Builtin reference": expand(srcA, index) x srcB + srcC;
  * "v_smfmac_f32_32x32x32_bf8_bf8" Semantics: D = A(sparse) * B + D), in double.  The
- * loop order is i-k-j; a zero a_ik adds nothing and is skipped. */
+ * loop order is i-k-j; a zero a_ik adds nothing and is skipped.  C may be f32, s32, or
+ * the 16-bit accumulators of "FP16-accumulate builtins" / "BF16-accumulate builtins". */
 int or_mma_f64(int ta, int tb, int64_t M, int64_t N, int64_t K, const void *values,
                int64_t ldv, const uint32_t *index, int64_t ldi, const void *B,
                int64_t ldb, int tc, const void *C, int64_t ldc, const int64_t *rows,
                int64_t nrows, double *D, double *S)
 {
-    if (!valid_ab(ta) || !valid_ab(tb) || (C && tc != OR_F32 && tc != OR_S32))
+    if (!valid_ab(ta) || !valid_ab(tb) ||
+        (C && tc != OR_F32 && tc != OR_S32 && tc != OR_F16 && tc != OR_BF16))
         return -1;
     (void)M;
     int besz = or_elem_bytes(tb);

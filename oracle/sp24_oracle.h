@@ -60,12 +60,18 @@ double or_decode(int dtype, uint32_t bits);
 /* Round a real number to the nearest bfloat16, ties to even; returns the bit pattern. */
 uint16_t or_round_bf16(double x);
 
+/* Round a real number to the nearest IEEE binary16, ties to even (65520 and above ->
+ * infinity); returns the bit pattern.  The FP16-accumulate result of "RDNA4 sparse WMMA
+ * builtins" is read as the exact sum rounded once to this format. */
+uint16_t or_round_f16(double x);
+
 /* Two's-complement wrap of an exact integer sum to 32 bits. */
 int32_t or_wrap_i32(int64_t x);
 
 /* Array forms of the three functions above (n elements each). */
 void or_decode_array(int dtype, const void *src, int64_t n, double *dst);
 void or_round_bf16_array(const double *src, int64_t n, uint16_t *dst);
+void or_round_f16_array(const double *src, int64_t n, uint16_t *dst);
 void or_wrap_i32_array(const int64_t *src, int64_t n, int32_t *dst);
 
 /*

@@ -105,6 +105,61 @@ def test_round_bf16_ties_to_even():
     assert oracle.round_bf16([2.0 ** 128])[0] == 0x7F80
 
 
+# --- f16 rounding (the FP16-accumulate output): pinned to torch's float32 -> float16
+# conversion, to the binary16 boundary values and to its own decode
+
+def test_round_f16_matches_torch_on_float32_values():
+    g = torch.Generator().manual_seed(6)
+    x = torch.randn(200000, generator=g) * torch.exp(torch.randn(200000, generator=g) * 5)
+    x = torch.cat([x, torch.tensor([0.0, -0.0, 6e-8, -3e-8, 65504.0, 65519.0, -7e4, 1e-30])])
+    ref = x.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.round_f16(x.double().numpy())
+    assert np.array_equal(got, ref)
+
+
+def test_round_f16_boundaries_and_ties():
+    u = 2.0 ** -10                       # ulp of 1.0
+    cases = [
+        (1.0 + u / 2, 0x3C00),           # half an ulp above 1: ties to even (down)
+        (1.0 + 1.5 * u, 0x3C02),         # 1.5 ulp: ties to even (up)
+        (1.0 + u / 2 + 2.0 ** -40, 0x3C01),
+        (65504.0, 0x7BFF),               # largest finite
+        (65519.99, 0x7BFF),
+        (65520.0, 0x7C00),               # halfway to 2^16: rounds to infinity
+        (-65520.0, 0xFC00),
+        (2.0 ** -24, 0x0001),            # smallest subnormal
+        (2.0 ** -25, 0x0000),            # half of it: ties to even (zero)
+        (1.5 * 2.0 ** -25, 0x0001),
+        (1023.5 * 2.0 ** -24, 0x0400),   # between the largest subnormal and 2^-14: even
+        (2.0 ** -14, 0x0400),            # smallest normal
+        (-0.0, 0x8000),
+        (np.inf, 0x7C00),
+    ]
+    got = oracle.round_f16([c[0] for c in cases])
+    assert [int(v) for v in got] == [c[1] for c in cases]
+    nan = oracle.round_f16([np.nan])[0]
+    assert (nan & 0x7C00) == 0x7C00 and (nan & 0x3FF) != 0
+
+
+def test_round_f16_inverts_decode():
+    bits = np.arange(65536, dtype=np.uint32)
+    finite = (bits & 0x7C00) != 0x7C00
+    vals = oracle.decode("f16", bits[finite])
+    assert np.array_equal(oracle.round_f16(vals), bits[finite].astype(np.uint16))
+
+
+def test_mma_f64_reads_16_bit_accumulators():
+    # B = 0: D is C decoded, for f16 and bf16 C alike
+    M, N, K = 3, 8, 32
+    values = np.zeros((M, K // 2), dtype=np.uint16)
+    index = np.full((M, 1), 0x44444444, dtype=np.uint32)
+    B = np.zeros((K, N), dtype=np.uint16)
+    for tc in ("f16", "bf16"):
+        C = np.arange(M * N, dtype=np.uint16).reshape(M, N) * 37 + 0x3C00
+        D, S = oracle.mma_f64(values, index, B, C, "f16", "f16", K, tc=tc)
+        assert np.array_equal(D, oracle.decode(tc, C)) and not S.any()
+
+
 def test_wrap_i32():
     v = np.array([0, 1, -1, 2 ** 31 - 1, 2 ** 31, -(2 ** 31) - 1, 2 ** 32 + 5], dtype=np.int64)
     exp = np.array([0, 1, -1, 2 ** 31 - 1, -(2 ** 31), 2 ** 31 - 1, 5], dtype=np.int32)
