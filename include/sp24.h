@@ -160,9 +160,10 @@ size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t
  * (expand(srcA, index) x srcB + srcC) on the tcgen05 sparse tensor cores.
  *
  * ta, tb, tc, td supported combinations (anything else: SP24_ERR_UNSUPPORTED):
- *   (F16, F16) and (BF16, BF16)     -> f32 accumulate, tc in {F32, none}, td in {F32, BF16}
+ *   (F16, F16) and (BF16, BF16)     -> f32 accumulate, tc in {F32, F16, BF16, none},
+ *                                      td in {F32, F16, BF16}
  *   (E4M3, E4M3), (E5M2, E5M2),
- *   (E4M3, E5M2) and (E5M2, E4M3)   -> f32 accumulate, tc in {F32, none}, td in {F32, BF16}
+ *   (E4M3, E5M2) and (E5M2, E4M3)   -> the same C and D types
  *   (S8, S8) and (U8, S8)           -> exact integer result, tc in {S32, none}, td = S32,
  *                                      32-bit two's-complement wrap, no clamp
  *   (S4 or U4, S4 or U4)            -> the same, for 4-bit operands (any sign mix)
@@ -176,8 +177,10 @@ size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t
  *           16-byte aligned, owned by the caller and used only by this call's kernels
  *           (integer operands only; NULL / 0 otherwise).
  * Leading dimensions count elements, also for 4-bit types (two per byte).
- * Accumulation: floats in f32 on the tensor cores; a BF16 D is the f32 result rounded to
- * nearest-even.  Integers are widened to bf16 (exact) and accumulated in f32 in chunks of
+ * Accumulation: floats in f32 on the tensor cores; a 16-bit C is widened exactly and a
+ * BF16 or F16 D is the f32 result rounded to nearest-even once.  (F16, F16, F16, F16) and
+ * (BF16, BF16, BF16, BF16) are the FP16- / BF16-accumulate forms of "RDNA4 sparse WMMA
+ * builtins"; summing in f32 and rounding once is at least as accurate as 16-bit sums.  Integers are widened to bf16 (exact) and accumulated in f32 in chunks of
  * 1024 dense K (every chunk sum is an exact integer below 2^24), the chunks then summed in
  * int32: the result is exact.  (A u8 x u8 chunk sum could pass 2^24, hence B = S8.)
  * Alignment: values, meta, B, C, D 16-byte aligned, every row pitch a multiple of 16 bytes.

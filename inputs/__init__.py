@@ -134,8 +134,8 @@ def case(ta: str, tb: str, M: int, N: int, K: int, *, seed: int = 0, tc: str | N
     A = apply_mask(values((M, K), ta, dist, ga), m)
     B = values((K, N), tb, b_dist or dist, gb)
     C = None
-    if tc == "f32":
-        C = values((M, N), "f32", c_dist or "normal", gc)
+    if tc in ("f32", "f16", "bf16"):
+        C = values((M, N), tc, c_dist or "normal", gc)
     elif tc == "s32":
         C = values((M, N), "s32", c_dist or "c_s32", gc)
     return {"A": A, "mask": m, "B": B, "C": C, "ta": ta, "tb": tb, "tc": tc,

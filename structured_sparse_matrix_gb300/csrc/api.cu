@@ -183,10 +183,10 @@ sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
   const bool integer = is_int(ta);
   if (f16ish || f8) {
     // 16-bit: A and B of one type; FP8: any mix of E4M3 and E5M2 (kind::f8f6f4 takes
-    // separate A and B type fields)
+    // separate A and B type fields).  C and D: f32, bf16 or f16 each.
     if (f16ish ? tb != ta : !is_f8(tb)) return SP24_ERR_UNSUPPORTED;
-    if (C != nullptr && tc != SP24_F32) return SP24_ERR_UNSUPPORTED;
-    if (td != SP24_F32 && td != SP24_BF16) return SP24_ERR_UNSUPPORTED;
+    if (C != nullptr && !is_float_acc(tc)) return SP24_ERR_UNSUPPORTED;
+    if (!is_float_acc(td)) return SP24_ERR_UNSUPPORTED;
   } else if (integer) {
     // 8-bit: B signed (u8 x u8 products could leave an f32 chunk sum inexact); 4-bit: any
     // mix of signed and unsigned
@@ -205,7 +205,7 @@ sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
     return SP24_ERR_INVALID_ARG;
   const int dsz = dtype_bytes(td);
   if (!aligned16(D) || (ldd * dsz) % 16) return SP24_ERR_ALIGN;
-  if (C && (!aligned16(C) || (ldc * 4) % 16)) return SP24_ERR_ALIGN;
+  if (C && (!aligned16(C) || (ldc * dtype_bytes(tc)) % 16)) return SP24_ERR_ALIGN;
   if (K > 0 && (!aligned16(values) || !aligned16(meta) || !aligned16(B) || !ld_ok16(ta, ldv) ||
                 !ld_ok16(tb, ldb)))
     return SP24_ERR_ALIGN;
@@ -228,8 +228,8 @@ sp24_status sp24_mma_strided_batched(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc
   const bool f16ish = (ta == SP24_F16 || ta == SP24_BF16);
   if (!(f16ish || is_f8(ta))) return SP24_ERR_UNSUPPORTED;  // float operands only
   if (f16ish ? tb != ta : !is_f8(tb)) return SP24_ERR_UNSUPPORTED;
-  if (C != nullptr && tc != SP24_F32) return SP24_ERR_UNSUPPORTED;
-  if (td != SP24_F32 && td != SP24_BF16) return SP24_ERR_UNSUPPORTED;
+  if (C != nullptr && !is_float_acc(tc)) return SP24_ERR_UNSUPPORTED;
+  if (!is_float_acc(td)) return SP24_ERR_UNSUPPORTED;
   if (batch < 0 || M < 0 || N < 0 || K < 0 || (K % 32) != 0) return SP24_ERR_INVALID_ARG;
   if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return SP24_ERR_INVALID_ARG;
   if (batch == 0 || M == 0 || N == 0) return SP24_OK;
@@ -246,12 +246,12 @@ sp24_status sp24_mma_strided_batched(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc
     if (K > 0 && (stride_values < 0 || stride_b < 0 ||
                   size_t(stride_meta) < sp24_meta_bytes(ta, M, K)))
       return SP24_ERR_INVALID_ARG;
-    if ((stride_d * dsz) % 16 || (C && (stride_c * 4) % 16)) return SP24_ERR_ALIGN;
+    if ((stride_d * dsz) % 16 || (C && (stride_c * dtype_bytes(tc)) % 16)) return SP24_ERR_ALIGN;
     if (K > 0 && ((stride_values * esz) % 16 || (stride_b * esz) % 16 || stride_meta % 16))
       return SP24_ERR_ALIGN;
   }
   if (!aligned16(D) || (ldd * dsz) % 16) return SP24_ERR_ALIGN;
-  if (C && (!aligned16(C) || (ldc * 4) % 16)) return SP24_ERR_ALIGN;
+  if (C && (!aligned16(C) || (ldc * dtype_bytes(tc)) % 16)) return SP24_ERR_ALIGN;
   if (K > 0 && (!aligned16(values) || !aligned16(meta) || !aligned16(B) || (ldv * esz) % 16 ||
                 (ldb * esz) % 16))
     return SP24_ERR_ALIGN;

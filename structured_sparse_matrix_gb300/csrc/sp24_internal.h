@@ -35,6 +35,8 @@ inline bool is_i8(int t) { return t == kS8 || t == kU8; }
 inline bool is_i4(int t) { return t == kS4 || t == kU4; }
 inline bool is_int(int t) { return is_i8(t) || is_i4(t); }
 inline bool is_signed_int(int t) { return t == kS8 || t == kS4; }
+// C and D types of the float products: f32, or the 16-bit accumulators
+inline bool is_float_acc(int t) { return t == kF32 || t == kBF16 || t == kF16; }
 
 // ---- sparse-GEMM K-step geometry (one pipeline stage) shared by meta.cu and spmma.cu
 // 16-bit operands: 128 dense K per stage = 4 MMAs of K=32, metadata one TMEM column

@@ -28,6 +28,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -55,6 +56,8 @@ struct MmaParams {
   int64_t ldc, ldd;
   int32_t* status;
   int c32, d32;  // C / D rows allow 32-byte vector accesses (base and pitch 32-byte aligned)
+  int ctype;     // float C: 0 = f32, 1 = bf16, 2 = f16
+  int d_f16;     // 16-bit float D (OUT == 1): 0 = bf16, 1 = f16
   int batoms;    // B boxes loaded per stage and CTA (the narrow variant skips empty ones)
   int M, N, K;
   int mtiles, ntiles, num_kb;  // tiles of the variant (128 or 256 rows, 128 or 256 cols)
@@ -163,7 +166,14 @@ __device__ __forceinline__ void ld_f32x8(const float* src, bool v32, float (&c)[
   }
 }
 
-// C (f32) at 8 consecutive columns of one output row; zeros beyond M, N or without C.
+// one 16-bit float (bf16 if !f16) as f32: exact
+__device__ __forceinline__ float half_bits_to_f32(uint32_t h, bool f16) {
+  return f16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
+             : __uint_as_float(h << 16);
+}
+
+// C at 8 consecutive columns of one output row, as f32 (C is f32, bf16 or f16 by
+// p.ctype); zeros beyond M, N or without C.
 __device__ __forceinline__ void load_c8(float (&c)[8], const MmaParams& p, int row, int col,
                                         int64_t cofs) {
   if (p.C == nullptr || row >= p.M || col >= p.N) {
@@ -171,12 +181,29 @@ __device__ __forceinline__ void load_c8(float (&c)[8], const MmaParams& p, int r
     for (int j = 0; j < 8; ++j) c[j] = 0.f;
     return;
   }
-  const float* crow = static_cast<const float*>(p.C) + cofs + int64_t(row) * p.ldc + col;
+  if (p.ctype == 0) {
+    const float* crow = static_cast<const float*>(p.C) + cofs + int64_t(row) * p.ldc + col;
+    if (col + 8 <= p.N) {
+      ld_f32x8(crow, p.c32 != 0, c);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = col + j < p.N ? crow[j] : 0.f;
+    }
+    return;
+  }
+  const bool f16 = p.ctype == 2;
+  const uint16_t* crow = static_cast<const uint16_t*>(p.C) + cofs + int64_t(row) * p.ldc + col;
   if (col + 8 <= p.N) {
-    ld_f32x8(crow, p.c32 != 0, c);
+    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(crow));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      c[2 * j] = half_bits_to_f32(w[j] & 0xFFFFu, f16);
+      c[2 * j + 1] = half_bits_to_f32(w[j] >> 16, f16);
+    }
   } else {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) c[j] = col + j < p.N ? crow[j] : 0.f;
+    for (int j = 0; j < 8; ++j) c[j] = col + j < p.N ? half_bits_to_f32(crow[j], f16) : 0.f;
   }
 }
 
@@ -203,6 +230,20 @@ __device__ __forceinline__ void store8(const float (&v)[8], const MmaParams& p, 
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         if (col + j < p.N) d[j] = v[j];
+    }
+  } else if (p.d_f16) {
+    __half* d = static_cast<__half*>(p.D) + dofs + int64_t(row) * p.ldd + col;
+    if (full) {
+      __half2 h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+      uint4 u;
+      memcpy(&u, h, 16);
+      __stcs(reinterpret_cast<uint4*>(d), u);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (col + j < p.N) d[j] = __float2half_rn(v[j]);
     }
   } else {
     __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + dofs + int64_t(row) * p.ldd + col;
@@ -256,7 +297,8 @@ __device__ __forceinline__ void prefetch_c_rows(const MmaParams& p, int row0, in
                                                 int cols, int64_t cofs) {
   if (p.C == nullptr || q != 0 || col0 >= p.N) return;
   const int ncols = p.N - col0 < cols ? p.N - col0 : cols;
-  const uint32_t bytes = uint32_t(ncols * 4) & ~15u;
+  const int csize = p.ctype == 0 ? 4 : 2;
+  const uint32_t bytes = uint32_t(ncols * csize) & ~15u;
   if (bytes == 0) return;
 #pragma unroll
   for (int h = 0; h < 2; ++h)
@@ -264,7 +306,8 @@ __device__ __forceinline__ void prefetch_c_rows(const MmaParams& p, int row0, in
     for (int e = 0; e < 2; ++e) {
       const int row = row0 + 16 * h + 8 * e;
       if (row < p.M)
-        bulk_prefetch_l2(static_cast<const float*>(p.C) + cofs + int64_t(row) * p.ldc + col0,
+        bulk_prefetch_l2(static_cast<const uint8_t*>(p.C) +
+                             (cofs + int64_t(row) * p.ldc + col0) * csize,
                          bytes);
     }
 }
@@ -306,8 +349,9 @@ __device__ __forceinline__ void store_chunk_s32(const uint32_t* v, const MmaPara
   }
 }
 
-// OUT: 0 = f32 output, 1 = bf16 output, 2 = s32 output (integer mode, single variant).
-// C (nullable) is f32 for float outputs, s32 for integer mode.
+// OUT: 0 = f32 output, 1 = 16-bit float output (bf16 or f16 by p.d_f16), 2 = s32 output
+// (integer mode).  C (nullable) is f32, bf16 or f16 (p.ctype) for float outputs, s32 for
+// integer mode.
 template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN>
 __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
     spmma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -761,7 +805,6 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
                  const void* values, int64_t ldv, const void* meta, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd, void* workspace,
                  int32_t* status, int num_sms, cudaStream_t s, const BatchArgs* batch) {
-  (void)tc;
   MmaParams p;
   memset(&p, 0, sizeof(p));
   BatchStrides bs{0, 0, 0};
@@ -781,6 +824,8 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   p.status = status;
   // 32-byte vector accesses need a 32-byte aligned base and pitch (the ABI promises 16)
   p.c32 = (reinterpret_cast<uintptr_t>(C) % 32 == 0 && (ldc * 4) % 32 == 0) ? 1 : 0;
+  p.ctype = (C != nullptr && tc == kBF16) ? 1 : (C != nullptr && tc == kF16) ? 2 : 0;
+  p.d_f16 = td == kF16 ? 1 : 0;
   p.d32 = (reinterpret_cast<uintptr_t>(D) % 32 == 0 && (ldd * 4) % 32 == 0) ? 1 : 0;
   p.M = int(M);
   p.N = int(N);
@@ -811,11 +856,11 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   // kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2
   const uint32_t at = (ta == kBF16 || ta == kE5M2) ? 1u : 0u;
   const uint32_t bt = (tb == kBF16 || tb == kE5M2) ? 1u : 0u;
-  const bool out_bf16 = td == kBF16;
+  const bool out16 = td != kF32;  // bf16 or f16 (p.d_f16)
   if (esz == 2)
-    return out_bf16 ? dispatch<2, 1>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s, bs)
+    return out16 ? dispatch<2, 1>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s, bs)
                     : dispatch<2, 0>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s, bs);
-  return out_bf16 ? dispatch<1, 1>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s, bs)
+  return out16 ? dispatch<1, 1>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s, bs)
                   : dispatch<1, 0>(p, values, ldv, meta, B, ldb, at, bt, num_sms, s, bs);
 }
 

@@ -34,19 +34,35 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.exp2(e - 7)
 
 
-def check_float(D: np.ndarray, Dref: np.ndarray, S: np.ndarray, out_bf16: bool, what: str):
-    """Float parity: f32 output within REL*S + ABS; bf16 output compared with the
-    round-to-nearest-even bf16 of the exact result, plus one bf16 ulp (the f32
-    accumulation error may flip a rounding)."""
+def f16_ulp(x: np.ndarray) -> np.ndarray:
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    e = np.maximum(e, -14)
+    return np.exp2(e - 10)
+
+
+OUT_KIND = {torch.float32: None, torch.bfloat16: "bf16", torch.float16: "f16"}
+
+
+def check_float(D: np.ndarray, Dref: np.ndarray, S: np.ndarray, out, what: str):
+    """Float parity: f32 output within REL*S + ABS; 16-bit output (out = "bf16" / "f16",
+    or True for bf16) compared with the round-to-nearest-even value of the exact result,
+    plus one ulp of that format (the f32 accumulation error may flip a rounding)."""
     D = np.asarray(D, dtype=np.float64)
-    if out_bf16:
+    if out is True:
+        out = "bf16"
+    if out == "bf16":
         ref = oracle.decode("bf16", oracle.round_bf16(Dref))
         tol = REL * S + ABS + bf16_ulp(ref)
+    elif out == "f16":
+        ref = oracle.decode("f16", oracle.round_f16(Dref))
+        tol = REL * S + ABS + f16_ulp(ref)
     else:
         ref = Dref
         tol = REL * S + ABS
-    err = np.abs(D - ref)
-    bad = ~(err <= tol)
+    with np.errstate(invalid="ignore"):  # inf - inf where both overflowed
+        err = np.abs(D - ref)
+    bad = ~((err <= tol) | (D == ref))  # equal infinities (a 16-bit overflow) agree
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(
@@ -82,13 +98,14 @@ def run_case(c: dict, mode: str = "mask", out_dtype=torch.float32, rows=None, ch
     if rows is None:
         rows = np.arange(M)
     Dg = D.float().cpu().numpy()[rows] if out_dtype != torch.int32 else D.cpu().numpy()[rows]
-    C_np = None if c["C"] is None else c["C"].numpy()
+    C_np = None if c["C"] is None else inputs.bits(c["C"])
     if ta in ("s8", "u8"):
         Dref = oracle.mma_i64(v_ref, i_ref, inputs.bits(c["B"]), C_np, ta, tb, K, rows=rows)
         if check:
             assert np.array_equal(Dg.astype(np.int64), oracle.wrap_i32(Dref).astype(np.int64))
         return Dg, Dref, None
-    Dref, S = oracle.mma_f64(v_ref, i_ref, inputs.bits(c["B"]), C_np, ta, tb, K, rows=rows)
+    Dref, S = oracle.mma_f64(v_ref, i_ref, inputs.bits(c["B"]), C_np, ta, tb, K,
+                             tc=c.get("tc") or "f32", rows=rows)
     if check:
-        check_float(Dg, Dref, S, out_dtype == torch.bfloat16, f"{ta} {M}x{N}x{K}")
+        check_float(Dg, Dref, S, OUT_KIND[out_dtype], f"{ta} {M}x{N}x{K}")
     return Dg, Dref, S

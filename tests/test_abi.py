@@ -196,3 +196,19 @@ def test_four_bit_valid_calls_reach_the_device_check():
     need = sp.lib().sp24_mma_workspace_bytes(S4, S4, 128, 128, 128)
     assert _compress(t=S4) == NODEV
     assert _mma(ta=S4, tb=S4, tc=S32, td=S32, ws=FAKE, ws_bytes=need) == NODEV
+
+
+def test_16bit_accumulator_argument_checks():
+    assert _mma(tc=S32) == UNSUPPORTED
+    assert _mma(td=S32) == UNSUPPORTED
+    assert _mma(td=E4M3) == UNSUPPORTED
+    assert _mma(tc=F16, ldc=132) == ALIGN          # 264-byte pitch
+    assert _mma(tc=BF16, ldc=100) == INVALID
+    assert _bmma(tc=F16, sc=128 * 128 + 4) == ALIGN  # 32776-byte stride
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
+def test_16bit_accumulator_calls_reach_the_device_check():
+    assert _mma(ta=F16, tb=F16, tc=F16, td=F16, ldc=136, ldd=136) == NODEV
+    assert _mma(ta=BF16, tb=BF16, tc=BF16, td=BF16) == NODEV
+    assert _mma(ta=E4M3, tb=E5M2, tc=BF16, td=F16) == NODEV

@@ -235,3 +235,40 @@ def test_int8_wraps_like_int32():
 def test_config4_full_size_int8(ta):
     c = inputs.config4(ta)
     run_case(c, mode="mask", out_dtype=torch.int32, rows=sample_rows(c["M"])[::4])
+
+
+# ---- 16-bit C and D: the FP16- / BF16-accumulate forms and mixed accumulator types -------
+
+@pytest.mark.parametrize("ta,tc,out", [("f16", "f16", torch.float16),
+                                       ("bf16", "bf16", torch.bfloat16),
+                                       ("f16", "f32", torch.float16),
+                                       ("bf16", "f16", torch.float32),
+                                       ("e4m3", "bf16", torch.float16),
+                                       ("e5m2", "f16", torch.bfloat16)])
+@pytest.mark.parametrize("M,N,K", [(200, 16, 384), (130, 96, 256), (257, 272, 1056)])
+def test_16bit_accumulator_forms(ta, tc, out, M, N, K):
+    # narrow (N <= 32), single (N <= 128) and pair (N > 128) variants, ragged M and N; FP8
+    # operands are small integers (a tensor scaled to the FP8 maximum would overflow f16)
+    c = inputs.case(ta, ta, M, N, K, seed=M + N, tc=tc,
+                    dist="int4" if ta in ("e4m3", "e5m2") else "normal")
+    run_case(c, mode="mask", out_dtype=out)
+
+
+def test_f16_accumulate_full_size_sampled():
+    # the FP16-accumulate form (f16 A, B, C, D) at 4096^3, checked on sampled rows
+    c = inputs.case("f16", "f16", 4096, 4096, 4096, seed=77, tc="f16")
+    run_case(c, mode="mask", out_dtype=torch.float16, rows=sample_rows(4096))
+
+
+def test_f16_output_overflows_to_infinity():
+    # a result beyond the binary16 range rounds to +-inf, as the oracle's rounding does
+    # every kept a = 4 and b = +-4 by column: the sums are +-1024 (K = 128), C = +-65000
+    # with the same sign, so every exact result is +-66024 (beyond 65519.99...)
+    M, N, K = 128, 64, 128
+    c = inputs.case("f16", "f16", M, N, K, seed=4, tc="f16", dist="int4")
+    c["A"] = torch.where(c["mask"], torch.tensor(4.0), torch.tensor(0.0)).to(torch.float16)
+    sign = torch.where(torch.arange(N) % 2 == 0, -1.0, 1.0)
+    c["B"] = (4.0 * sign).expand(K, N).contiguous().to(torch.float16)
+    c["C"] = (65000.0 * sign).expand(M, N).contiguous().to(torch.float16)
+    Dg, Dref, _ = run_case(c, mode="mask", out_dtype=torch.float16)
+    assert np.all(np.isinf(Dg)) and np.all(np.sign(Dg) == sign.numpy())
