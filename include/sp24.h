@@ -149,6 +149,21 @@ sp24_status sp24_meta_prepare(sp24_dtype t, int64_t M, int64_t K, const uint32_t
                               int64_t ldi, void *meta, void *stream);
 
 /*
+ * sp24_compress_meta -- sp24_compress and sp24_meta_prepare in one pass over A: writes
+ * values, the canonical index (optional) and the metadata image sp24_mma reads, with the
+ * contents the two calls write.  One read of A instead of a read of A plus a read of the
+ * index, and one launch instead of two ("Structured sparsity (2:4 pattern)": the
+ * compression; the image is this library's own format for tensor memory).
+ * Arguments as in sp24_compress, plus:
+ * index : device or NULL (then no canonical index is written and ldi is ignored).
+ * meta  : device, sp24_meta_bytes(t, M, K) bytes, 16-byte aligned.
+ */
+sp24_status sp24_compress_meta(sp24_dtype t, int64_t M, int64_t K, const void *A, int64_t lda,
+                               const uint8_t *mask, int64_t ldm, sp24_mode mode, void *values,
+                               int64_t ldv, uint32_t *index, int64_t ldi, void *meta,
+                               int32_t *d_status, void *stream);
+
+/*
  * sp24_mma_workspace_bytes -- device workspace sp24_mma needs for (ta, tb, M, N, K): for
  * integer operands the bytes of both operands widened to bf16 (A_c: M x K/2, B: K x N
  * with the row pitch rounded up to 8 elements); 0 for float operands.

@@ -25,7 +25,7 @@ import torch
 
 from . import _build
 
-__all__ = ["lib", "compress", "decompress", "meta_bytes", "meta_prepare", "mma", "mma_batched",
+__all__ = ["lib", "compress", "compress_meta", "decompress", "meta_bytes", "meta_prepare", "mma", "mma_batched",
            "workspace_bytes",
            "SparseMatrix", "Sp24Error", "DEV_NOT_2_4", "DEV_TIMEOUT", "DTYPE_CODES"]
 
@@ -42,7 +42,7 @@ DEV_NOT_2_4 = 1
 DEV_TIMEOUT = 2
 
 # every symbol include/sp24.h declares
-EXPORTS = ("sp24_compress", "sp24_decompress", "sp24_meta_bytes", "sp24_meta_prepare",
+EXPORTS = ("sp24_compress", "sp24_compress_meta", "sp24_decompress", "sp24_meta_bytes", "sp24_meta_prepare",
            "sp24_mma_workspace_bytes", "sp24_mma", "sp24_mma_strided_batched", "sp24_mma_i8_noalloc",
            "sp24_diag_wait_timeout", "sp24_status_string", "sp24_version")
 
@@ -70,6 +70,9 @@ def lib():
             i64, p, i32, u64 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
             L.sp24_compress.restype = i32
             L.sp24_compress.argtypes = [i32, i64, i64, p, i64, p, i64, i32, p, i64, p, i64, p, p]
+            L.sp24_compress_meta.restype = i32
+            L.sp24_compress_meta.argtypes = [i32, i64, i64, p, i64, p, i64, i32, p, i64, p, i64,
+                                             p, p, p]
             L.sp24_decompress.restype = i32
             L.sp24_decompress.argtypes = [i32, i64, i64, p, i64, p, i64, p, i64, p]
             L.sp24_meta_bytes.restype = ctypes.c_size_t
@@ -165,6 +168,36 @@ def compress(A: torch.Tensor, mode: str = "exact", mask: torch.Tensor | None = N
         t, M, K, _ptr(A), _ld(A, elem), _ptr(m), ldm, MODES[mode], _ptr(values),
         _ld(values, elem), _ptr(index), _ld(index), _ptr(status), _stream(stream)))
     return values, index
+
+
+def compress_meta(A: torch.Tensor, mode: str = "exact", mask: torch.Tensor | None = None,
+                  status: torch.Tensor | None = None, stream=None, elem: str | None = None,
+                  with_index: bool = True):
+    """compress() and meta_prepare() in one pass: (values, index or None, meta)."""
+    t = _elem_code(A, elem)
+    per = 2 if elem in PACKED4 else 1
+    M, K = A.shape[0], A.shape[1] * per
+    vcols = K // 2 // per
+    if per == 2:
+        values = torch.empty((M, (vcols + 15) // 16 * 16), dtype=A.dtype,
+                             device=A.device)[:, :vcols]
+    else:
+        values = torch.empty((M, vcols), dtype=A.dtype, device=A.device)
+    index = torch.empty((M, K // 32), dtype=torch.int32, device=A.device) if with_index else None
+    nbytes = int(lib().sp24_meta_bytes(t, M, K))
+    meta = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=A.device)
+    m = None
+    ldm = K
+    if mode == "mask":
+        if mask is None:
+            raise ValueError("mask mode needs a mask")
+        m = mask.to(torch.uint8) if mask.dtype != torch.uint8 else mask
+        ldm = _ld(m)
+    _check("sp24_compress_meta", lib().sp24_compress_meta(
+        t, M, K, _ptr(A), _ld(A, elem), _ptr(m), ldm, MODES[mode], _ptr(values),
+        _ld(values, elem), _ptr(index), _ld(index) if index is not None else 0, _ptr(meta),
+        _ptr(status), _stream(stream)))
+    return values, index, meta
 
 
 def decompress(values: torch.Tensor, index: torch.Tensor, K: int, stream=None,
@@ -280,8 +313,8 @@ class SparseMatrix:
 
     @classmethod
     def from_dense(cls, A, mode="exact", mask=None, status=None, stream=None):
-        values, index = compress(A, mode=mode, mask=mask, status=status, stream=stream)
-        meta = meta_prepare(index, A.dtype, A.shape[0], A.shape[1], stream=stream)
+        values, index, meta = compress_meta(A, mode=mode, mask=mask, status=status,
+                                            stream=stream)
         return cls(values, index, meta, A.shape[1])
 
     def to_dense(self, stream=None):

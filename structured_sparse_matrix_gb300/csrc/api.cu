@@ -106,7 +106,46 @@ sp24_status sp24_compress(sp24_dtype t, int64_t M, int64_t K, const void* A, int
   a.M = M;
   a.K = K;
   a.status = d_status;
+  a.meta = nullptr;
+  a.mtiles = a.ksteps = 0;
   if (launch_compress(a, t, mode, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SP24_ERR_CUDA;
+  return SP24_OK;
+}
+
+sp24_status sp24_compress_meta(sp24_dtype t, int64_t M, int64_t K, const void* A, int64_t lda,
+                               const uint8_t* mask, int64_t ldm, sp24_mode mode, void* values,
+                               int64_t ldv, uint32_t* index, int64_t ldi, void* meta,
+                               int32_t* d_status, void* stream) {
+  if (!is_ab_type(t)) return SP24_ERR_UNSUPPORTED;
+  if (mode < SP24_MODE_EXACT || mode > SP24_MODE_MAGNITUDE) return SP24_ERR_INVALID_ARG;
+  if (M < 0 || K < 0 || (K % 32) != 0) return SP24_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return SP24_OK;
+  if (!A || !values || !meta || (mode == SP24_MODE_MASK && !mask)) return SP24_ERR_INVALID_ARG;
+  if (lda < K || ldv < K / 2 || (index && ldi < K / 32) || (mode == SP24_MODE_MASK && ldm < K))
+    return SP24_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(values) || !aligned16(meta) ||
+      (reinterpret_cast<uintptr_t>(index) & 3u) || !ld_ok16(t, lda) || !ld_ok16(t, ldv))
+    return SP24_ERR_ALIGN;
+  if (mode == SP24_MODE_MASK && (!aligned16(mask) || ldm % 16)) return SP24_ERR_ALIGN;
+  int sms = 0;
+  if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
+  CompressArgs a;
+  a.A = static_cast<const uint8_t*>(A);
+  a.lda_bytes = ld_bytes(t, lda);
+  a.mask = mask;
+  a.ldm = ldm;
+  a.values = static_cast<uint8_t*>(values);
+  a.ldv_bytes = ld_bytes(t, ldv);
+  a.index = index;
+  a.ldi = ldi;
+  a.M = M;
+  a.K = K;
+  a.status = d_status;
+  a.meta = static_cast<uint32_t*>(meta);
+  a.mtiles = meta_mtiles(M);
+  a.ksteps = (K + stage_k(t) - 1) / stage_k(t);
+  if (launch_compress_meta(a, t, mode, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return SP24_ERR_CUDA;
   return SP24_OK;
 }

@@ -244,11 +244,37 @@ __device__ __forceinline__ void compress_chunk(const uint4& v, const uint32_t (&
   vals = make_uint2(out[0], out[1]);
 }
 
+// One 16-byte chunk of A (row, chunk cc of the row) and, in mask mode, its mask bytes
+// (one per element, one word per group).
+template <int EB, int MODE>
+__device__ __forceinline__ void load_chunk(const CompressArgs& a, int64_t row, int64_t cc,
+                                           uint4& v, uint32_t (&m)[8]) {
+  constexpr int kElems = 128 / EB;
+  v = __ldcs(reinterpret_cast<const uint4*>(a.A + row * a.lda_bytes + cc * 16));
+  if constexpr (MODE == 1) {
+    if constexpr (kElems == 8) {
+      const uint2 mm = __ldcs(reinterpret_cast<const uint2*>(a.mask + row * a.ldm + cc * 8));
+      m[0] = mm.x;
+      m[1] = mm.y;
+    } else {
+#pragma unroll
+      for (int h = 0; h < kElems / 16; ++h) {  // 16 mask bytes per load
+        const uint4 mm = __ldcs(
+            reinterpret_cast<const uint4*>(a.mask + row * a.ldm + cc * kElems + 16 * h));
+        m[4 * h + 0] = mm.x;
+        m[4 * h + 1] = mm.y;
+        m[4 * h + 2] = mm.z;
+        m[4 * h + 3] = mm.w;
+      }
+    }
+  }
+}
+
 // EB = element bits (16, 8 or 4); MODE = SP24_MODE_* value.  Each warp step covers
 // kUnroll runs of 32 consecutive chunks; all their loads are issued before any is used,
 // so a thread keeps kUnroll 16-byte loads (plus mask loads) in flight.
 template <int EB, int CLS, int MODE>
-__global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
+__global__ void __launch_bounds__(256, EB == 4 ? 3 : 4) compress_kernel(CompressArgs a) {
   constexpr int kElems = 128 / EB;   // elements per 16-byte chunk
   constexpr int kGroups = kElems / 4;  // groups per chunk
   constexpr int kLanesPerWord = 32 / kElems;
@@ -282,27 +308,7 @@ __global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
       v[u] = make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int q = 0; q < 8; ++q) mbits[u][q] = 0;
-      if (active[u]) {
-        v[u] = __ldcs(reinterpret_cast<const uint4*>(a.A + row[u] * a.lda_bytes + cc[u] * 16));
-        if constexpr (MODE == 1) {
-          if constexpr (kElems == 8) {
-            const uint2 m =
-                __ldcs(reinterpret_cast<const uint2*>(a.mask + row[u] * a.ldm + cc[u] * 8));
-            mbits[u][0] = m.x;
-            mbits[u][1] = m.y;
-          } else {
-#pragma unroll
-            for (int h = 0; h < kElems / 16; ++h) {  // 16 mask bytes per load
-              const uint4 m = __ldcs(reinterpret_cast<const uint4*>(
-                  a.mask + row[u] * a.ldm + cc[u] * kElems + 16 * h));
-              mbits[u][4 * h + 0] = m.x;
-              mbits[u][4 * h + 1] = m.y;
-              mbits[u][4 * h + 2] = m.z;
-              mbits[u][4 * h + 3] = m.w;
-            }
-          }
-        }
-      }
+      if (active[u]) load_chunk<EB, MODE>(a, row[u], cc[u], v[u], mbits[u]);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -320,6 +326,116 @@ __global__ void __launch_bounds__(256, 4) compress_kernel(CompressArgs a) {
       }
       if (active[u] && (lane % kLanesPerWord) == 0) {
         a.index[row[u] * a.ldi + (cc[u] * kElems) / 32] = word;
+      }
+    }
+  }
+  if (a.status != nullptr && __any_sync(0xFFFFFFFFu, any_flag != 0u) && lane == 0)
+    atomicOr(a.status, kDevNot24);
+}
+
+// Compression and the sparse GEMM's metadata image in one pass (the image the separate
+// re-layout kernel in meta.cu writes from the canonical index; its layout is described
+// there).  One warp per (16-row band of a 128-row tile, GEMM stage): it compresses the
+// band's 16 rows over the stage's K range chunk by chunk as compress_kernel does (values
+// and canonical index words, which stay the interchange format; index may be null), then
+// writes the band's rows of the stage's 4 MMA blocks with 16-byte stores.  Rows beyond M
+// and K beyond the operand count as all-zero groups (pattern {0,1}): the image padding.
+// kL8: the FP8 layout (256 dense K per stage, lane = row, the MMA's two canonical words);
+// otherwise the 16-bit layout (128 dense K per stage; lane 16b + l of band b holds 16-bit
+// halves h = l/8 of the canonical words of rows l%8 and l%8 + 8), also used by integers.
+//
+// Lane L of the warp covers chunk c = L % kCpr of rows kRpi*k + L / kCpr (k = 0 .. kIters-1)
+// of the band, so row r and row r + 8 of the band sit in the same lane (k and k + kIters/2).
+template <int EB, int CLS, int MODE, bool kL8>
+__global__ void __launch_bounds__(256, 3) compress_meta_kernel(CompressArgs a) {
+  constexpr int kStageK = kL8 ? 256 : 128;
+  constexpr int kElems = 128 / EB;                 // elements per 16-byte chunk
+  constexpr int kGroups = kElems / 4;
+  constexpr int kCpr = kStageK / kElems;           // chunks per row and stage: 16, 16, 8, 4
+  constexpr int kRpi = 32 / kCpr;                  // rows per warp iteration: 2, 2, 4, 8
+  constexpr int kIters = 16 / kRpi;                // 8, 8, 4, 2
+  constexpr int kLanesPerWord = kElems < 32 ? 32 / kElems : 1;
+  constexpr int kHalves = kElems >= 16 ? kElems / 16 : 1;  // 16-K halves a chunk starts
+  constexpr uint32_t kPadWord = 0x44444444u;
+  constexpr uint32_t kPadNibs = kGroups == 8 ? kPadWord : (kPadWord >> (32 - 4 * kGroups));
+  static_assert(kCpr * kRpi == 32 && kIters * kRpi == 16, "warp tiling");
+  static_assert(!kL8 || EB == 8, "the FP8 layout holds 8-bit elements");
+  const int lane = threadIdx.x & 31;
+  const int c = lane % kCpr, rsub = lane / kCpr;
+  const int64_t units = a.mtiles * 8 * a.ksteps;
+  const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  uint4* meta = reinterpret_cast<uint4*>(a.meta);
+  uint32_t any_flag = 0;
+  constexpr int kBatch = kIters < 4 ? kIters : 4;
+  uint4 v[kBatch];
+  uint32_t m[kBatch][8];
+
+  for (int64_t u = warp0; u < units; u += nwarps) {
+    const int64_t band = u / a.ksteps, s = u - band * a.ksteps;
+    const int64_t cc = s * kCpr + c;              // chunk of the row
+    const bool kin = cc * kElems < a.K;
+    // image rows of this band: block (tile, stage, MMA j) starts at uint4
+    // ((tile * ksteps + s) * 4 + j) * 128, the band's rows at + (band % 8) * 16
+    uint4* img = meta + ((band >> 3) * a.ksteps + s) * (kMmasPerStage * 128) + (band & 7) * 16;
+    uint32_t half16[kIters][kHalves];
+#pragma unroll
+    for (int k = 0; k < kIters; ++k) {
+      const int64_t row = band * 16 + kRpi * k + rsub;
+      const bool valid = kin && row < a.M;
+      // loads of kBatch iterations are issued together before any of them is used
+      if (k % kBatch == 0) {
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int64_t rb = row + kRpi * b;
+          v[b] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) m[b][q] = 0;
+          if (kin && rb < a.M) load_chunk<EB, MODE>(a, rb, cc, v[b], m[b]);
+        }
+      }
+      uint2 vals;
+      uint32_t nibs, flags;
+      compress_chunk<EB, CLS, MODE>(v[k % kBatch], m[k % kBatch], vals, nibs, flags);
+      if (!valid) nibs = kPadNibs;
+      if (valid) {
+        any_flag |= flags & 1u;
+        __stcs(reinterpret_cast<uint2*>(a.values + row * a.ldv_bytes + cc * 8), vals);
+      }
+      // the row's canonical word of this chunk, merged across the lanes that share it
+      uint32_t word = nibs << ((4 * kGroups) * (lane % kLanesPerWord));
+      if constexpr (kLanesPerWord > 1) {
+#pragma unroll
+        for (int o = 1; o < kLanesPerWord; o <<= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, o);
+      }
+      if (valid && a.index != nullptr && (lane % kLanesPerWord) == 0)
+        a.index[row * a.ldi + (cc * kElems) / 32] = word;
+      if constexpr (kL8) {
+        // MMA j = c / 4 reads canonical words 2j (lanes 4j, 4j+1) and 2j+1 (4j+2, 4j+3)
+        const uint32_t next = __shfl_xor_sync(0xFFFFFFFFu, word, 2);
+        if ((c & 3) == 0)
+          img[(c >> 2) * 128 + kRpi * k + rsub] = make_uint4(word, next, kPadWord, kPadWord);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kHalves; ++i) {
+          const int hidx = (c * kElems) / 16 + i;  // 16-K half of the stage (0 .. 7)
+          half16[k][i] = (word >> (16 * (hidx & 1))) & 0xFFFFu;
+        }
+      }
+    }
+    if constexpr (!kL8) {
+      // lanes whose chunk starts a 16-K half write it for rows r (< 8) and r + 8 of the band
+      if ((c * kElems) % 16 == 0) {
+#pragma unroll
+        for (int k = 0; k < kIters / 2; ++k) {
+#pragma unroll
+          for (int i = 0; i < kHalves; ++i) {
+            const int hidx = (c * kElems) / 16 + i;
+            const int j = hidx >> 1, h = hidx & 1;
+            const uint32_t w = half16[k][i] | (half16[k + kIters / 2][i] << 16);
+            img[j * 128 + kRpi * k + rsub + 8 * h] = make_uint4(w, kPadWord, kPadWord, kPadWord);
+          }
+        }
       }
     }
   }
@@ -404,6 +520,36 @@ cudaError_t launch_compress(const CompressArgs& a, int dtype, int mode, int num_
     case kU8: return launch_compress_cls<8, kUnsigned8>(a, mode, grid, s);
     case kS4: return launch_compress_cls<4, kSigned4>(a, mode, grid, s);
     default: return launch_compress_cls<4, kUnsigned4>(a, mode, grid, s);
+  }
+}
+
+namespace {
+template <int EB, int CLS, bool kL8>
+cudaError_t launch_compress_meta_cls(const CompressArgs& a, int mode, int grid, cudaStream_t s) {
+  switch (mode) {
+    case 0: compress_meta_kernel<EB, CLS, 0, kL8><<<grid, 256, 0, s>>>(a); break;
+    case 1: compress_meta_kernel<EB, CLS, 1, kL8><<<grid, 256, 0, s>>>(a); break;
+    default: compress_meta_kernel<EB, CLS, 2, kL8><<<grid, 256, 0, s>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_compress_meta(const CompressArgs& a, int dtype, int mode, int num_sms,
+                                 cudaStream_t s) {
+  const int64_t warps = a.mtiles * 8 * a.ksteps;  // one warp per (band, stage)
+  int64_t want = (warps + 7) / 8;
+  int64_t cap = int64_t(num_sms) * 3;
+  const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+  switch (dtype) {
+    case kF16:
+    case kBF16: return launch_compress_meta_cls<16, kFloat16, false>(a, mode, grid, s);
+    case kE4M3:
+    case kE5M2: return launch_compress_meta_cls<8, kFloat8, true>(a, mode, grid, s);
+    case kS8: return launch_compress_meta_cls<8, kSigned8, false>(a, mode, grid, s);
+    case kU8: return launch_compress_meta_cls<8, kUnsigned8, false>(a, mode, grid, s);
+    case kS4: return launch_compress_meta_cls<4, kSigned4, false>(a, mode, grid, s);
+    default: return launch_compress_meta_cls<4, kUnsigned4, false>(a, mode, grid, s);
   }
 }
 

@@ -60,6 +60,9 @@ struct CompressArgs {
   uint32_t* index; int64_t ldi;
   int64_t M, K;
   int32_t* status;
+  // fused compression + metadata image only: the image and its tiles / stages
+  uint32_t* meta;
+  int64_t mtiles, ksteps;
 };
 
 struct DecompressArgs {
@@ -77,6 +80,8 @@ struct MetaArgs {
 };
 
 cudaError_t launch_compress(const CompressArgs& a, int dtype, int mode, int num_sms, cudaStream_t s);
+cudaError_t launch_compress_meta(const CompressArgs& a, int dtype, int mode, int num_sms,
+                                 cudaStream_t s);
 cudaError_t launch_decompress(const DecompressArgs& a, int dtype, int num_sms, cudaStream_t s);
 cudaError_t launch_meta_prepare(const MetaArgs& a, int dtype, int num_sms, cudaStream_t s);
 // rows x cols 8- or 4-bit integers (`bits`; pitch ld_src bytes) -> bfloat16 (pitch

@@ -79,12 +79,20 @@ def gpu_compress(c: dict, mode: str):
     return values, index, status
 
 
-def run_case(c: dict, mode: str = "mask", out_dtype=torch.float32, rows=None, check=True):
-    """Compress + meta_prepare + mma on the GPU, oracle on the CPU, compare."""
+def run_case(c: dict, mode: str = "mask", out_dtype=torch.float32, rows=None, check=True,
+             fused: bool = False):
+    """Compress + meta_prepare + mma on the GPU (fused: compress_meta), oracle on the CPU,
+    compare."""
     ta, tb = c["ta"], c["tb"]
     M, N, K = c["M"], c["N"], c["K"]
-    values, index, status = gpu_compress(c, mode)
-    meta = sp.meta_prepare(index, c["A"].dtype, M, K)
+    if fused:
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        values, index, meta = sp.compress_meta(
+            dev(c["A"]), mode=mode, mask=dev(c["mask"]) if mode == "mask" else None,
+            status=status)
+    else:
+        values, index, status = gpu_compress(c, mode)
+        meta = sp.meta_prepare(index, c["A"].dtype, M, K)
     B = dev(c["B"])
     C = dev(c["C"])
     D = sp.mma(values, meta, B, C, out_dtype=out_dtype)

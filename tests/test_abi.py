@@ -212,3 +212,23 @@ def test_16bit_accumulator_calls_reach_the_device_check():
     assert _mma(ta=F16, tb=F16, tc=F16, td=F16, ldc=136, ldd=136) == NODEV
     assert _mma(ta=BF16, tb=BF16, tc=BF16, td=BF16) == NODEV
     assert _mma(ta=E4M3, tb=E5M2, tc=BF16, td=F16) == NODEV
+
+
+def test_compress_meta_argument_checks():
+    L = sp.lib()
+
+    def cm(t=F16, M=64, K=128, A=FAKE, lda=128, mask=None, ldm=128, mode=0, values=FAKE,
+           ldv=64, index=FAKE, ldi=4, meta=FAKE):
+        return L.sp24_compress_meta(t, M, K, A, lda, mask, ldm, mode, values, ldv, index, ldi,
+                                    meta, None, None)
+    assert cm(t=F32) == UNSUPPORTED
+    assert cm(K=100) == INVALID
+    assert cm(meta=None) == INVALID
+    assert cm(mode=1) == INVALID                       # mask mode without a mask
+    assert cm(ldi=2) == INVALID
+    assert cm(meta=FAKE_ODD) == ALIGN
+    assert cm(lda=132) == ALIGN
+    assert cm(M=0) == OK
+    if not torch.cuda.is_available():
+        assert cm(index=None, ldi=0) == NODEV           # the index is optional
+        assert cm() == NODEV

@@ -168,3 +168,70 @@ def test_meta_prepare_layout(ta, M, K):
     want = _meta_image_np(index_np(index), M, K, ta in ("e4m3", "e5m2", "s8", "u8"))
     assert got.shape == want.shape
     assert np.array_equal(got, want)
+
+
+# --- compression and the metadata image in one pass (sp24_compress_meta) -------------------
+
+def _fused_inputs(ta, M, K, seed, mode):
+    """Dense operand for ta (4-bit types as one nibble per byte), its mask, and the tensor
+    handed to the library (4-bit types packed two per byte)."""
+    mask = inputs.keep_mask(M, K, inputs.gen(seed + 1))
+    if ta in ("s4", "u4"):
+        dense = inputs.gen_nibbles((M, K), inputs.gen(seed))
+        if mode == "exact":
+            dense = np.where(mask.numpy(), dense, 0).astype(np.uint8)
+        return dense, mask, torch.from_numpy(inputs.pack4(dense)).cuda()
+    c = _dense_case(ta, M, K, seed, with_zeros=True)
+    A = inputs.apply_mask(c["A"], mask) if mode == "exact" else c["A"]
+    return inputs.bits(A), mask, A.cuda()
+
+
+@pytest.mark.parametrize("ta", TYPES + ["s4", "u4"])
+@pytest.mark.parametrize("mode", ["exact", "mask", "magnitude"])
+@pytest.mark.parametrize("M,K", [(37, 160), (200, 352), (257, 544)])
+def test_compress_meta_matches_oracle(ta, mode, M, K):
+    # ragged against the band (16 rows), the tile pair (256 rows) and the stage (128 / 256 K)
+    dense, mask, A = _fused_inputs(ta, M, K, seed=M + K, mode=mode)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    elem = ta if ta in ("s4", "u4") else None
+    values, index, meta = sp.compress_meta(A, mode=mode,
+                                           mask=mask.cuda() if mode == "mask" else None,
+                                           status=status, elem=elem)
+    torch.cuda.synchronize()
+    v_ref, i_ref, flags = oracle.compress(dense, ta, mode,
+                                          mask=mask.numpy() if mode == "mask" else None)
+    got_v = values.cpu().numpy() if elem else inputs.bits(values.cpu())
+    if elem:
+        got_v = inputs.unpack4(got_v)
+    assert np.array_equal(index_np(index), i_ref)
+    assert np.array_equal(got_v, v_ref)
+    assert bool(status.item() & sp.DEV_NOT_2_4) == bool(flags.any())
+    want = _meta_image_np(i_ref, M, K, ta in ("e4m3", "e5m2"))
+    got = meta.cpu().numpy().view(np.uint32)
+    assert got.shape == want.shape
+    assert np.array_equal(got, want)
+
+
+def test_compress_meta_without_index_and_padded_pitch():
+    M, K = 130, 256
+    big = inputs.values((M, K + 64), "bf16", "normal", inputs.gen(31)).cuda()
+    A = big[:, 32:32 + K]
+    values, index, meta = sp.compress_meta(A, mode="magnitude", with_index=False)
+    v2, i2 = sp.compress(A, mode="magnitude")
+    m2 = sp.meta_prepare(i2, torch.bfloat16, M, K)
+    torch.cuda.synchronize()
+    assert index is None
+    assert torch.equal(values, v2) and torch.equal(meta, m2)
+
+
+def test_compress_meta_full_size_config5_magnitude():
+    # the LLM layer's weight (14336 x 4096): image equal to the separate re-layout's
+    c = inputs.config5(N=16)
+    A = c["A"].cuda()
+    values, index, meta = sp.compress_meta(A, mode="magnitude")
+    v2, i2 = sp.compress(A, mode="magnitude")
+    m2 = sp.meta_prepare(i2, torch.bfloat16, A.shape[0], A.shape[1])
+    torch.cuda.synchronize()
+    assert torch.equal(index, i2) and torch.equal(values, v2) and torch.equal(meta, m2)
+    v_ref, i_ref, _ = oracle.compress(inputs.bits(c["A"]), "bf16", "magnitude")
+    assert np.array_equal(index_np(index), i_ref)

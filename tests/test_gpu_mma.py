@@ -272,3 +272,20 @@ def test_f16_output_overflows_to_infinity():
     c["C"] = (65000.0 * sign).expand(M, N).contiguous().to(torch.float16)
     Dg, Dref, _ = run_case(c, mode="mask", out_dtype=torch.float16)
     assert np.all(np.isinf(Dg)) and np.all(np.sign(Dg) == sign.numpy())
+
+
+# ---- the product on the image written by the fused compression pass ---------------------
+
+@pytest.mark.parametrize("ta,tc,out", [("bf16", "f32", torch.float32),
+                                       ("e4m3", None, torch.bfloat16),
+                                       ("s8", "s32", torch.int32)])
+@pytest.mark.parametrize("M,N,K", [(200, 16, 384), (257, 272, 1056)])
+def test_product_on_fused_image(ta, tc, out, M, N, K):
+    c = inputs.case(ta, "s8" if ta == "s8" else ta, M, N, K, seed=M + 3, tc=tc,
+                    dist="full" if ta == "s8" else "normal")
+    run_case(c, mode="mask", out_dtype=out, fused=True)
+
+
+def test_config2_through_the_fused_pass():
+    c = inputs.config2()
+    run_case(c, mode="mask", rows=sample_rows(c["M"]), fused=True)
