@@ -77,10 +77,14 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# the sources sp24_mma's kernel is built from (its ncu summary is stale once they change)
+SPMMA_SOURCES = ("spmma.cu", "sp24_device.cuh", "sp24_internal.h")
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     cs = os.path.join(ROOT, "structured_sparse_matrix_gb300", "csrc")
-    for name in sorted(os.listdir(cs)):
+    for name in SPMMA_SOURCES:
         with open(os.path.join(cs, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -304,19 +308,33 @@ def gpu_arm(args, world, rank, local):
     ws_bytes = sp.workspace_bytes(tdt, base["B"].dtype, M, N, K)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
 
+    fused = args.pass_mode == "fused"
+    # kernels one step launches: compression (+ re-layout), the product (+ two widening
+    # passes for integer operands)
+    launches_per_step = (1 if fused else 2) + (3 if integer else 1)
+
     def launch(s, ev=None):
-        # the three C-ABI calls of one step, on the current stream
+        # the C-ABI calls of one step, on the current stream
         st = sp._stream(stream)
         m = s["mask"]
         if ev is not None:
             ev[0].record(stream)
-        rc = L.sp24_compress(cs["ta"], M, K, sp._ptr(s["A"]), K, sp._ptr(m), K,
-                             sp.MODES[mode], sp._ptr(s["values"]), K // 2, sp._ptr(s["index"]),
-                             K // 32, sp._ptr(status), st)
-        if ev is not None:
-            ev[1].record(stream)
-        rc |= L.sp24_meta_prepare(cs["ta"], M, K, sp._ptr(s["index"]), K // 32,
-                                  sp._ptr(s["meta"]), st)
+        if fused:
+            # compression and the metadata image in one pass
+            rc = L.sp24_compress_meta(cs["ta"], M, K, sp._ptr(s["A"]), K, sp._ptr(m), K,
+                                      sp.MODES[mode], sp._ptr(s["values"]), K // 2,
+                                      sp._ptr(s["index"]), K // 32, sp._ptr(s["meta"]),
+                                      sp._ptr(status), st)
+            if ev is not None:
+                ev[1].record(stream)
+        else:
+            rc = L.sp24_compress(cs["ta"], M, K, sp._ptr(s["A"]), K, sp._ptr(m), K,
+                                 sp.MODES[mode], sp._ptr(s["values"]), K // 2,
+                                 sp._ptr(s["index"]), K // 32, sp._ptr(status), st)
+            if ev is not None:
+                ev[1].record(stream)
+            rc |= L.sp24_meta_prepare(cs["ta"], M, K, sp._ptr(s["index"]), K // 32,
+                                      sp._ptr(s["meta"]), st)
         if ev is not None:
             ev[2].record(stream)
         rc |= L.sp24_mma(cs["ta"], cs["tb"], cs["tc"], cs["td"], M, N, K, sp._ptr(s["values"]),
@@ -388,12 +406,18 @@ def gpu_arm(args, world, rank, local):
     cbytes = M * K * esz + (M * K if mode == "mask" else 0) + M * K // 2 * esz + M * K // 8
     kernels = {
         "note": "sp24_mma time includes the int8->bf16 widening pass" if integer else None,
-        "sp24_compress_us": k_compress * 1e3,
-        "sp24_compress_gbs": cbytes / (k_compress * 1e-3) / 1e9,
-        "sp24_meta_prepare_us": k_meta * 1e3,
         "sp24_mma_us": k_mma * 1e3,
         "sp24_mma_tflops": achieved_tf,
     }
+    if fused:
+        # + the image written (the separate pass would read the index and write the image)
+        fbytes = cbytes + sp.meta_bytes(tdt, M, K)
+        kernels["sp24_compress_meta_us"] = k_compress * 1e3
+        kernels["sp24_compress_meta_gbs"] = fbytes / (k_compress * 1e-3) / 1e9
+    else:
+        kernels["sp24_compress_us"] = k_compress * 1e3
+        kernels["sp24_compress_gbs"] = cbytes / (k_compress * 1e-3) / 1e9
+        kernels["sp24_meta_prepare_us"] = k_meta * 1e3
 
     # --- end to end through the C ABI with host buffers: H2D inputs, 3 calls, D2H result
     e2e = None
@@ -447,7 +471,8 @@ def gpu_arm(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ta, "data": "synthetic",
             "config": {"workload": desc, "name": args.config, "M": M, "N": N, "K": K,
-                       "step": f"sp24_compress({mode}) + sp24_meta_prepare + sp24_mma",
+                       "step": (f"sp24_compress_meta({mode}) + sp24_mma" if fused else
+                                f"sp24_compress({mode}) + sp24_meta_prepare + sp24_mma"),
                        "l2": f"{len(sets)} rotating input sets, "
                              f"{len(sets) * set_bytes(sets[0]) / 2**20:.0f} MiB > L2",
                        "parallelism": f"replicas x{world}"},
@@ -455,7 +480,7 @@ def gpu_arm(args, world, rank, local):
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -470,6 +495,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--pass", dest="pass_mode", default="fused", choices=["fused", "separate"],
+                    help="compression and metadata image in one kernel (fused) or two")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     try:

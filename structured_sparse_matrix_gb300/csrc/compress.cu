@@ -16,6 +16,7 @@
 // A (+ mask) once and writes values + index once.
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "sp24_device.cuh"
 #include "sp24_internal.h"
@@ -333,83 +334,179 @@ __global__ void __launch_bounds__(256, EB == 4 ? 3 : 4) compress_kernel(Compress
     atomicOr(a.status, kDevNot24);
 }
 
+// Asynchronous global -> shared copies of one thread (no registers in flight).
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Geometry of the fused pass.  A warp's unit is one (16-row band of a 128-row tile, GEMM
+// stage): kStageK dense K of 16 rows.  Lane L covers chunk c = L % kCpr of rows
+// kRpi * k + L / kCpr (k = 0 .. kIters-1) of the band, so rows r and r + 8 of the band
+// sit in the same lane (k and k + kIters / 2).
+template <int EB, int MODE, bool kL8>
+struct FusedGeo {
+  static constexpr int kStageK = kL8 ? 256 : 128;
+  static constexpr int kElems = 128 / EB;            // elements per 16-byte chunk
+  static constexpr int kCpr = kStageK / kElems;      // chunks per row and stage: 16, 16, 8, 4
+  static constexpr int kRpi = 32 / kCpr;             // rows per warp iteration: 2, 2, 4, 8
+  static constexpr int kIters = 16 / kRpi;           // 8, 8, 4, 2
+  static constexpr int kMaskBytes = MODE == 1 ? kElems : 0;  // mask bytes per chunk
+  static constexpr int kUnitBytes = kIters * 32 * (16 + kMaskBytes);  // staged per unit
+  // units staged per warp: the one being worked on and kBufs - 1 ahead (mask mode stages
+  // more bytes per unit, so fewer fit)
+  static constexpr int kBufs = 2;
+  static constexpr int kWarps = 4;
+  static constexpr int kSmem = kWarps * kBufs * kUnitBytes;
+  static_assert(kCpr * kRpi == 32 && kIters * kRpi == 16, "warp tiling");
+};
+
 // Compression and the sparse GEMM's metadata image in one pass (the image the separate
 // re-layout kernel in meta.cu writes from the canonical index; its layout is described
-// there).  One warp per (16-row band of a 128-row tile, GEMM stage): it compresses the
-// band's 16 rows over the stage's K range chunk by chunk as compress_kernel does (values
-// and canonical index words, which stay the interchange format; index may be null), then
-// writes the band's rows of the stage's 4 MMA blocks with 16-byte stores.  Rows beyond M
-// and K beyond the operand count as all-zero groups (pattern {0,1}): the image padding.
+// there).  Each warp compresses its unit's 16 rows over the stage's K range chunk by chunk
+// as compress_kernel does (values and canonical index words, which stay the interchange
+// format; index may be null), then writes the band's rows of the stage's 4 MMA blocks
+// with 16-byte stores.  Rows beyond M and K beyond the operand count as all-zero groups
+// (pattern {0,1}): the image padding.
 // kL8: the FP8 layout (256 dense K per stage, lane = row, the MMA's two canonical words);
 // otherwise the 16-bit layout (128 dense K per stage; lane 16b + l of band b holds 16-bit
 // halves h = l/8 of the canonical words of rows l%8 and l%8 + 8), also used by integers.
 //
-// Lane L of the warp covers chunk c = L % kCpr of rows kRpi*k + L / kCpr (k = 0 .. kIters-1)
-// of the band, so row r and row r + 8 of the band sit in the same lane (k and k + kIters/2).
+// Loads: every lane copies the chunks (and mask bytes) it will use into its warp's
+// shared-memory ring with cp.async, two units ahead of the one it works on, so each SM
+// keeps 2 x (warps) units of A in flight without holding them in registers.  A lane only
+// ever reads back what it copied itself, so its own cp.async.wait_group is the only
+// synchronisation (no barrier, no spin).
 template <int EB, int CLS, int MODE, bool kL8>
-__global__ void __launch_bounds__(256, 3) compress_meta_kernel(CompressArgs a) {
-  constexpr int kStageK = kL8 ? 256 : 128;
-  constexpr int kElems = 128 / EB;                 // elements per 16-byte chunk
+__global__ void __launch_bounds__(128) compress_meta_kernel(CompressArgs a) {
+  using G = FusedGeo<EB, MODE, kL8>;
+  constexpr int kElems = G::kElems, kCpr = G::kCpr, kRpi = G::kRpi, kIters = G::kIters;
   constexpr int kGroups = kElems / 4;
-  constexpr int kCpr = kStageK / kElems;           // chunks per row and stage: 16, 16, 8, 4
-  constexpr int kRpi = 32 / kCpr;                  // rows per warp iteration: 2, 2, 4, 8
-  constexpr int kIters = 16 / kRpi;                // 8, 8, 4, 2
   constexpr int kLanesPerWord = kElems < 32 ? 32 / kElems : 1;
   constexpr int kHalves = kElems >= 16 ? kElems / 16 : 1;  // 16-K halves a chunk starts
   constexpr uint32_t kPadWord = 0x44444444u;
   constexpr uint32_t kPadNibs = kGroups == 8 ? kPadWord : (kPadWord >> (32 - 4 * kGroups));
-  static_assert(kCpr * kRpi == 32 && kIters * kRpi == 16, "warp tiling");
   static_assert(!kL8 || EB == 8, "the FP8 layout holds 8-bit elements");
-  const int lane = threadIdx.x & 31;
+  extern __shared__ __align__(16) uint8_t fused_smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = lane % kCpr, rsub = lane / kCpr;
   const int64_t units = a.mtiles * 8 * a.ksteps;
   const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
   uint4* meta = reinterpret_cast<uint4*>(a.meta);
+  uint8_t* ring = fused_smem + warp * (G::kBufs * G::kUnitBytes);
   uint32_t any_flag = 0;
-  constexpr int kBatch = kIters < 4 ? kIters : 4;
-  uint4 v[kBatch];
-  uint32_t m[kBatch][8];
 
+  // rows of the band (from row0 = first row of this lane) that exist, capped
+  auto rows_left = [&](int64_t row0) -> int {
+    const int64_t r = a.M - row0;
+    return r > 16 ? 16 : int(r);
+  };
+  const int64_t a_step = kRpi * a.lda_bytes, m_step = kRpi * a.ldm;
+  const int64_t v_step = kRpi * a.ldv_bytes, i_step = kRpi * a.ldi;
+
+  // stage unit u into ring buffer `buf` (always commits a group, possibly empty)
+  auto issue = [&](int64_t u, int buf) {
+    if (u < units) {
+      const int64_t band = u / a.ksteps, s = u - band * a.ksteps;
+      const int64_t cc = s * kCpr + c;
+      const int64_t row0 = band * 16 + rsub;
+      const int left = rows_left(row0);
+      const uint32_t sb = smem_addr(ring + buf * G::kUnitBytes);
+      if (cc * kElems < a.K) {
+        const uint8_t* ag = a.A + row0 * a.lda_bytes + cc * 16;
+        const uint8_t* mg = MODE == 1 ? a.mask + row0 * a.ldm + cc * kElems : nullptr;
+#pragma unroll
+        for (int k = 0; k < kIters; ++k) {
+          if (kRpi * k < left) {
+            cp_async16(sb + (k * 32 + lane) * 16, ag);
+            if constexpr (MODE == 1) {
+              const uint32_t ms = sb + kIters * 32 * 16 + (k * 32 + lane) * G::kMaskBytes;
+              if constexpr (kElems == 8) {
+                cp_async8(ms, mg);
+              } else {
+#pragma unroll
+                for (int h = 0; h < kElems / 16; ++h) cp_async16(ms + 16 * h, mg + 16 * h);
+              }
+            }
+          }
+          ag += a_step;
+          if constexpr (MODE == 1) mg += m_step;
+        }
+      }
+    }
+    cp_async_commit();
+  };
+
+#pragma unroll
+  for (int b = 0; b < G::kBufs - 1; ++b) issue(warp0 + b * nwarps, b);
+  int buf = 0;
   for (int64_t u = warp0; u < units; u += nwarps) {
+    issue(u + (G::kBufs - 1) * nwarps, buf == 0 ? G::kBufs - 1 : buf - 1);
+    cp_async_wait<G::kBufs - 1>();  // this lane's copies of unit u have landed
     const int64_t band = u / a.ksteps, s = u - band * a.ksteps;
     const int64_t cc = s * kCpr + c;              // chunk of the row
     const bool kin = cc * kElems < a.K;
+    const int64_t row0 = band * 16 + rsub;
+    const int left = rows_left(row0);
+    uint8_t* vg = a.values + row0 * a.ldv_bytes + cc * 8;
+    uint32_t* ig = a.index + row0 * a.ldi + (cc * kElems) / 32;
+    const uint8_t* st = ring + buf * G::kUnitBytes;
     // image rows of this band: block (tile, stage, MMA j) starts at uint4
     // ((tile * ksteps + s) * 4 + j) * 128, the band's rows at + (band % 8) * 16
     uint4* img = meta + ((band >> 3) * a.ksteps + s) * (kMmasPerStage * 128) + (band & 7) * 16;
     uint32_t half16[kIters][kHalves];
 #pragma unroll
     for (int k = 0; k < kIters; ++k) {
-      const int64_t row = band * 16 + kRpi * k + rsub;
-      const bool valid = kin && row < a.M;
-      // loads of kBatch iterations are issued together before any of them is used
-      if (k % kBatch == 0) {
+      const bool valid = kin && kRpi * k < left;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      uint32_t m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (valid) {
+        v = *reinterpret_cast<const uint4*>(st + (k * 32 + lane) * 16);
+        if constexpr (MODE == 1) {
+          const uint8_t* ms = st + kIters * 32 * 16 + (k * 32 + lane) * G::kMaskBytes;
+          if constexpr (kElems == 8) {
+            const uint2 mm = *reinterpret_cast<const uint2*>(ms);
+            m[0] = mm.x;
+            m[1] = mm.y;
+          } else {
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          const int64_t rb = row + kRpi * b;
-          v[b] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) m[b][q] = 0;
-          if (kin && rb < a.M) load_chunk<EB, MODE>(a, rb, cc, v[b], m[b]);
+            for (int h = 0; h < kElems / 16; ++h) {
+              const uint4 mm = *reinterpret_cast<const uint4*>(ms + 16 * h);
+              m[4 * h + 0] = mm.x;
+              m[4 * h + 1] = mm.y;
+              m[4 * h + 2] = mm.z;
+              m[4 * h + 3] = mm.w;
+            }
+          }
         }
       }
       uint2 vals;
       uint32_t nibs, flags;
-      compress_chunk<EB, CLS, MODE>(v[k % kBatch], m[k % kBatch], vals, nibs, flags);
+      compress_chunk<EB, CLS, MODE>(v, m, vals, nibs, flags);
       if (!valid) nibs = kPadNibs;
       if (valid) {
         any_flag |= flags & 1u;
-        __stcs(reinterpret_cast<uint2*>(a.values + row * a.ldv_bytes + cc * 8), vals);
+        __stcs(reinterpret_cast<uint2*>(vg), vals);
       }
+      vg += v_step;
       // the row's canonical word of this chunk, merged across the lanes that share it
       uint32_t word = nibs << ((4 * kGroups) * (lane % kLanesPerWord));
       if constexpr (kLanesPerWord > 1) {
 #pragma unroll
         for (int o = 1; o < kLanesPerWord; o <<= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, o);
       }
-      if (valid && a.index != nullptr && (lane % kLanesPerWord) == 0)
-        a.index[row * a.ldi + (cc * kElems) / 32] = word;
+      if (valid && a.index != nullptr && (lane % kLanesPerWord) == 0) *ig = word;
+      ig += i_step;
       if constexpr (kL8) {
         // MMA j = c / 4 reads canonical words 2j (lanes 4j, 4j+1) and 2j+1 (4j+2, 4j+3)
         const uint32_t next = __shfl_xor_sync(0xFFFFFFFFu, word, 2);
@@ -438,7 +535,9 @@ __global__ void __launch_bounds__(256, 3) compress_meta_kernel(CompressArgs a) {
         }
       }
     }
+    buf = buf == G::kBufs - 1 ? 0 : buf + 1;
   }
+  cp_async_wait<0>();
   if (a.status != nullptr && __any_sync(0xFFFFFFFFu, any_flag != 0u) && lane == 0)
     atomicOr(a.status, kDevNot24);
 }
@@ -524,32 +623,57 @@ cudaError_t launch_compress(const CompressArgs& a, int dtype, int mode, int num_
 }
 
 namespace {
-template <int EB, int CLS, bool kL8>
-cudaError_t launch_compress_meta_cls(const CompressArgs& a, int mode, int grid, cudaStream_t s) {
-  switch (mode) {
-    case 0: compress_meta_kernel<EB, CLS, 0, kL8><<<grid, 256, 0, s>>>(a); break;
-    case 1: compress_meta_kernel<EB, CLS, 1, kL8><<<grid, 256, 0, s>>>(a); break;
-    default: compress_meta_kernel<EB, CLS, 2, kL8><<<grid, 256, 0, s>>>(a); break;
+// Blocks of 4 warps; as many per SM as the shared-memory rings allow (queried once per
+// kernel instance).
+template <int EB, int CLS, int MODE, bool kL8>
+cudaError_t launch_compress_meta_mode(const CompressArgs& a, int num_sms, cudaStream_t s) {
+  using G = FusedGeo<EB, MODE, kL8>;
+  static int per_sm = 0;  // 0: not yet set up
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (per_sm == 0) {
+      auto k = compress_meta_kernel<EB, CLS, MODE, kL8>;
+      if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem) !=
+              cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, G::kWarps * 32, G::kSmem) !=
+              cudaSuccess ||
+          per_sm < 1) {
+        per_sm = 0;
+        return cudaErrorInvalidConfiguration;
+      }
+    }
   }
+  const int64_t units = a.mtiles * 8 * a.ksteps;  // one warp per (band, stage) at a time
+  int64_t want = (units + G::kWarps - 1) / G::kWarps;
+  int64_t cap = int64_t(num_sms) * per_sm;
+  const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+  compress_meta_kernel<EB, CLS, MODE, kL8><<<grid, G::kWarps * 32, G::kSmem, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int EB, int CLS, bool kL8>
+cudaError_t launch_compress_meta_cls(const CompressArgs& a, int mode, int num_sms,
+                                     cudaStream_t s) {
+  switch (mode) {
+    case 0: return launch_compress_meta_mode<EB, CLS, 0, kL8>(a, num_sms, s);
+    case 1: return launch_compress_meta_mode<EB, CLS, 1, kL8>(a, num_sms, s);
+    default: return launch_compress_meta_mode<EB, CLS, 2, kL8>(a, num_sms, s);
+  }
 }
 }  // namespace
 
 cudaError_t launch_compress_meta(const CompressArgs& a, int dtype, int mode, int num_sms,
                                  cudaStream_t s) {
-  const int64_t warps = a.mtiles * 8 * a.ksteps;  // one warp per (band, stage)
-  int64_t want = (warps + 7) / 8;
-  int64_t cap = int64_t(num_sms) * 3;
-  const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
   switch (dtype) {
     case kF16:
-    case kBF16: return launch_compress_meta_cls<16, kFloat16, false>(a, mode, grid, s);
+    case kBF16: return launch_compress_meta_cls<16, kFloat16, false>(a, mode, num_sms, s);
     case kE4M3:
-    case kE5M2: return launch_compress_meta_cls<8, kFloat8, true>(a, mode, grid, s);
-    case kS8: return launch_compress_meta_cls<8, kSigned8, false>(a, mode, grid, s);
-    case kU8: return launch_compress_meta_cls<8, kUnsigned8, false>(a, mode, grid, s);
-    case kS4: return launch_compress_meta_cls<4, kSigned4, false>(a, mode, grid, s);
-    default: return launch_compress_meta_cls<4, kUnsigned4, false>(a, mode, grid, s);
+    case kE5M2: return launch_compress_meta_cls<8, kFloat8, true>(a, mode, num_sms, s);
+    case kS8: return launch_compress_meta_cls<8, kSigned8, false>(a, mode, num_sms, s);
+    case kU8: return launch_compress_meta_cls<8, kUnsigned8, false>(a, mode, num_sms, s);
+    case kS4: return launch_compress_meta_cls<4, kSigned4, false>(a, mode, num_sms, s);
+    default: return launch_compress_meta_cls<4, kUnsigned4, false>(a, mode, num_sms, s);
   }
 }
 
