@@ -119,39 +119,17 @@ __device__ __forceinline__ uint32_t pack8(uint32_t w, uint32_t nib) {
 }
 
 // Magnitude mode: keep the two largest |x| of a group; equal magnitudes keep the lower
-// position.  With the positions ordered by (|x| descending, position ascending), p is
-// kept when fewer than two positions come before it, which is a function of the six
-// comparisons c_ab = (k_b > k_a), a < b.  They form a 6-bit index (bit 0 c01, 1 c02,
-// 2 c13, 3 c03, 4 c12, 5 c23) into kTopLut, the nibble p0 | p1 << 2 for each outcome.
-constexpr uint32_t top2_rule(uint32_t idx) {
-  const uint32_t c01 = idx & 1u, c02 = (idx >> 1) & 1u, c13 = (idx >> 2) & 1u,
-                 c03 = (idx >> 3) & 1u, c12 = (idx >> 4) & 1u, c23 = (idx >> 5) & 1u;
-  const uint32_t before[4] = {c01 + c02 + c03, (1u - c01) + c12 + c13,
-                              (1u - c02) + (1u - c12) + c23, (1u - c03) + (1u - c13) + (1u - c23)};
-  uint32_t keep = 0;
-  for (int p = 0; p < 4; ++p) keep |= (before[p] < 2u ? 1u : 0u) << p;
-  return pick_rule(keep);
-}
-constexpr uint64_t make_top_lut(int part) {
-  uint64_t r = 0;
-  for (uint32_t i = 0; i < 16; ++i) r |= uint64_t(top2_rule(uint32_t(part) * 16u + i)) << (4 * i);
-  return r;
-}
-constexpr uint64_t kTopLut0 = make_top_lut(0), kTopLut1 = make_top_lut(1),
-                   kTopLut2 = make_top_lut(2), kTopLut3 = make_top_lut(3);
-
-__device__ __forceinline__ uint32_t top_lookup(uint32_t lo3, uint32_t hi3) {
-  const uint32_t idx = lo3 | (hi3 << 3);
-  const uint64_t q = (idx & 32u) ? ((idx & 16u) ? kTopLut3 : kTopLut2)
-                                 : ((idx & 16u) ? kTopLut1 : kTopLut0);
-  return uint32_t(q >> (4 * (idx & 15u))) & 0xFu;
-}
-
-// Index into kTopLut from the four keys of a group (plain compares).
+// position.  Each key k_p (a magnitude below 2^16) becomes the composite (k_p << 2) |
+// (3 - p), which orders the positions totally (magnitude first, then lower position), so
+// the kept pair is the two largest composites: a four-input max/min network, and the
+// positions are the composites' low two bits.  Returns the nibble p0 | p1 << 2.
 __device__ __forceinline__ uint32_t top2_keys(uint32_t k0, uint32_t k1, uint32_t k2, uint32_t k3) {
-  const uint32_t lo3 = uint32_t(k1 > k0) | (uint32_t(k2 > k0) << 1) | (uint32_t(k3 > k1) << 2);
-  const uint32_t hi3 = uint32_t(k3 > k0) | (uint32_t(k2 > k1) << 1) | (uint32_t(k3 > k2) << 2);
-  return top_lookup(lo3, hi3);
+  const uint32_t c0 = (k0 << 2) | 3u, c1 = (k1 << 2) | 2u, c2 = (k2 << 2) | 1u, c3 = k3 << 2;
+  const uint32_t a = max(c0, c1), b = min(c0, c1), c = max(c2, c3), d = min(c2, c3);
+  const uint32_t t1 = max(a, c);                  // the largest
+  const uint32_t t2 = max(min(a, c), max(b, d));  // the second largest
+  const uint32_t q1 = ~t1 & 3u, q2 = ~t2 & 3u;    // their positions
+  return min(q1, q2) | (max(q1, q2) << 2);
 }
 
 // 16-bit group in words w0 (elements 0, 1) and w1 (2, 3); keys = bits without the sign.
