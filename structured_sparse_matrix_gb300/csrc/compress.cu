@@ -254,6 +254,7 @@ __device__ __forceinline__ void load_chunk(const CompressArgs& a, int64_t row, i
 // so a thread keeps kUnroll 16-byte loads (plus mask loads) in flight.
 template <int EB, int CLS, int MODE>
 __global__ void __launch_bounds__(256, EB == 4 ? 3 : 4) compress_kernel(CompressArgs a) {
+  griddep_launch_dependents();  // the GEMM after this pass may start its prologue
   constexpr int kElems = 128 / EB;   // elements per 16-byte chunk
   constexpr int kGroups = kElems / 4;  // groups per chunk
   constexpr int kLanesPerWord = 32 / kElems;
@@ -366,6 +367,7 @@ struct FusedGeo {
 // synchronisation (no barrier, no spin).
 template <int EB, int CLS, int MODE, bool kL8>
 __global__ void __launch_bounds__(128) compress_meta_kernel(CompressArgs a) {
+  griddep_launch_dependents();  // the GEMM after this pass may start its prologue
   using G = FusedGeo<EB, MODE, kL8>;
   constexpr int kElems = G::kElems, kCpr = G::kCpr, kRpi = G::kRpi, kIters = G::kIters;
   constexpr int kGroups = kElems / 4;

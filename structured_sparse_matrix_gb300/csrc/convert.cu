@@ -14,6 +14,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "sp24_device.cuh"
 #include "sp24_internal.h"
 
 namespace sp24 {
@@ -37,6 +38,7 @@ template <bool kSigned, int kBits>
 __global__ void __launch_bounds__(256) widen_kernel(const uint8_t* src, int64_t ld_src,
                                                     __nv_bfloat16* dst, int64_t ld_dst,
                                                     int64_t rows, int64_t cols) {
+  griddep_launch_dependents();  // the GEMM after this pass may start its prologue
   constexpr uint32_t kMask = (1u << kBits) - 1;
   const int64_t cpr = (cols + 15) / 16;  // 16-element chunks per row (last may be partial)
   const int64_t total = rows * cpr;

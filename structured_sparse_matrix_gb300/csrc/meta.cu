@@ -27,6 +27,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "sp24_device.cuh"
 #include "sp24_internal.h"
 
 namespace sp24 {
@@ -54,6 +55,7 @@ __device__ __forceinline__ uint4 canon4(const MetaArgs& a, int64_t row, int64_t 
 // lanes of a warp).
 template <bool kEightBit>
 __global__ void __launch_bounds__(256) meta_kernel(MetaArgs a) {
+  griddep_launch_dependents();  // the GEMM after this pass may start its prologue
   const int64_t total = a.mtiles * a.ksteps * 128;
   for (int64_t o = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; o < total;
        o += int64_t(gridDim.x) * blockDim.x) {

@@ -87,6 +87,18 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start while the kernel before it on the stream is still running; griddep_wait()
+// returns once that kernel has completed and its memory writes are visible.  A kernel that
+// calls griddep_launch_dependents() lets the next such kernel start early (its blocks are
+// placed as resources free up; it still waits before touching data).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (TMA, tcgen05.cp, tcgen05.mma read shared memory through it)
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -408,6 +408,9 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &abort_flag;
+  // the prologue above may overlap the previous kernel on the stream (programmatic
+  // dependent launch); nothing below runs before that kernel's writes are visible
+  griddep_wait();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -747,16 +750,19 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
       cudaSuccess)
     return 4;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kPair ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start during the previous kernel's tail; the kernel waits before touching data
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(G::kThreads, 1, 1);
   cfg.dynamicSmemBytes = G::kSmemBytes;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const int tiles = p.mtiles * p.ntiles * p.batch;
   int units = num_sms;
   if (kPair) {
