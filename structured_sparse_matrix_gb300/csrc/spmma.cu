@@ -48,11 +48,12 @@ namespace {
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = 128 * 128;  // one stage of compressed A: 128 rows x 128 bytes
 constexpr int kSlotCols = 16;       // TMEM columns per MMA metadata slot (aligned)
-// Integer mode: 8-bit integers widened to bf16 are exact, every product |a b| <= 255 * 128,
-// so 512 non-zero products (1024 dense K = 8 bf16 stages) sum to less than 2^24 and the
-// f32 accumulator of one such chunk holds an exact integer.  The epilogue adds the chunks
-// in int32 (two's-complement wrap).
-constexpr int kIntChunkStages = 8;
+// Integer mode: integers widened to bf16 are exact, and the f32 accumulator holds an exact
+// integer as long as every partial sum stays within 2^24.  A chunk of MmaParams::chunk
+// stages (128 dense K each, half of them kept products) is sized for that: s8 x s8
+// (|a b| <= 2^14): 2048 dense K, 1024 products; u8 x s8 (|a b| <= 255 * 128): 1024 dense K;
+// 4-bit (|a b| <= 225): 8192 dense K.  The epilogue adds the chunks in int32
+// (two's-complement wrap).
 
 struct MmaParams {
   const void* C;
@@ -61,6 +62,7 @@ struct MmaParams {
   int32_t* status;
   int c32, d32;  // C / D rows allow 32-byte vector accesses (base and pitch 32-byte aligned)
   int ctype;     // float C: 0 = f32, 1 = bf16, 2 = f16
+  int chunk;     // integer mode: stages per exactly-summed f32 chunk
   int d_f16;     // 16-bit float D (OUT == 1): 0 = bf16, 1 = f16
   int batoms;    // B boxes loaded per stage and CTA (the narrow variant skips empty ones)
   int M, N, K;
@@ -482,11 +484,12 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
         for (int kb = 0; kb < p.num_kb; ++kb, ++q) {
           const int s = q % kStages;
           const uint32_t par = (q / kStages) & 1;
-          const int kc = kb % kIntChunkStages;  // stage within an integer chunk
+          const int kc = (OUT == 2) ? kb % p.chunk : 0;  // stage within an integer chunk
           if constexpr (OUT == 2) {
             if (kc == 0) {  // new chunk: next accumulator buffer
-              abuf = chunk & 1;
-              if (!mbar_wait(&acc_empty[abuf], ((chunk >> 1) & 1) ^ 1u, abort, p.limit_ns)) {
+              abuf = G::kAccBufs == 1 ? 0 : (chunk & 1);
+              const int cuse = G::kAccBufs == 1 ? chunk : (chunk >> 1);  // earlier uses
+              if (!mbar_wait(&acc_empty[abuf], (cuse & 1) ^ 1u, abort, p.limit_ns)) {
                 ok = false;
                 break;
               }
@@ -530,7 +533,7 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
           else
             tc_commit(&empty_bar[s]);
           if constexpr (OUT == 2) {
-            if (kc == kIntChunkStages - 1 || kb == p.num_kb - 1) {  // chunk done
+            if (kc == p.chunk - 1 || kb == p.num_kb - 1) {  // chunk done
               if constexpr (kPair)
                 tc_commit_pair_mc(&acc_full[abuf], 3);
               else
@@ -582,11 +585,12 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
         uint32_t sum[kIntCols];
 #pragma unroll
         for (int j = 0; j < kIntCols; ++j) sum[j] = 0u;
-        const int nch = (p.num_kb + kIntChunkStages - 1) / kIntChunkStages;
+        const int nch = (p.num_kb + p.chunk - 1) / p.chunk;
         bool ok = true;
         for (int c = 0; c < nch; ++c, ++ichunk) {
-          const int b = ichunk & 1;
-          if (!mbar_wait(&acc_full[b], (ichunk >> 1) & 1, abort, p.limit_ns)) {
+          const int b = G::kAccBufs == 1 ? 0 : (ichunk & 1);
+          const int cuse = G::kAccBufs == 1 ? ichunk : (ichunk >> 1);
+          if (!mbar_wait(&acc_full[b], cuse & 1, abort, p.limit_ns)) {
             ok = false;
             break;
           }
@@ -598,13 +602,16 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
             uint32_t r[32];
             tc_ld_32x32b_x32(base + uint32_t(q4 * 32), r);
             tc_wait_ld();
+            if (q4 == kIntCols / 32 - 1) {
+              // the whole chunk is in registers: free the accumulator before the last adds
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(b * sizeof(uint64_t)));
+            }
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               sum[q4 * 32 + j] += uint32_t(__float2int_rn(__uint_as_float(r[j])));
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(b * sizeof(uint64_t)));
         }
         if (!ok) break;
         if (row < p.M) {
@@ -862,8 +869,8 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   p.limit_ns = 1000000000ull;  // 1 s per wait
   if (is_int(ta)) {
     // integers: widen both operands to bf16 (exact) and run the bf16 tensor path with
-    // chunked integer accumulation; 256 x 128 tiles on CTA pairs with double-buffered
-    // accumulators
+    // chunked integer accumulation on 256 x 256 tiles (the MMA waits for each chunk's
+    // drain, which is short against a chunk of 8 to 64 stages)
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uint8_t* wa = ws;
     uint8_t* wb = ws + (M * (K / 2) * 2 + 255) / 256 * 256;
@@ -875,9 +882,10 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
                        num_sms, s) != cudaSuccess)
         return 4;
     }
+    p.chunk = (ta == kS8 && tb == kS8) ? 16 : is_i4(ta) ? 64 : 8;
     // kind::f16 with bf16 operands: type code 1 for A and B
-    return run<2, 2, true, false, true>(p, wa, K / 2, meta, wb, ldbw,
-                                        idesc_sparse_f32(1, 1, 256, 128), num_sms, s, bs);
+    return run<2, 2, true>(p, wa, K / 2, meta, wb, ldbw, idesc_sparse_f32(1, 1, 256, 256),
+                           num_sms, s, bs);
   }
   const int esz = dtype_bytes(ta);
   // kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = E4M3, 1 = E5M2
