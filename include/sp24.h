@@ -195,9 +195,11 @@ size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t
  * Accumulation: floats in f32 on the tensor cores; a 16-bit C is widened exactly and a
  * BF16 or F16 D is the f32 result rounded to nearest-even once.  (F16, F16, F16, F16) and
  * (BF16, BF16, BF16, BF16) are the FP16- / BF16-accumulate forms of "RDNA4 sparse WMMA
- * builtins"; summing in f32 and rounding once is at least as accurate as 16-bit sums.  Integers are widened to bf16 (exact) and accumulated in f32 in chunks of
- * 1024 dense K (every chunk sum is an exact integer below 2^24), the chunks then summed in
- * int32: the result is exact.  (A u8 x u8 chunk sum could pass 2^24, hence B = S8.)
+ * builtins"; summing in f32 and rounding once is at least as accurate as 16-bit sums.
+ * Integers are widened to bf16 (exact) and accumulated in f32 in chunks whose sums are
+ * exact integers of at most 2^24 (2048 dense K for S8 x S8, 1024 for U8 x S8, 8192 for
+ * 4-bit operands), the chunks then summed in int32: the result is exact.  (A u8 x u8
+ * chunk of even 1024 K could pass 2^24, hence B = S8 for 8-bit operands.)
  * Alignment: values, meta, B, C, D 16-byte aligned, every row pitch a multiple of 16 bytes.
  * Device status: SP24_DEV_TIMEOUT if a pipeline wait gave up (D is then invalid).
  */
