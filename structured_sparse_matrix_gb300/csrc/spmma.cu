@@ -12,8 +12,9 @@
 //           CTA issues the MMAs, so each loaded byte feeds twice the work.  The 256-column
 //           accumulator is single-buffered; eight epilogue warps drain it to registers
 //           first and release it before they add C and store.
-//   pair 256 x 128 (16-bit operands with 32 < N <= 128, and every integer product): the
-//           same with 64-column halves of B and double-buffered 128-column accumulators.
+//           Integer products (widened to bf16) use it too, summing f32 chunks into int32.
+//   pair 256 x 128 (16-bit operands with 32 < N <= 128): the same with 64-column halves
+//           of B and double-buffered 128-column accumulators.
 //   single  (FP8 with 32 < N <= 128): one CTA per 128 x 128 tile, cta_group::1,
 //           accumulator double-buffered in TMEM so the epilogue of one tile overlaps the
 //           next.
@@ -72,10 +73,9 @@ struct MmaParams {
   uint64_t limit_ns;
 };
 
-// Variants: pair (256 x 256 tiles on a CTA pair), pair with 256 x 128 tiles and
-// double-buffered accumulators (the integer path, whose chunked accumulation switches
-// buffers every 8 stages, and 16-bit operands with 32 < N <= 128), single (128 x 128
-// tiles: FP8 with 32 < N <= 128) and narrow (128 x 32 tiles for
+// Variants: pair (256 x 256 tiles on a CTA pair; also the integer path), pair with
+// 256 x 128 tiles and double-buffered accumulators (16-bit operands with 32 < N <= 128),
+// single (128 x 128 tiles: FP8 with 32 < N <= 128) and narrow (128 x 32 tiles for
 // N <= 32: B staged in 32-byte swizzle atoms, so a stage holds only the columns that
 // exist and seven stages fit in shared memory).
 template <int ESZ, bool kPair, bool kNarrow = false, bool kHalfN = false>
@@ -577,8 +577,8 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
       const int row = mt * G::kTileM + int(rank) * 128 + quad * 32 + lane;
       const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16) + uint32_t(abuf * G::kTileN);
       if constexpr (OUT == 2) {
-        // integer mode: one f32 chunk per 1024 dense K, summed exactly in int32; each
-        // thread owns one row x kIntCols columns (single: 128, pair 256 x 128: 64)
+        // integer mode: one f32 chunk per p.chunk stages, summed exactly in int32; each
+        // thread owns one row x kIntCols columns (pair 256 x 256: 128)
         (void)abuf;
         constexpr int kIntCols = G::kTileN * 4 / G::kEpiWarps;
         const int cbase = (ew >> 2) * kIntCols;  // this warp's first column in the tile
