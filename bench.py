@@ -388,7 +388,9 @@ def gpu_arm(args, world, rank, local):
     peak = dense_peak * SPARSE_OVER_DENSE
     esz = torch.empty((), dtype=tdt).element_size()
     osz = torch.empty((), dtype=out_dtype).element_size()
-    mma_bytes = (M * K // 2 * esz + sp.meta_bytes(tdt, M, K) + K * N * esz +
+    # algorithmic bytes: compressed A, the sparsity metadata at its information size (the
+    # canonical index, M*K/8 bytes; the kernel's image is 4x that), B, C (if any), D, once
+    mma_bytes = (M * K // 2 * esz + M * K // 8 + K * N * esz +
                  (M * N * 4 if base["C"] is not None else 0) + M * N * osz)
     unit = "TOP/s" if integer else "TFLOP/s"
     achieved_tf = flops / (k_mma * 1e-3) / 1e12
@@ -420,7 +422,7 @@ def gpu_arm(args, world, rank, local):
     }
     if fused:
         # + the image written (the separate pass would read the index and write the image)
-        fbytes = cbytes + sp.meta_bytes(tdt, M, K)
+        fbytes = cbytes + M * K // 8  # + the metadata image at its information size
         kernels["sp24_compress_meta_us"] = k_compress * 1e3
         kernels["sp24_compress_meta_gbs"] = fbytes / (k_compress * 1e-3) / 1e9
     else:
