@@ -314,8 +314,9 @@ def gpu_arm(args, world, rank, local):
     launches_per_step = (1 if fused else 2) + (3 if integer else 1)
 
     def launch(s, ev=None):
-        # the C-ABI calls of one step, on the current stream
-        st = sp._stream(stream)
+        # the C-ABI calls of one step, on the current stream (a graph's capture stream
+        # while one is being recorded)
+        st = sp._stream(torch.cuda.current_stream(dev))
         m = s["mask"]
         if ev is not None:
             ev[0].record(stream)
@@ -351,6 +352,28 @@ def gpu_arm(args, world, rank, local):
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} during warm-up")
 
+    # the K steps recorded once as a CUDA graph (launch overhead off the timed path; the
+    # GEMM's programmatic dependency on the pass before it becomes a graph edge); eager
+    # launches if capture is refused
+    graph = None
+    if not args.eager:
+        try:
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.graph(g, stream=cap):
+                for i in range(args.steps):
+                    launch(sets[i % len(sets)])
+            stream.wait_stream(cap)
+            g.replay()  # untimed: uploads the graph
+            torch.cuda.synchronize(dev)
+            graph = g
+        except Exception as exc:  # noqa: BLE001 - any capture failure means eager timing
+            log(f"graph capture failed, timing eager launches: {exc}")
+            torch.cuda.synchronize(dev)
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} during warm-up")
+
     # timed region: K steps back to back, no events between the kernels (the GEMM may
     # start during the previous kernel's tail)
     barrier(world)
@@ -359,8 +382,11 @@ def gpu_arm(args, world, rank, local):
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        for i in range(args.steps):
-            launch(sets[i % len(sets)])
+        if graph is not None:
+            graph.replay()
+        else:
+            for i in range(args.steps):
+                launch(sets[i % len(sets)])
         t_end.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
@@ -486,7 +512,9 @@ def gpu_arm(args, world, rank, local):
                                 f"sp24_compress({mode}) + sp24_meta_prepare + sp24_mma"),
                        "l2": f"{len(sets)} rotating input sets, "
                              f"{len(sets) * set_bytes(sets[0]) / 2**20:.0f} MiB > L2",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}",
+                       "launch": ("one CUDA graph of the K steps" if graph is not None
+                                  else "eager launches")},
             "roofline": roof,
             "kernels": kernels,
             "cpu_baseline": cpu,
@@ -506,6 +534,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the timed steps one by one instead of as a CUDA graph")
     ap.add_argument("--pass", dest="pass_mode", default="fused", choices=["fused", "separate"],
                     help="compression and metadata image in one kernel (fused) or two")
     args = ap.parse_args()

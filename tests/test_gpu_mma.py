@@ -289,3 +289,43 @@ def test_product_on_fused_image(ta, tc, out, M, N, K):
 def test_config2_through_the_fused_pass():
     c = inputs.config2()
     run_case(c, mode="mask", rows=sample_rows(c["M"]), fused=True)
+
+
+# ---- CUDA graphs: the calls are stream-ordered and allocation-free, so they capture --------
+
+def test_graph_capture_replays_the_eager_result():
+    M, N, K = 1000, 200, 1024
+    c = inputs.case("bf16", "bf16", M, N, K, seed=12, tc="f32")
+    A, mask, B, C = c["A"].cuda(), c["mask"].cuda().to(torch.uint8), c["B"].cuda(), c["C"].cuda()
+    values = torch.empty((M, K // 2), dtype=torch.bfloat16, device="cuda")
+    index = torch.empty((M, K // 32), dtype=torch.int32, device="cuda")
+    meta = torch.empty(sp.meta_bytes(torch.bfloat16, M, K), dtype=torch.uint8, device="cuda")
+    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    L = sp.lib()
+
+    def step():
+        st = sp._stream(torch.cuda.current_stream())
+        assert L.sp24_compress_meta(1, M, K, sp._ptr(A), K, sp._ptr(mask), K, 1, sp._ptr(values),
+                                    K // 2, sp._ptr(index), K // 32, sp._ptr(meta), None, st) == 0
+        assert L.sp24_mma(1, 1, 6, 6, M, N, K, sp._ptr(values), K // 2, sp._ptr(meta),
+                          sp._ptr(B), N, sp._ptr(C), N, sp._ptr(D), N, None, 0, None, st) == 0
+
+    step()  # eager (also sets up the kernels' attributes before capture)
+    torch.cuda.synchronize()
+    eager = D.clone()
+    D.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    D.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(D, eager)
+    rows = sample_rows(M)
+    v_ref, i_ref, _ = oracle.compress(inputs.bits(c["A"]), "bf16", "mask", mask=c["mask"].numpy())
+    Dref, S = oracle.mma_f64(v_ref, i_ref, inputs.bits(c["B"]), c["C"].numpy(), "bf16", "bf16", K,
+                             rows=rows)
+    check_float(D.cpu().numpy()[rows], Dref, S, False, "graph replay")
