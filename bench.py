@@ -42,23 +42,23 @@ SPARSE_OVER_DENSE = 2.0
 
 CONFIGS = {
     # name: (generator, ta, mode, out dtype, description)
-    "c2": (lambda: inputs.config2(), "bf16", "mask", torch.float32,
+    "bf16-4096": (lambda: inputs.bf16_square(), "bf16", "mask", torch.float32,
            "bf16 M=N=K=4096, random 2:4 mask, C f32, D f32"),
-    "c1": (lambda: inputs.config1(), "f16", "mask", torch.float32,
+    "fixed-f16-64x128": (lambda: inputs.fixed_pattern_case(), "f16", "mask", torch.float32,
            "f16 64x64x128, fixed positions-0-and-2 pattern, integers in [-4,4], C f32"),
-    "c3-e4m3": (lambda: inputs.config3("e4m3"), "e4m3", "mask", torch.float32,
+    "e4m3-8192": (lambda: inputs.fp8_square("e4m3"), "e4m3", "mask", torch.float32,
                 "fp8 E4M3 M=N=K=8192, random 2:4 mask, no C, D f32"),
-    "c3-e5m2": (lambda: inputs.config3("e5m2"), "e5m2", "mask", torch.float32,
+    "e5m2-8192": (lambda: inputs.fp8_square("e5m2"), "e5m2", "mask", torch.float32,
                 "fp8 E5M2 M=N=K=8192, random 2:4 mask, no C, D f32"),
-    "c4-s8": (lambda: inputs.config4("s8"), "s8", "mask", torch.int32,
+    "s8-8192": (lambda: inputs.int8_square("s8"), "s8", "mask", torch.int32,
               "int8 s8 x s8 M=N=K=8192, random 2:4 mask, C s32, D s32 (exact)"),
-    "c4-u8": (lambda: inputs.config4("u8"), "u8", "mask", torch.int32,
+    "u8s8-8192": (lambda: inputs.int8_square("u8"), "u8", "mask", torch.int32,
               "int8 u8 x s8 M=N=K=8192, random 2:4 mask, C s32, D s32 (exact)"),
-    "c5-16": (lambda: inputs.config5(16), "bf16", "magnitude", torch.bfloat16,
+    "llm-n16": (lambda: inputs.llm_layer(16), "bf16", "magnitude", torch.bfloat16,
               "LLM layer W 14336x4096 bf16 magnitude-pruned, X 4096x16, D bf16"),
-    "c5-128": (lambda: inputs.config5(128), "bf16", "magnitude", torch.bfloat16,
+    "llm-n128": (lambda: inputs.llm_layer(128), "bf16", "magnitude", torch.bfloat16,
                "LLM layer W 14336x4096 bf16 magnitude-pruned, X 4096x128, D bf16"),
-    "c5-2048": (lambda: inputs.config5(2048), "bf16", "magnitude", torch.bfloat16,
+    "llm-n2048": (lambda: inputs.llm_layer(2048), "bf16", "magnitude", torch.bfloat16,
                 "LLM layer W 14336x4096 bf16 magnitude-pruned, X 4096x2048, D bf16"),
 }
 
@@ -553,7 +553,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="c2", choices=sorted(CONFIGS))
+    ap.add_argument("--config", default="bf16-4096", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

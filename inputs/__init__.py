@@ -6,18 +6,19 @@ imported by both the tests / bench (to feed the CUDA library) and the oracle che
 the two sides see bit-identical inputs.
 
 Workloads (all synthetic; the pages measure nothing on a public suite):
-  c1  f16 64x128 A with the fixed pattern that keeps positions 0 and 2 of each group,
-      B 128x64 f16, C 64x64 f32, integers uniform in [-4, 4], one generator seeded 0
-      drawing A, B, C in that order;
-  c2  bf16 M=N=K=4096, mask uniform over the six two-of-four patterns, A, B ~ N(0,1),
-      C f32 ~ N(0,1);
-  c3  8192^3 FP8 (E4M3 x E4M3, E5M2 x E5M2), N(0,1) scaled per tensor to the format's
-      maximum and rounded to nearest-even with saturation, random mask, no C;
-  c4  8192^3 int8 (s8 x s8, u8 x s8), uniform over the full 8-bit range, random mask,
-      C s32 uniform in [-2^20, 2^20];
-  c5  LLM layer: W bf16 14336x4096 ~ N(0, 0.02) (pruned by magnitude on the device),
+  fixed_pattern_case  f16 64x128 A with the fixed pattern that keeps positions 0 and 2 of
+      each group, B 128x64 f16, C 64x64 f32, integers uniform in [-4, 4], one generator
+      seeded 0 drawing A, B, C in that order (the pages' example kernel);
+  bf16_square  bf16 M=N=K=4096, mask uniform over the six two-of-four patterns,
+      A, B ~ N(0,1), C f32 ~ N(0,1);
+  fp8_square  8192^3 FP8 (E4M3 x E4M3, E5M2 x E5M2), N(0,1) scaled per tensor to the
+      format's maximum and rounded to nearest-even with saturation, random mask, no C;
+  int8_square  8192^3 int8 (s8 x s8, u8 x s8), uniform over the full 8-bit range, random
+      mask, C s32 uniform in [-2^20, 2^20];
+  llm_layer  W bf16 14336x4096 ~ N(0, 0.02) (pruned by magnitude on the device),
       X bf16 4096xN ~ N(0,1), N in {16, 128, 2048}.
-Seeds for c2-c5: A=0, B=1, C=2, mask=3 (plus the size in the generic helper).
+Seeds of the square cases and the layer: A=0, B=1, C=2, mask=3 (plus the size in the
+generic helper).
 """
 from __future__ import annotations
 
@@ -142,8 +143,8 @@ def case(ta: str, tb: str, M: int, N: int, K: int, *, seed: int = 0, tc: str | N
             "M": M, "N": N, "K": K}
 
 
-def config1() -> dict:
-    """c1: one generator seeded 0 draws A (64x128), B (128x64), C (64x64) in order;
+def fixed_pattern_case() -> dict:
+    """The pages' example: one generator seeded 0 draws A (64x128), B (128x64), C (64x64) in order;
     integers in [-4, 4]; fixed positions-0-and-2 pattern."""
     g = gen(0)
     M, N, K = 64, 64, 128
@@ -155,8 +156,8 @@ def config1() -> dict:
             "tc": "f32", "M": M, "N": N, "K": K}
 
 
-def config2(M: int = 4096, N: int = 4096, K: int = 4096) -> dict:
-    """c2: bf16, random two-of-four mask, A, B ~ N(0,1), C f32 ~ N(0,1)."""
+def bf16_square(M: int = 4096, N: int = 4096, K: int = 4096) -> dict:
+    """bf16, random two-of-four mask, A, B ~ N(0,1), C f32 ~ N(0,1)."""
     m = keep_mask(M, K, gen(3))
     A = apply_mask(values((M, K), "bf16", "normal", gen(0)), m)
     B = values((K, N), "bf16", "normal", gen(1))
@@ -165,8 +166,8 @@ def config2(M: int = 4096, N: int = 4096, K: int = 4096) -> dict:
             "M": M, "N": N, "K": K}
 
 
-def config3(fmt: str = "e4m3", M: int = 8192, N: int = 8192, K: int = 8192) -> dict:
-    """c3: FP8 (same format for A and B), per-tensor scaled N(0,1), random mask, no C."""
+def fp8_square(fmt: str = "e4m3", M: int = 8192, N: int = 8192, K: int = 8192) -> dict:
+    """FP8 (same format for A and B), per-tensor scaled N(0,1), random mask, no C."""
     m = keep_mask(M, K, gen(3))
     A = apply_mask(values((M, K), fmt, "normal", gen(0)), m)
     B = values((K, N), fmt, "normal", gen(1))
@@ -174,8 +175,8 @@ def config3(fmt: str = "e4m3", M: int = 8192, N: int = 8192, K: int = 8192) -> d
             "M": M, "N": N, "K": K}
 
 
-def config4(ta: str = "s8", M: int = 8192, N: int = 8192, K: int = 8192) -> dict:
-    """c4: int8, full 8-bit range (A s8 or u8, B s8), random mask, C s32 in +-2^20."""
+def int8_square(ta: str = "s8", M: int = 8192, N: int = 8192, K: int = 8192) -> dict:
+    """int8, full 8-bit range (A s8 or u8, B s8), random mask, C s32 in +-2^20."""
     m = keep_mask(M, K, gen(3))
     A = apply_mask(values((M, K), ta, "full", gen(0)), m)
     B = values((K, N), "s8", "full", gen(1))
@@ -184,8 +185,8 @@ def config4(ta: str = "s8", M: int = 8192, N: int = 8192, K: int = 8192) -> dict
             "M": M, "N": N, "K": K}
 
 
-def config5(N: int = 2048, M: int = 14336, K: int = 4096) -> dict:
-    """c5: dense bf16 weight W ~ N(0, 0.02) (no mask: pruned by magnitude on the device)
+def llm_layer(N: int = 2048, M: int = 14336, K: int = 4096) -> dict:
+    """LLM layer: dense bf16 weight W ~ N(0, 0.02) (no mask: pruned by magnitude on the device)
     and activations X ~ N(0,1)."""
     W = values((M, K), "bf16", "normal", gen(0), std=0.02)
     X = values((K, N), "bf16", "normal", gen(1))

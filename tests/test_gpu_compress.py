@@ -67,8 +67,8 @@ def test_exact_mode_fill_rules_f16():
     assert status.item() & sp.DEV_NOT_2_4
 
 
-def test_compress_config1_index_literal():
-    c = inputs.config1()
+def test_compress_fixed_pattern_index_literal():
+    c = inputs.fixed_pattern_case()
     values, index, status = gpu_compress(c, "mask")
     torch.cuda.synchronize()
     assert status.item() == 0
@@ -102,8 +102,8 @@ def test_decompress_round_trip(ta):
     assert np.array_equal(ref, inputs.bits(c["A"]))
 
 
-def test_compress_full_size_config2_mask_mode():
-    c = inputs.config2()
+def test_compress_full_size_bf16_4096_mask_mode():
+    c = inputs.bf16_square()
     values, index, status = gpu_compress(c, "mask")
     torch.cuda.synchronize()
     assert status.item() == 0
@@ -112,8 +112,8 @@ def test_compress_full_size_config2_mask_mode():
     assert np.array_equal(inputs.bits(values.cpu()), v_ref)
 
 
-def test_prune_full_size_config5_magnitude():
-    c = inputs.config5(N=16)
+def test_prune_full_size_llm_weight():
+    c = inputs.llm_layer(N=16)
     values, index, status = gpu_compress(c, "magnitude")
     torch.cuda.synchronize()
     v_ref, i_ref, _ = oracle.compress(inputs.bits(c["A"]), "bf16", "magnitude")
@@ -224,9 +224,9 @@ def test_compress_meta_without_index_and_padded_pitch():
     assert torch.equal(values, v2) and torch.equal(meta, m2)
 
 
-def test_compress_meta_full_size_config5_magnitude():
+def test_compress_meta_full_size_llm_weight():
     # the LLM layer's weight (14336 x 4096): image equal to the separate re-layout's
-    c = inputs.config5(N=16)
+    c = inputs.llm_layer(N=16)
     A = c["A"].cuda()
     values, index, meta = sp.compress_meta(A, mode="magnitude")
     v2, i2 = sp.compress(A, mode="magnitude")

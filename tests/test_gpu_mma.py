@@ -15,9 +15,9 @@ pytestmark = pytest.mark.gpu
 FLOAT_TYPES = ["f16", "bf16", "e4m3", "e5m2"]
 
 
-def test_config1_bit_exact():
+def test_fixed_pattern_bit_exact():
     # integer-valued f16 inputs: every partial sum is a small integer, so D is exact
-    c = inputs.config1()
+    c = inputs.fixed_pattern_case()
     Dg, Dref, _ = run_case(c, mode="mask", check=False)
     assert np.array_equal(Dg.astype(np.float64), Dref)
 
@@ -175,20 +175,20 @@ def test_bounded_wait_gives_up_and_context_survives():
 
 # ---- full-size workloads, compared on sampled rows --------------------------------------
 
-def test_config2_full_size_bf16():
-    c = inputs.config2()
+def test_full_size_bf16_4096():
+    c = inputs.bf16_square()
     run_case(c, mode="mask", rows=sample_rows(c["M"]))
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-def test_config3_full_size_fp8(fmt):
-    c = inputs.config3(fmt)
+def test_full_size_fp8_8192(fmt):
+    c = inputs.fp8_square(fmt)
     run_case(c, mode="mask", rows=sample_rows(c["M"])[::4])
 
 
 @pytest.mark.parametrize("N", [16, 128, 2048])
-def test_config5_llm_layer(N):
-    c = inputs.config5(N=N)
+def test_llm_layer(N):
+    c = inputs.llm_layer(N=N)
     run_case(c, mode="magnitude", out_dtype=torch.bfloat16, rows=sample_rows(c["M"]))
 
 
@@ -232,8 +232,8 @@ def test_int8_wraps_like_int32():
 
 
 @pytest.mark.parametrize("ta", ["s8", "u8"])
-def test_config4_full_size_int8(ta):
-    c = inputs.config4(ta)
+def test_full_size_int8_8192(ta):
+    c = inputs.int8_square(ta)
     run_case(c, mode="mask", out_dtype=torch.int32, rows=sample_rows(c["M"])[::4])
 
 
@@ -286,8 +286,8 @@ def test_product_on_fused_image(ta, tc, out, M, N, K):
     run_case(c, mode="mask", out_dtype=out, fused=True)
 
 
-def test_config2_through_the_fused_pass():
-    c = inputs.config2()
+def test_bf16_4096_through_the_fused_pass():
+    c = inputs.bf16_square()
     run_case(c, mode="mask", rows=sample_rows(c["M"]), fused=True)
 
 

@@ -47,7 +47,7 @@ def test_reference_arm_under_torchrun_prints_once():
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
-           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "c1",
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "fixed-f16-64x128",
            "--gpus", "2", "--steps", "1", "--warmup", "1"]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]

@@ -186,8 +186,8 @@ def test_fixed_pattern_index_literal_0x88():
     assert np.array_equal(values[:, 1::2], A[:, p1::4])
 
 
-def test_config1_index_is_all_0x88888888():
-    c = inputs.config1()
+def test_fixed_pattern_index_is_all_0x88888888():
+    c = inputs.fixed_pattern_case()
     _, index, flags = oracle.compress(inputs.bits(c["A"]), "f16", "mask",
                                       mask=c["mask"].numpy())
     assert not flags.any()
