@@ -224,7 +224,9 @@ def reference_arm(args, world, rank):
         return
     gen, ta, mode, out_dtype, desc = CONFIGS[args.config]
     c = gen()
-    budget = float(os.environ.get("SP24_REF_STEP_SECONDS", "8"))
+    # per-step sample sized so that warm-up + timed steps take about 2.5 minutes in all
+    total = float(os.environ.get("SP24_REF_TOTAL_SECONDS", "150"))
+    budget = min(8.0, max(0.2, total / max(args.steps + args.warmup, 1)))
     # size the per-step sample once, then time warmup + steps on that sample
     _, rows, _, threads = oracle_sample(c, mode, budget)
     import oracle
