@@ -329,3 +329,27 @@ def test_graph_capture_replays_the_eager_result():
     Dref, S = oracle.mma_f64(v_ref, i_ref, inputs.bits(c["B"]), c["C"].numpy(), "bf16", "bf16", K,
                              rows=rows)
     check_float(D.cpu().numpy()[rows], Dref, S, False, "graph replay")
+
+
+# ---- large extents: many row tiles, very long K ------------------------------------------
+
+@pytest.mark.parametrize("ta,M,N,K", [("bf16", 200_000, 16, 64),      # 1563 narrow tiles
+                                      ("bf16", 128, 128, 131_072),    # 1024 K stages
+                                      ("e4m3", 300, 48, 65_536)])     # 256 FP8 stages
+def test_large_extents(ta, M, N, K):
+    c = inputs.case(ta, ta, M, N, K, seed=M % 97, tc="f32",
+                    dist="int4" if ta == "e4m3" else "normal")
+    run_case(c, mode="mask", rows=sample_rows(M)[::7], fused=True)
+
+
+def test_int8_long_k_exact():
+    # K = 65536: 32 chunks of the s8 x s8 integer accumulation, every product at its extreme
+    M, N, K = 256, 64, 65_536
+    m = inputs.keep_mask(M, K, inputs.gen(3))
+    A = torch.where(m, torch.full((M, K), -128), torch.zeros((M, K), dtype=torch.long)).to(torch.int8)
+    B = torch.full((K, N), -128, dtype=torch.int8)
+    C = torch.zeros((M, N), dtype=torch.int32)
+    c = {"A": A, "mask": m, "B": B, "C": C, "ta": "s8", "tb": "s8", "tc": "s32",
+         "M": M, "N": N, "K": K}
+    Dg, Dref, _ = run_case(c, mode="mask", out_dtype=torch.int32, rows=np.arange(0, M, 17))
+    assert np.all(Dref == (K // 2) * 16384)   # 2^29: far beyond 2^24, exact
