@@ -244,6 +244,30 @@ sp24_status sp24_mma_strided_batched(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc
                                      int64_t stride_c, void *D, int64_t ldd, int64_t stride_d,
                                      int32_t *d_status, void *stream);
 
+/* One problem of a grouped product (all fields as the sp24_mma arguments of that name). */
+typedef struct sp24_mma_problem {
+    int64_t M, N, K;
+    const void *values; int64_t ldv;
+    const void *meta;
+    const void *B; int64_t ldb;
+    const void *C; int64_t ldc;   /* C may be NULL */
+    void *D; int64_t ldd;
+} sp24_mma_problem;
+
+/*
+ * sp24_mma_grouped -- D_g = expand(values_g, meta_g) * B_g + C_g for `count` problems of
+ * different shapes (e.g. the experts of a mixture-of-experts layer with their own token
+ * counts), one persistent launch per 32 problems whose tiles share the GPU.  Float
+ * operands only, one (ta, tb, tc, td) combination for all problems (the pairs and C / D
+ * types sp24_mma takes for 16-bit and FP8 operands); every problem is validated as
+ * sp24_mma validates its arguments, and nothing is enqueued if any problem fails.
+ * Problems with M == 0 or N == 0 are skipped.  The tile shape follows the widest N of
+ * each launch's problems.  problems: host array, read during the call only.
+ */
+sp24_status sp24_mma_grouped(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
+                             const sp24_mma_problem *problems, int64_t count,
+                             int32_t *d_status, void *stream);
+
 /*
  * sp24_mma_i8_noalloc -- the 8-bit integer form of sp24_mma without a workspace argument.
  * The source pages have no counterpart; this entry point exists for callers that cannot

@@ -25,7 +25,8 @@ import torch
 
 from . import _build
 
-__all__ = ["lib", "compress", "compress_meta", "decompress", "meta_bytes", "meta_prepare", "mma", "mma_batched",
+__all__ = ["lib", "compress", "compress_meta", "decompress", "meta_bytes", "meta_prepare", "mma",
+           "mma_batched", "mma_grouped",
            "workspace_bytes",
            "SparseMatrix", "Sp24Error", "DEV_NOT_2_4", "DEV_TIMEOUT", "DTYPE_CODES"]
 
@@ -43,8 +44,19 @@ DEV_TIMEOUT = 2
 
 # every symbol include/sp24.h declares
 EXPORTS = ("sp24_compress", "sp24_compress_meta", "sp24_decompress", "sp24_meta_bytes", "sp24_meta_prepare",
-           "sp24_mma_workspace_bytes", "sp24_mma", "sp24_mma_strided_batched", "sp24_mma_i8_noalloc",
+           "sp24_mma_workspace_bytes", "sp24_mma", "sp24_mma_strided_batched", "sp24_mma_grouped",
+           "sp24_mma_i8_noalloc",
            "sp24_diag_wait_timeout", "sp24_status_string", "sp24_version")
+
+class Problem(ctypes.Structure):
+    """One problem of sp24_mma_grouped (the C struct sp24_mma_problem)."""
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("values", ctypes.c_void_p), ("ldv", ctypes.c_int64),
+                ("meta", ctypes.c_void_p),
+                ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64),
+                ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+                ("D", ctypes.c_void_p), ("ldd", ctypes.c_int64)]
+
 
 _lock = threading.Lock()
 _lib = None
@@ -88,6 +100,8 @@ def lib():
             L.sp24_mma_strided_batched.argtypes = [i32, i32, i32, i32, i64, i64, i64, i64, p, i64,
                                                    i64, p, i64, p, i64, i64, p, i64, i64, p,
                                                    i64, i64, p, p]
+            L.sp24_mma_grouped.restype = i32
+            L.sp24_mma_grouped.argtypes = [i32, i32, i32, i32, ctypes.POINTER(Problem), i64, p, p]
             L.sp24_mma_i8_noalloc.restype = i32
             L.sp24_mma_i8_noalloc.argtypes = [i32, i32, i32, i32, i64, i64, i64, p, i64, p, p,
                                               i64, p, i64, p, i64, p, p]
@@ -282,6 +296,34 @@ def mma_batched(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor,
         C.stride(1) if C is not None else N, C.stride(0) if C is not None else 0,
         _ptr(out), out.stride(1), out.stride(0), _ptr(status), _stream(stream)))
     return out
+
+
+def mma_grouped(items, out_dtype=torch.float32, status: torch.Tensor | None = None,
+                stream=None) -> list:
+    """D_g = expand(values_g, meta_g) @ B_g + C_g for problems of different shapes in one
+    launch (per 32 problems).  items: sequence of (values, meta, B, C or None); float
+    operands of one type.  Returns the list of D_g (M_g x N_g, out_dtype)."""
+    items = list(items)
+    if not items:
+        return []
+    outs, keep = [], []
+    arr = (Problem * len(items))()
+    ta = tb = tc = None
+    for i, (values, meta, B, C) in enumerate(items):
+        M, (K, N) = values.shape[0], B.shape
+        D = torch.empty((M, N), dtype=out_dtype, device=B.device)
+        outs.append(D)
+        keep.extend([values, meta, B, C, D])
+        ta, tb = _code(values.dtype), _code(B.dtype)
+        if C is not None:
+            tc = _code(C.dtype)
+        arr[i] = Problem(M, N, K, values.data_ptr(), _ld(values), meta.data_ptr(), B.data_ptr(),
+                         _ld(B), 0 if C is None else C.data_ptr(), N if C is None else _ld(C),
+                         D.data_ptr(), _ld(D))
+    _check("sp24_mma_grouped", lib().sp24_mma_grouped(
+        ta, tb, tc if tc is not None else _code(torch.float32), _code(out_dtype), arr, len(items),
+        _ptr(status), _stream(stream)))
+    return outs
 
 
 def mma_i8_noalloc(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor,

@@ -308,6 +308,53 @@ sp24_status sp24_mma_strided_batched(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc
   return static_cast<sp24_status>(rc);
 }
 
+sp24_status sp24_mma_grouped(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
+                             const sp24_mma_problem* problems, int64_t count, int32_t* d_status,
+                             void* stream) {
+  const bool f16ish = (ta == SP24_F16 || ta == SP24_BF16);
+  if (!(f16ish || is_f8(ta))) return SP24_ERR_UNSUPPORTED;  // float operands only
+  if (f16ish ? tb != ta : !is_f8(tb)) return SP24_ERR_UNSUPPORTED;
+  if (!is_float_acc(tc) || !is_float_acc(td)) return SP24_ERR_UNSUPPORTED;
+  if (count < 0 || (count > 0 && !problems)) return SP24_ERR_INVALID_ARG;
+  const int esz = dtype_bytes(ta);
+  const int dsz = dtype_bytes(td);
+  const int csz = dtype_bytes(tc);
+  int64_t live = 0;
+  for (int64_t g = 0; g < count; ++g) {
+    const sp24_mma_problem& q = problems[g];
+    if (q.M < 0 || q.N < 0 || q.K < 0 || (q.K % 32) != 0) return SP24_ERR_INVALID_ARG;
+    if (q.M > INT32_MAX / 2 || q.N > INT32_MAX / 2 || q.K > INT32_MAX / 2)
+      return SP24_ERR_INVALID_ARG;
+    if (q.M == 0 || q.N == 0) continue;
+    if (!q.D || (q.K > 0 && (!q.values || !q.meta || !q.B))) return SP24_ERR_INVALID_ARG;
+    if (q.ldd < q.N || (q.C && q.ldc < q.N) || (q.K > 0 && (q.ldv < q.K / 2 || q.ldb < q.N)))
+      return SP24_ERR_INVALID_ARG;
+    if ((q.M + 255) / 256 * ((q.N + 31) / 32) > INT32_MAX / 64) return SP24_ERR_INVALID_ARG;
+    if (!aligned16(q.D) || (q.ldd * dsz) % 16) return SP24_ERR_ALIGN;
+    if (q.C && (!aligned16(q.C) || (q.ldc * csz) % 16)) return SP24_ERR_ALIGN;
+    if (q.K > 0 && (!aligned16(q.values) || !aligned16(q.meta) || !aligned16(q.B) ||
+                    (q.ldv * esz) % 16 || (q.ldb * esz) % 16))
+      return SP24_ERR_ALIGN;
+    ++live;
+  }
+  if (live == 0) return SP24_OK;
+  int sms = 0;
+  if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
+  // launches of up to kMaxGroupPerLaunch non-empty problems, in order
+  sp24_mma_problem batch[kMaxGroupPerLaunch];
+  int n = 0;
+  for (int64_t g = 0; g <= count; ++g) {
+    if (g < count && problems[g].M > 0 && problems[g].N > 0) batch[n++] = problems[g];
+    if (n == kMaxGroupPerLaunch || (g == count && n > 0)) {
+      const int rc = launch_spmma_grouped(ta, tb, tc, td, batch, n, d_status, sms,
+                                          static_cast<cudaStream_t>(stream));
+      if (rc != 0) return static_cast<sp24_status>(rc);
+      n = 0;
+    }
+  }
+  return SP24_OK;
+}
+
 sp24_status sp24_diag_wait_timeout(int32_t* d_status, uint64_t limit_ns, void* stream) {
   if (!d_status) return SP24_ERR_INVALID_ARG;
   int sms = 0;

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+struct sp24_mma_problem;  // include/sp24.h
+
 namespace sp24 {
 
 // element codes: identical to sp24_dtype in include/sp24.h
@@ -109,6 +111,12 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
                  const void* values, int64_t ldv, const void* meta, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd, void* workspace,
                  int32_t* status, int num_sms, cudaStream_t s, const BatchArgs* batch = nullptr);
+
+// Up to kMaxGroupPerLaunch validated, non-empty float problems in one launch (the caller
+// splits longer lists); returns 0 or an sp24_status value.
+constexpr int kMaxGroupPerLaunch = 32;
+int launch_spmma_grouped(int ta, int tb, int tc, int td, const sp24_mma_problem* problems,
+                         int count, int32_t* status, int num_sms, cudaStream_t s);
 
 // device properties of the current device, cached; returns false if not sm_103
 bool current_device(int* num_sms);

@@ -40,6 +40,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "../../include/sp24.h"
 #include "sp24_device.cuh"
 #include "sp24_internal.h"
 
@@ -356,14 +357,76 @@ __device__ __forceinline__ void store_chunk_s32(const uint32_t* v, const MmaPara
   }
 }
 
+// A grouped launch: up to kMaxGroup problems of different shapes (same element types)
+// whose tiles share one persistent grid.  Everything the kernel reads per problem, tensor
+// maps included, travels in kernel parameter space (about 15 KB), so the launch needs no
+// device memory of its own.
+constexpr int kMaxGroup = 32;
+static_assert(kMaxGroup == kMaxGroupPerLaunch, "one group table per launch");
+struct GroupTable {
+  CUtensorMap a[kMaxGroup], b[kMaxGroup], m[kMaxGroup];
+  int count;
+  int tile_start[kMaxGroup + 1];  // problem g owns launch tiles tile_start[g] .. [g+1]-1
+  int M[kMaxGroup], N[kMaxGroup], K[kMaxGroup], num_kb[kMaxGroup];
+  int mtiles[kMaxGroup], ntiles[kMaxGroup], batoms[kMaxGroup];
+  uint32_t idesc[kMaxGroup];
+  const void* C[kMaxGroup];
+  void* D[kMaxGroup];
+  int64_t ldc[kMaxGroup], ldd[kMaxGroup];
+  int c32[kMaxGroup], d32[kMaxGroup];
+};
+
+// The problem a launch tile belongs to (0 without a group table) and its tile number
+// inside that problem.
+template <bool kGrouped>
+__device__ __forceinline__ int tile_problem(const GroupTable* gt, int t, int& local) {
+  if constexpr (!kGrouped) {
+    local = t;
+    return 0;
+  } else {
+    int g = 0;
+    while (g + 1 < gt->count && t >= gt->tile_start[g + 1]) ++g;
+    local = t - gt->tile_start[g];
+    return g;
+  }
+}
+
+// The kernel parameters as one problem of a group sees them (the launch's own parameters
+// without a group table).
+template <bool kGrouped>
+__device__ __forceinline__ void problem_params(const MmaParams& p, const GroupTable* gt, int g,
+                                               MmaParams& q) {
+  if constexpr (kGrouped) {
+    q = p;
+    q.M = gt->M[g];
+    q.N = gt->N[g];
+    q.K = gt->K[g];
+    q.num_kb = gt->num_kb[g];
+    q.mtiles = gt->mtiles[g];
+    q.ntiles = gt->ntiles[g];
+    q.batoms = gt->batoms[g];
+    q.C = gt->C[g];
+    q.D = gt->D[g];
+    q.ldc = gt->ldc[g];
+    q.ldd = gt->ldd[g];
+    q.c32 = gt->c32[g];
+    q.d32 = gt->d32[g];
+    q.batch = 1;
+    q.stride_c = q.stride_d = 0;
+  } else {
+    (void)p, (void)gt, (void)g, (void)q;
+  }
+}
+
 // OUT: 0 = f32 output, 1 = 16-bit float output (bf16 or f16 by p.d_f16), 2 = s32 output
 // (integer mode).  C (nullable) is f32, bf16 or f16 (p.ctype) for float outputs, s32 for
 // integer mode.
-template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN>
-__global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
-    spmma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmM, const MmaParams p,
-                 const uint32_t idesc) {
+// kGrouped: the tiles of the problems of a group table (tmA/tmB/tmM/idesc unused);
+// otherwise one problem, or a strided batch, with tensor maps tmA, tmB, tmM.
+template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN, bool kGrouped>
+__device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                           const CUtensorMap* tmM, const MmaParams& p,
+                                           const uint32_t idesc, const GroupTable* gt) {
   using G = Geo<ESZ, kPair, kNarrow, kHalfN>;
   constexpr int kStages = G::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -380,7 +443,7 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kABytes;
   uint8_t* sM = sB + kStages * G::kBBytes;
-  const int ntiles_total = p.mtiles * p.ntiles * p.batch;
+  const int ntiles_total = kGrouped ? gt->tile_start[gt->count] : p.mtiles * p.ntiles * p.batch;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -396,9 +459,11 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
-    prefetch_tmap(&tmM);
+    if constexpr (!kGrouped) {
+      prefetch_tmap(tmA);
+      prefetch_tmap(tmB);
+      prefetch_tmap(tmM);
+    }
   }
   if (warp == 1) {
     if constexpr (kPair) {
@@ -424,35 +489,43 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
     if (lane == 0) {
       int q = 0;
       for (int t = unit; t < ntiles_total && !*abort; t += nunits) {
+        int lt;
+        const int g = tile_problem<kGrouped>(gt, t, lt);
+        MmaParams qg;
+        problem_params<kGrouped>(p, gt, g, qg);
+        const MmaParams& pp = kGrouped ? qg : p;
+        const CUtensorMap* mA = kGrouped ? &gt->a[g] : tmA;
+        const CUtensorMap* mB = kGrouped ? &gt->b[g] : tmB;
+        const CUtensorMap* mM = kGrouped ? &gt->m[g] : tmM;
         int b, mt, nt;
-        batch_tile<G::kTileM>(p, t, b, mt, nt);
+        batch_tile<G::kTileM>(pp, lt, b, mt, nt);
         const int mt128 = kPair ? mt * 2 + int(rank) : mt;  // this CTA's 128-row tile
         const int bcol = nt * G::kTileN + int(rank) * G::kBCols;
         const uint32_t tx =
-            uint32_t(kABytes + p.batoms * G::kAtomBytes + G::kMetaBytes) * (kPair ? 2u : 1u);
-        for (int kb = 0; kb < p.num_kb; ++kb, ++q) {
+            uint32_t(kABytes + pp.batoms * G::kAtomBytes + G::kMetaBytes) * (kPair ? 2u : 1u);
+        for (int kb = 0; kb < pp.num_kb; ++kb, ++q) {
           const int s = q % kStages;
           if (!mbar_wait(&empty_bar[s], ((q / kStages) & 1) ^ 1u, abort, p.limit_ns)) break;
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], tx);
           const int kx = kb * (G::kStageK / 2);
-          const int mrow = (mt128 * p.num_kb + kb) * (G::kMetaBytes / 128);
+          const int mrow = (mt128 * pp.num_kb + kb) * (G::kMetaBytes / 128);
           if constexpr (kPair) {
             const uint32_t fb = mapa(&full_bar[s], 0);
-            tma_load_3d_pair(sA + s * kABytes, &tmA, fb, kx, mt128 * 128, b);
+            tma_load_3d_pair(sA + s * kABytes, mA, fb, kx, mt128 * 128, b);
 #pragma unroll
             for (int a = 0; a < G::kAtoms; ++a)
-              if (a < p.batoms)
-                tma_load_3d_pair(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, fb,
+              if (a < pp.batoms)
+                tma_load_3d_pair(sB + s * G::kBBytes + a * G::kAtomBytes, mB, fb,
                                  bcol + a * G::kAtomN, kb * G::kStageK, b);
-            tma_load_3d_pair(sM + s * G::kMetaBytes, &tmM, fb, 0, mrow, b);
+            tma_load_3d_pair(sM + s * G::kMetaBytes, mM, fb, 0, mrow, b);
           } else {
-            tma_load_3d(sA + s * kABytes, &tmA, &full_bar[s], kx, mt128 * 128, b);
+            tma_load_3d(sA + s * kABytes, mA, &full_bar[s], kx, mt128 * 128, b);
 #pragma unroll
             for (int a = 0; a < G::kAtoms; ++a)
-              if (a < p.batoms)
-                tma_load_3d(sB + s * G::kBBytes + a * G::kAtomBytes, &tmB, &full_bar[s],
+              if (a < pp.batoms)
+                tma_load_3d(sB + s * G::kBBytes + a * G::kAtomBytes, mB, &full_bar[s],
                             bcol + a * G::kAtomN, kb * G::kStageK, b);
-            tma_load_3d(sM + s * G::kMetaBytes, &tmM, &full_bar[s], 0, mrow, b);
+            tma_load_3d(sM + s * G::kMetaBytes, mM, &full_bar[s], 0, mrow, b);
           }
         }
       }
@@ -471,6 +544,11 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
       const uint64_t mdesc_hi = smem_desc_hi(0, 128, 0);
       int q = 0, local = 0, chunk = 0;
       for (int t = unit; t < ntiles_total && !*abort; t += nunits, ++local) {
+        int lt;
+        const int g = tile_problem<kGrouped>(gt, t, lt);
+        const int num_kb = kGrouped ? gt->num_kb[g] : p.num_kb;
+        const int kdense = kGrouped ? gt->K[g] : p.K;
+        const uint32_t id = kGrouped ? gt->idesc[g] : idesc;
         bool ok = true;
         int abuf = 0;
         uint32_t d_tmem = tmem;
@@ -481,7 +559,7 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
           tc_fence_after();
           d_tmem = tmem + uint32_t(abuf * G::kTileN);
         }
-        for (int kb = 0; kb < p.num_kb; ++kb, ++q) {
+        for (int kb = 0; kb < num_kb; ++kb, ++q) {
           const int s = q % kStages;
           const uint32_t par = (q / kStages) & 1;
           const int kc = (OUT == 2) ? kb % p.chunk : 0;  // stage within an integer chunk
@@ -518,14 +596,14 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
           const int first = (OUT == 2) ? kc : kb;  // accumulate unless the chunk/tile starts
 #pragma unroll
           for (int j = 0; j < G::kMmas; ++j) {
-            if (k0 + j * G::kMmaK < p.K) {
+            if (k0 + j * G::kMmaK < kdense) {
               const uint64_t ad = smem_desc(a_saddr + 32 * j, adesc_hi);
               const uint64_t bd = smem_desc(b_saddr + j * G::kMmaK * G::kAtomInner, bdesc_hi);
               const uint32_t acc = (first > 0 || j > 0) ? 1u : 0u;
               if constexpr (kPair)
-                tc_mma_sp_pair<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, idesc, acc);
+                tc_mma_sp_pair<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, id, acc);
               else
-                tc_mma_sp<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, idesc, acc);
+                tc_mma_sp<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, id, acc);
             }
           }
           if constexpr (kPair)
@@ -533,7 +611,7 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
           else
             tc_commit(&empty_bar[s]);
           if constexpr (OUT == 2) {
-            if (kc == p.chunk - 1 || kb == p.num_kb - 1) {  // chunk done
+            if (kc == p.chunk - 1 || kb == num_kb - 1) {  // chunk done
               if constexpr (kPair)
                 tc_commit_pair_mc(&acc_full[abuf], 3);
               else
@@ -565,19 +643,24 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
         kPair ? mapa(&acc_empty[0], 0) : smem_addr(&acc_empty[0]);
     int local = 0, ichunk = 0;
     for (int t = unit; t < ntiles_total; t += nunits, ++local) {
+      int lt;
+      const int g = tile_problem<kGrouped>(gt, t, lt);
+      MmaParams qg;
+      problem_params<kGrouped>(p, gt, g, qg);
+      const MmaParams& pp = kGrouped ? qg : p;
       int b, mt, nt;
-      batch_tile<G::kTileM>(p, t, b, mt, nt);
-      const int64_t cofs = b * p.stride_c, dofs = b * p.stride_d;
+      batch_tile<G::kTileM>(pp, lt, b, mt, nt);
+      const int64_t cofs = b * pp.stride_c, dofs = b * pp.stride_d;
       const int abuf = G::kAccBufs == 1 ? 0 : (local & 1);
       const int use = G::kAccBufs == 1 ? local : (local >> 1);
       if constexpr (OUT != 2) {
-        if (!mbar_wait(&acc_full[abuf], use & 1, abort, p.limit_ns)) break;
+        if (!mbar_wait(&acc_full[abuf], use & 1, abort, pp.limit_ns)) break;
         tc_fence_after();
       }
       const int row = mt * G::kTileM + int(rank) * 128 + quad * 32 + lane;
       const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16) + uint32_t(abuf * G::kTileN);
       if constexpr (OUT == 2) {
-        // integer mode: one f32 chunk per p.chunk stages, summed exactly in int32; each
+        // integer mode: one f32 chunk per pp.chunk stages, summed exactly in int32; each
         // thread owns one row x kIntCols columns (pair 256 x 256: 128)
         (void)abuf;
         constexpr int kIntCols = G::kTileN * 4 / G::kEpiWarps;
@@ -585,12 +668,12 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
         uint32_t sum[kIntCols];
 #pragma unroll
         for (int j = 0; j < kIntCols; ++j) sum[j] = 0u;
-        const int nch = (p.num_kb + p.chunk - 1) / p.chunk;
+        const int nch = (pp.num_kb + pp.chunk - 1) / pp.chunk;
         bool ok = true;
         for (int c = 0; c < nch; ++c, ++ichunk) {
           const int b = G::kAccBufs == 1 ? 0 : (ichunk & 1);
           const int cuse = G::kAccBufs == 1 ? ichunk : (ichunk >> 1);
-          if (!mbar_wait(&acc_full[b], cuse & 1, abort, p.limit_ns)) {
+          if (!mbar_wait(&acc_full[b], cuse & 1, abort, pp.limit_ns)) {
             ok = false;
             break;
           }
@@ -614,11 +697,11 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
           }
         }
         if (!ok) break;
-        if (row < p.M) {
+        if (row < pp.M) {
 #pragma unroll
           for (int c = 0; c < kIntCols / 32; ++c) {
             const int col0 = nt * G::kTileN + cbase + c * 32;
-            if (col0 < p.N) store_chunk_s32(&sum[c * 32], p, row, col0);
+            if (col0 < pp.N) store_chunk_s32(&sum[c * 32], pp, row, col0);
           }
         }
       } else if constexpr (kPair) {
@@ -644,22 +727,32 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
         const int col0 = nt * G::kTileN + half * kCols;
         if (t + nunits < ntiles_total) {  // the next tile's C, needed one mainloop from now
           int b2, mt2, nt2;
-          batch_tile<G::kTileM>(p, t + nunits, b2, mt2, nt2);
-          prefetch_c_rows(p, mt2 * G::kTileM + int(rank) * 128 + quad * 32 + (lane >> 2),
-                          nt2 * G::kTileN + half * kCols, lane & 3, kCols, b2 * p.stride_c);
+          int lt2;
+          const int g2 = tile_problem<kGrouped>(gt, t + nunits, lt2);
+          MmaParams qg2;
+          problem_params<kGrouped>(p, gt, g2, qg2);
+          const MmaParams& pp2 = kGrouped ? qg2 : p;
+          batch_tile<G::kTileM>(pp2, lt2, b2, mt2, nt2);
+          prefetch_c_rows(pp2, mt2 * G::kTileM + int(rank) * 128 + quad * 32 + (lane >> 2),
+                          nt2 * G::kTileN + half * kCols, lane & 3, kCols, b2 * pp2.stride_c);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            store_row<OUT, kSegP>(r[h], e, p, row0 + 16 * h + 8 * e, col0, lane & 3, cofs, dofs);
+            store_row<OUT, kSegP>(r[h], e, pp, row0 + 16 * h + 8 * e, col0, lane & 3, cofs, dofs);
       } else {
         const int row0 = mt * G::kTileM + quad * 32 + (lane >> 2);
         if (t + nunits < ntiles_total) {  // the next tile's C, needed one mainloop from now
           int b2, mt2, nt2;
-          batch_tile<G::kTileM>(p, t + nunits, b2, mt2, nt2);
-          prefetch_c_rows(p, mt2 * G::kTileM + quad * 32 + (lane >> 2), nt2 * G::kTileN, lane & 3,
-                          G::kTileN, b2 * p.stride_c);
+          int lt2;
+          const int g2 = tile_problem<kGrouped>(gt, t + nunits, lt2);
+          MmaParams qg2;
+          problem_params<kGrouped>(p, gt, g2, qg2);
+          const MmaParams& pp2 = kGrouped ? qg2 : p;
+          batch_tile<G::kTileM>(pp2, lt2, b2, mt2, nt2);
+          prefetch_c_rows(pp2, mt2 * G::kTileM + quad * 32 + (lane >> 2), nt2 * G::kTileN,
+                          lane & 3, G::kTileN, b2 * pp2.stride_c);
         }
         constexpr int kSeg = G::kTileN / 32;
         uint32_t r[2][16 * kSeg];
@@ -675,7 +768,7 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            store_row<OUT, kSeg>(r[h], e, p, row0 + 16 * h + 8 * e, nt * G::kTileN, lane & 3,
+            store_row<OUT, kSeg>(r[h], e, pp, row0 + 16 * h + 8 * e, nt * G::kTileN, lane & 3,
                                  cofs, dofs);
         tc_fence_before();
         __syncwarp();
@@ -695,6 +788,23 @@ __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
       tmem_dealloc(tmem, kTmemCols);
   }
   if (threadIdx.x == 0 && *abort && p.status != nullptr) atomicOr(p.status, kDevTimeout);
+}
+
+// One problem (or a strided batch of equal problems).
+template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN>
+__global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
+    spmma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmM, const __grid_constant__ MmaParams p,
+                 const uint32_t idesc) {
+  spmma_body<ESZ, OUT, kPair, kNarrow, kHalfN, false>(&tmA, &tmB, &tmM, p, idesc, nullptr);
+}
+
+// The problems of a group table, one persistent grid over all their tiles.
+template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN>
+__global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
+    spmma_grouped_kernel(const __grid_constant__ MmaParams p,
+                         const __grid_constant__ GroupTable gt) {
+  spmma_body<ESZ, OUT, kPair, kNarrow, kHalfN, true>(nullptr, nullptr, nullptr, p, 0u, &gt);
 }
 
 // ------------------------------------------------------------------ host side
@@ -833,6 +943,117 @@ size_t int_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const int64_t a = (M * (K / 2) * 2 + 255) / 256 * 256;
   const int64_t b = K * int_ws_ldb(N) * 2;
   return size_t(a + b);
+}
+
+namespace {
+
+// One launch over up to kMaxGroup problems (already validated, all non-empty): a group
+// table with each problem's tensor maps, tile range and epilogue fields.
+template <int ESZ, int OUT, bool kPair, bool kNarrow = false, bool kHalfN = false>
+int run_grouped(MmaParams p, const sp24_mma_problem* pr, int count, uint32_t at, uint32_t bt,
+                int stage_k, int num_sms, cudaStream_t s) {
+  using G = Geo<ESZ, kPair, kNarrow, kHalfN>;
+  GroupTable gt;
+  memset(&gt, 0, sizeof(gt));
+  gt.count = count;
+  int tiles = 0;
+  for (int g = 0; g < count; ++g) {
+    const sp24_mma_problem& q = pr[g];
+    const int M = int(q.M), N = int(q.N), K = int(q.K);
+    gt.M[g] = M;
+    gt.N[g] = N;
+    gt.K[g] = K;
+    gt.num_kb[g] = (K + stage_k - 1) / stage_k;
+    gt.mtiles[g] = (M + G::kTileM - 1) / G::kTileM;
+    gt.ntiles[g] = (N + G::kTileN - 1) / G::kTileN;
+    gt.batoms[g] = kNarrow ? (N + G::kAtomN - 1) / G::kAtomN : G::kAtoms;
+    gt.idesc[g] = kNarrow ? idesc_sparse_f32(at, bt, 128, uint32_t((N + 15) / 16 * 16))
+                          : idesc_sparse_f32(at, bt, kPair ? 256 : 128, uint32_t(G::kTileN));
+    gt.C[g] = q.C;
+    gt.D[g] = q.D;
+    gt.ldc[g] = q.ldc;
+    gt.ldd[g] = q.ldd;
+    gt.c32[g] = (reinterpret_cast<uintptr_t>(q.C) % 32 == 0 && (q.ldc * 4) % 32 == 0) ? 1 : 0;
+    gt.d32[g] = (reinterpret_cast<uintptr_t>(q.D) % 32 == 0 && (q.ldd * 4) % 32 == 0) ? 1 : 0;
+    if (K > 0) {
+      if (!make_tmap(&gt.a[g], q.values, ESZ, uint64_t(K / 2), uint64_t(M),
+                     uint64_t(q.ldv) * ESZ, 128 / ESZ, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1, 0) ||
+          !make_tmap(&gt.b[g], q.B, ESZ, uint64_t(N), uint64_t(K), uint64_t(q.ldb) * ESZ,
+                     G::kAtomN, G::kStageK,
+                     kNarrow ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B, 1, 0) ||
+          !make_tmap(&gt.m[g], q.meta, 4, 32,
+                     uint64_t(meta_mtiles(M)) * gt.num_kb[g] * (G::kMetaBytes / 128), 128, 32,
+                     G::kMetaBytes / 128, CU_TENSOR_MAP_SWIZZLE_NONE, 1, 0))
+        return 4;
+    }
+    gt.tile_start[g] = tiles;
+    tiles += gt.mtiles[g] * gt.ntiles[g];
+  }
+  gt.tile_start[count] = tiles;
+  auto kern = spmma_grouped_kernel<ESZ, OUT, kPair, kNarrow, kHalfN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) !=
+      cudaSuccess)
+    return 4;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(G::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = G::kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  int units = kPair ? num_sms / 2 : num_sms;
+  if (tiles < units) units = tiles;
+  cfg.gridDim = dim3(units * (kPair ? 2 : 1), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kern, p, gt) != cudaSuccess) return 4;
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+// The tile shape is the one sp24_mma picks for the widest output of the group, so that
+// every problem fits it.
+template <int ESZ, int OUT>
+int dispatch_grouped(const MmaParams& p, const sp24_mma_problem* pr, int count, uint32_t at,
+                     uint32_t bt, int stage_k, int num_sms, cudaStream_t s) {
+  int64_t nmax = 0;
+  for (int g = 0; g < count; ++g) nmax = pr[g].N > nmax ? pr[g].N : nmax;
+  if (nmax > 128) return run_grouped<ESZ, OUT, true>(p, pr, count, at, bt, stage_k, num_sms, s);
+  if (nmax <= 32)
+    return run_grouped<ESZ, OUT, false, true>(p, pr, count, at, bt, stage_k, num_sms, s);
+  if constexpr (ESZ == 2)
+    return run_grouped<ESZ, OUT, true, false, true>(p, pr, count, at, bt, stage_k, num_sms, s);
+  else
+    return run_grouped<ESZ, OUT, false>(p, pr, count, at, bt, stage_k, num_sms, s);
+}
+
+}  // namespace
+
+int launch_spmma_grouped(int ta, int tb, int tc, int td, const sp24_mma_problem* problems,
+                         int count, int32_t* status, int num_sms, cudaStream_t s) {
+  if (count <= 0) return 0;
+  MmaParams p;
+  memset(&p, 0, sizeof(p));
+  p.batch = 1;
+  p.status = status;
+  p.chunk = 8;
+  p.limit_ns = 1000000000ull;
+  bool anyC = false;
+  for (int g = 0; g < count; ++g) anyC = anyC || problems[g].C != nullptr;
+  p.ctype = (anyC && tc == kBF16) ? 1 : (anyC && tc == kF16) ? 2 : 0;
+  p.d_f16 = td == kF16 ? 1 : 0;
+  const uint32_t at = (ta == kBF16 || ta == kE5M2) ? 1u : 0u;
+  const uint32_t bt = (tb == kBF16 || tb == kE5M2) ? 1u : 0u;
+  const bool out16 = td != kF32;
+  const int sk = stage_k(ta);
+  if (dtype_bytes(ta) == 2)
+    return out16 ? dispatch_grouped<2, 1>(p, problems, count, at, bt, sk, num_sms, s)
+                 : dispatch_grouped<2, 0>(p, problems, count, at, bt, sk, num_sms, s);
+  return out16 ? dispatch_grouped<1, 1>(p, problems, count, at, bt, sk, num_sms, s)
+               : dispatch_grouped<1, 0>(p, problems, count, at, bt, sk, num_sms, s);
 }
 
 int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K,

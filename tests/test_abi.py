@@ -232,3 +232,29 @@ def test_compress_meta_argument_checks():
     if not torch.cuda.is_available():
         assert cm(index=None, ldi=0) == NODEV           # the index is optional
         assert cm() == NODEV
+
+
+def test_grouped_argument_checks():
+    L = sp.lib()
+
+    def grouped(ta=BF16, tb=BF16, tc=F32, td=F32, probs=None, count=None):
+        probs = probs if probs is not None else [dict()]
+        arr = (sp.Problem * len(probs))()
+        for i, d in enumerate(probs):
+            f = dict(M=128, N=128, K=128, values=0x10000, ldv=64, meta=0x10000, B=0x10000,
+                     ldb=128, C=0, ldc=128, D=0x10000, ldd=128)
+            f.update(d)
+            arr[i] = sp.Problem(**f)
+        return L.sp24_mma_grouped(ta, tb, tc, td, arr, len(probs) if count is None else count,
+                                  None, None)
+    assert grouped(ta=S8, tb=S8, tc=S32, td=S32) == UNSUPPORTED
+    assert grouped(ta=F16, tb=BF16) == UNSUPPORTED
+    assert grouped(td=S32) == UNSUPPORTED
+    assert grouped(count=-1) == INVALID
+    assert grouped(count=0) == OK
+    assert grouped(probs=[dict(K=48)]) == INVALID
+    assert grouped(probs=[dict(), dict(D=0)]) == INVALID           # any bad problem refuses
+    assert grouped(probs=[dict(ldb=132)]) == ALIGN
+    assert grouped(probs=[dict(M=0), dict(N=0)]) == OK              # nothing to do
+    if not torch.cuda.is_available():
+        assert grouped(probs=[dict(), dict(M=300, N=40)]) == NODEV

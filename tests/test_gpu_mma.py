@@ -353,3 +353,52 @@ def test_int8_long_k_exact():
          "M": M, "N": N, "K": K}
     Dg, Dref, _ = run_case(c, mode="mask", out_dtype=torch.int32, rows=np.arange(0, M, 17))
     assert np.all(Dref == (K // 2) * 16384)   # 2^29: far beyond 2^24, exact
+
+
+# ---- grouped products: problems of different shapes in one launch -----------------------
+
+def _grouped_case(ta, shapes, tc, out, seed):
+    items, refs = [], []
+    for i, (M, N, K) in enumerate(shapes):
+        c = inputs.case(ta, ta, M, N, K, seed=seed + i, tc=tc,
+                        dist="int4" if ta in ("e4m3", "e5m2") else "normal")
+        values, index, meta = sp.compress_meta(c["A"].cuda(), mode="mask", mask=c["mask"].cuda())
+        items.append((values, meta, c["B"].cuda(), None if c["C"] is None else c["C"].cuda()))
+        refs.append(c)
+    D = sp.mma_grouped(items, out_dtype=out)
+    torch.cuda.synchronize()
+    for c, Dg in zip(refs, D):
+        M, N, K = c["M"], c["N"], c["K"]
+        v_ref, i_ref, _ = oracle.compress(inputs.bits(c["A"]), ta, "mask", mask=c["mask"].numpy())
+        rows = sample_rows(M)
+        Dref, S = oracle.mma_f64(v_ref, i_ref, inputs.bits(c["B"]),
+                                 None if c["C"] is None else inputs.bits(c["C"]), ta, ta, K,
+                                 tc=tc or "f32", rows=rows)
+        from parity import OUT_KIND
+        check_float(Dg.float().cpu().numpy()[rows], Dref, S, OUT_KIND[out],
+                    f"grouped {ta} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("ta,shapes,tc,out", [
+    # widest N > 128: 256 x 256 pair tiles for all
+    ("bf16", [(300, 200, 352), (128, 64, 128), (513, 136, 1056), (64, 8, 64)], "f32",
+     torch.float32),
+    # widest N <= 32: narrow tiles, each problem its own MMA N
+    ("e4m3", [(1000, 16, 512), (200, 32, 256), (64, 32, 1024)], None, torch.bfloat16),
+    # 32 < widest N <= 128, 16-bit: 256 x 128 pair tiles; FP8: 128 x 128 single tiles
+    ("f16", [(700, 104, 384), (129, 40, 128), (256, 128, 2048)], "f16", torch.float16),
+    ("e5m2", [(700, 112, 512), (129, 48, 256)], "f32", torch.float32),
+])
+def test_grouped_shapes(ta, shapes, tc, out):
+    _grouped_case(ta, shapes, tc, out, seed=len(shapes))
+
+
+def test_grouped_many_problems_and_empty_ones():
+    # 40 problems (two launches of 32 and 8), two of them empty
+    shapes = [(64 + 16 * (i % 5), 16 * (1 + i % 3), 128 * (1 + i % 2)) for i in range(38)]
+    _grouped_case("bf16", shapes, "f32", torch.float32, seed=100)
+    values = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    meta = torch.empty(16, dtype=torch.uint8, device="cuda")
+    B = torch.zeros((128, 16), dtype=torch.bfloat16, device="cuda")
+    D = sp.mma_grouped([(values, meta, B, None)])
+    assert D[0].shape == (0, 16)
