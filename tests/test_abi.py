@@ -258,3 +258,15 @@ def test_grouped_argument_checks():
     assert grouped(probs=[dict(M=0), dict(N=0)]) == OK              # nothing to do
     if not torch.cuda.is_available():
         assert grouped(probs=[dict(), dict(M=300, N=40)]) == NODEV
+
+
+def test_header_is_plain_c_and_cpp(tmp_path):
+    # the boundary header compiles on its own as C99 and as C++17 (no torch or CUDA types)
+    import shutil
+    import subprocess
+    for compiler, std, lang in (("gcc", "-std=c99", "c"), ("g++", "-std=c++17", "c++")):
+        if shutil.which(compiler) is None:
+            pytest.skip(f"{compiler} not available")
+        r = subprocess.run([compiler, std, "-Wall", "-Wextra", "-pedantic", "-fsyntax-only",
+                            "-x", lang, HEADER], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
