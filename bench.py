@@ -315,6 +315,52 @@ def gpu_arm(args, world, rank, local):
     # passes for integer operands)
     launches_per_step = (1 if fused else 2) + (3 if integer else 1)
 
+    def compress_call(s, st):
+        m = s["mask"]
+        if fused:
+            return L.sp24_compress_meta(cs["ta"], M, K, sp._ptr(s["A"]), K, sp._ptr(m), K,
+                                        sp.MODES[mode], sp._ptr(s["values"]), K // 2,
+                                        sp._ptr(s["index"]), K // 32, sp._ptr(s["meta"]),
+                                        sp._ptr(status), st)
+        rc = L.sp24_compress(cs["ta"], M, K, sp._ptr(s["A"]), K, sp._ptr(m), K,
+                             sp.MODES[mode], sp._ptr(s["values"]), K // 2,
+                             sp._ptr(s["index"]), K // 32, sp._ptr(status), st)
+        return rc | L.sp24_meta_prepare(cs["ta"], M, K, sp._ptr(s["index"]), K // 32,
+                                        sp._ptr(s["meta"]), st)
+
+    def product_call(s, st):
+        return L.sp24_mma(cs["ta"], cs["tb"], cs["tc"], cs["td"], M, N, K, sp._ptr(s["values"]),
+                          K // 2, sp._ptr(s["meta"]), sp._ptr(s["B"]), N, sp._ptr(s["C"]), N,
+                          sp._ptr(s["D"]), N, sp._ptr(ws), ws_bytes, sp._ptr(status), st)
+
+    s_comp, s_prod = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def launch_overlapped(nsteps):
+        # the compression of step i on one stream, the products on another: step i+1's
+        # compression runs while step i's product finishes (each step's product waits for
+        # its own compression; a compression waits for the last product that read its
+        # input set)
+        cur = torch.cuda.current_stream(dev)
+        s_comp.wait_stream(cur)
+        s_prod.wait_stream(cur)
+        comp_done = [torch.cuda.Event() for _ in range(nsteps)]
+        prod_done = [torch.cuda.Event() for _ in range(nsteps)]
+        for i in range(nsteps):
+            s = sets[i % len(sets)]
+            with torch.cuda.stream(s_comp):
+                if i >= len(sets):
+                    s_comp.wait_event(prod_done[i - len(sets)])
+                rc = compress_call(s, sp._stream(s_comp))
+                comp_done[i].record(s_comp)
+            with torch.cuda.stream(s_prod):
+                s_prod.wait_event(comp_done[i])
+                rc |= product_call(s, sp._stream(s_prod))
+                prod_done[i].record(s_prod)
+            if rc != 0:
+                raise RuntimeError(f"sp24 call failed (status bits {rc})")
+        cur.wait_stream(s_comp)
+        cur.wait_stream(s_prod)
+
     def launch(s, ev=None):
         # the C-ABI calls of one step, on the current stream (a graph's capture stream
         # while one is being recorded)
@@ -357,22 +403,36 @@ def gpu_arm(args, world, rank, local):
     # the K steps recorded once as a CUDA graph (launch overhead off the timed path; the
     # GEMM's programmatic dependency on the pass before it becomes a graph edge); eager
     # launches if capture is refused
-    graph = None
-    if not args.eager:
-        try:
-            g = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream(dev)
-            cap.wait_stream(stream)
-            with torch.cuda.graph(g, stream=cap):
+    # Schedules: "overlapped" (the default) runs the steps' compressions on one stream and
+    # their products on another, so step i+1's compression fills the SMs that step i's
+    # product leaves idle in its last wave; "serial" runs each step's two calls back to
+    # back on one stream (the product launched to overlap the compression's tail).
+    overlap = not args.serial
+
+    def capture(overlapped):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            if overlapped:
+                launch_overlapped(args.steps)
+            else:
                 for i in range(args.steps):
                     launch(sets[i % len(sets)])
-            stream.wait_stream(cap)
-            g.replay()  # untimed: uploads the graph
-            torch.cuda.synchronize(dev)
-            graph = g
+        stream.wait_stream(cap)
+        g.replay()  # untimed: uploads the graph
+        torch.cuda.synchronize(dev)
+        return g
+
+    graph = graph_serial = None
+    if not args.eager:
+        try:
+            graph = capture(overlap)
+            graph_serial = capture(False) if overlap else graph
         except Exception as exc:  # noqa: BLE001 - any capture failure means eager timing
             log(f"graph capture failed, timing eager launches: {exc}")
             torch.cuda.synchronize(dev)
+            graph = graph_serial = None
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} during warm-up")
 
@@ -386,6 +446,8 @@ def gpu_arm(args, world, rank, local):
         t_start.record(stream)
         if graph is not None:
             graph.replay()
+        elif overlap:
+            launch_overlapped(args.steps)
         else:
             for i in range(args.steps):
                 launch(sets[i % len(sets)])
@@ -394,6 +456,19 @@ def gpu_arm(args, world, rank, local):
     barrier(world)
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, world)
+    # the serial schedule's step time, for comparison (same steps, one stream)
+    ms_step_serial = None
+    if overlap:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        if graph_serial is not None:
+            graph_serial.replay()
+        else:
+            for i in range(args.steps):
+                launch(sets[i % len(sets)])
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_step_serial = a.elapsed_time(b) / args.steps
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} in the timed region")
     ms_step = total_ms / args.steps
@@ -437,16 +512,22 @@ def gpu_arm(args, world, rank, local):
                       "timed region on the same stream and inputs (events between the kernels "
                       "inside the timed region would serialise the GEMM's programmatic launch)")
     roof["algorithmic_bytes"] = mma_bytes
-    roof["peak_source"] = (f"{src}: bf16 dense {dense} TFLOP/s"
-                           f"{' x2 (fp8/bf16 nominal)' if ta in ('e4m3', 'e5m2') else ''}"
-                           " x2 (2:4 sparse / dense nominal), burst figure"
-                           f"{'; int8 runs exactly on the bf16 path' if integer else ''}")
+    if roof["bound"] == "tensor":
+        roof["peak_source"] = (f"{src}: bf16 dense {dense} TFLOP/s"
+                               f"{' x2 (fp8/bf16 nominal)' if ta in ('e4m3', 'e5m2') else ''}"
+                               " x2 (2:4 sparse / dense nominal), burst figure"
+                               f"{'; int8 runs exactly on the bf16 path' if integer else ''}")
+    else:
+        roof["peak_source"] = (f"{src}: HBM copy bandwidth; the product's intensity "
+                               f"{intensity:.0f} flop/B is below the sparse tensor ridge "
+                               f"{ridge:.0f} flop/B")
     # compression kernel: HBM-bound, algorithmic bytes = A + mask read, values + index written
     cbytes = M * K * esz + (M * K if mode == "mask" else 0) + M * K // 2 * esz + M * K // 8
     kernels = {
         "note": "sp24_mma time includes the int8->bf16 widening pass" if integer else None,
         "sp24_mma_us": k_mma * 1e3,
         "sp24_mma_tflops": achieved_tf,
+        "step_us_serial_schedule": None if ms_step_serial is None else ms_step_serial * 1e3,
     }
     if fused:
         # + the image written (the separate pass would read the index and write the image)
@@ -539,7 +620,12 @@ def gpu_arm(args, world, rank, local):
                              f"{len(sets) * set_bytes(sets[0]) / 2**20:.0f} MiB > L2",
                        "parallelism": f"replicas x{world}",
                        "launch": ("one CUDA graph of the K steps" if graph is not None
-                                  else "eager launches")},
+                                  else "eager launches"),
+                       "schedule": ("overlapped: the K independent steps run their "
+                                    "compressions on one stream and their products on "
+                                    "another, so step i+1's compression overlaps step i's "
+                                    "product" if overlap else
+                                    "serial: each step's calls back to back on one stream")},
             "roofline": roof,
             "kernels": kernels,
             "cpu_baseline": cpu,
@@ -559,6 +645,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--serial", action="store_true",
+                    help="run each step's calls back to back on one stream (by default step "
+                         "i+1's compression runs on its own stream during step i's product)")
     ap.add_argument("--eager", action="store_true",
                     help="launch the timed steps one by one instead of as a CUDA graph")
     ap.add_argument("--pass", dest="pass_mode", default="fused", choices=["fused", "separate"],
