@@ -492,7 +492,7 @@ def gpu_arm(args, world, rank, local):
     esz = torch.empty((), dtype=tdt).element_size()
     osz = torch.empty((), dtype=out_dtype).element_size()
     # algorithmic bytes: compressed A, the sparsity metadata at its information size (the
-    # canonical index, M*K/8 bytes; the kernel's image is 4x that), B, C (if any), D, once
+    # canonical index, M*K/8 bytes, the size of the kernel's image), B, C (if any), D, once
     mma_bytes = (M * K // 2 * esz + M * K // 8 + K * N * esz +
                  (M * N * 4 if base["C"] is not None else 0) + M * N * osz)
     unit = "TOP/s" if integer else "TFLOP/s"

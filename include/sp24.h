@@ -134,12 +134,14 @@ size_t sp24_meta_bytes(sp24_dtype t, int64_t M, int64_t K);
 
 /*
  * sp24_meta_prepare -- re-lay the canonical index (as sp24_compress writes it) into the
- * image sp24_mma copies into tensor memory: for every 128-row tile of A, every K step of
- * the kernel (128 dense K for 16-bit types, 256 for FP8 types) and each of the step's
- * four MMAs, one [128][16-byte] block.  Rows are padded to a multiple of 256 and K to
- * the K step; pad groups get the valid pattern {0,1} and their values are zero, so they
- * add nothing.  The image is a format private to sp24_mma (sp24_meta_bytes() gives its
- * size); the canonical index stays the interchange format.
+ * image from which sp24_mma fills tensor memory: for every 128-row tile of A and every K
+ * step of the kernel (128 dense K for 16-bit types, 256 for FP8 types) one block of
+ * 128 lanes x 16 bytes (16-bit types) or x 32 bytes (FP8 types), each lane holding its
+ * words for the step's four MMAs.  Rows are padded to a multiple of 256 and K to the K
+ * step; pad groups get the valid pattern {0,1} and their values are zero, so they add
+ * nothing.  For whole tiles and steps the image is M x K / 8 bytes, the size of the
+ * index.  It is a format private to sp24_mma (sp24_meta_bytes() gives its size); the
+ * canonical index stays the interchange format.
  * 8- and 4-bit integer types use the layout of the 16-bit types (their product runs on
  * the bf16 tensor path).
  * index : device, M x K/32 words, ldi >= K/32, 4-byte aligned.

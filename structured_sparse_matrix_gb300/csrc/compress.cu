@@ -353,10 +353,10 @@ struct FusedGeo {
 // re-layout kernel in meta.cu writes from the canonical index; its layout is described
 // there).  Each warp compresses its unit's 16 rows over the stage's K range chunk by chunk
 // as compress_kernel does (values and canonical index words, which stay the interchange
-// format; index may be null), then writes the band's rows of the stage's 4 MMA blocks
-// with 16-byte stores.  Rows beyond M and K beyond the operand count as all-zero groups
-// (pattern {0,1}): the image padding.
-// kL8: the FP8 layout (256 dense K per stage, lane = row, the MMA's two canonical words);
+// format; index may be null), then writes the band's 16 TMEM lanes of the stage's image
+// block with 16-byte stores (the words of a lane gathered by shuffles).  Rows beyond M and
+// K beyond the operand count as all-zero groups (pattern {0,1}): the image padding.
+// kL8: the FP8 layout (256 dense K per stage, lane = row, the row's 8 canonical words);
 // otherwise the 16-bit layout (128 dense K per stage; lane 16b + l of band b holds 16-bit
 // halves h = l/8 of the canonical words of rows l%8 and l%8 + 8), also used by integers.
 //
@@ -375,6 +375,7 @@ __global__ void __launch_bounds__(128) compress_meta_kernel(CompressArgs a) {
   constexpr int kHalves = kElems >= 16 ? kElems / 16 : 1;  // 16-K halves a chunk starts
   constexpr uint32_t kPadWord = 0x44444444u;
   constexpr uint32_t kPadNibs = kGroups == 8 ? kPadWord : (kPadWord >> (32 - 4 * kGroups));
+  constexpr int kLaneVecs = kL8 ? 2 : 1;  // 16-byte vectors per TMEM lane in an image block
   static_assert(!kL8 || EB == 8, "the FP8 layout holds 8-bit elements");
   extern __shared__ __align__(16) uint8_t fused_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -441,9 +442,10 @@ __global__ void __launch_bounds__(128) compress_meta_kernel(CompressArgs a) {
     uint8_t* vg = a.values + row0 * a.ldv_bytes + cc * 8;
     uint32_t* ig = a.index + row0 * a.ldi + (cc * kElems) / 32;
     const uint8_t* st = ring + buf * G::kUnitBytes;
-    // image rows of this band: block (tile, stage, MMA j) starts at uint4
-    // ((tile * ksteps + s) * 4 + j) * 128, the band's rows at + (band % 8) * 16
-    uint4* img = meta + ((band >> 3) * a.ksteps + s) * (kMmasPerStage * 128) + (band & 7) * 16;
+    // the band's lanes of the (tile, stage) block: the block starts at uint4
+    // (tile * ksteps + s) * kLaneVecs * 128, lane L at + L * kLaneVecs, the band at lane
+    // (band % 8) * 16
+    uint4* img = meta + ((band >> 3) * a.ksteps + s) * (kLaneVecs * 128) + (band & 7) * 16 * kLaneVecs;
     uint32_t half16[kIters][kHalves];
 #pragma unroll
     for (int k = 0; k < kIters; ++k) {
@@ -488,10 +490,13 @@ __global__ void __launch_bounds__(128) compress_meta_kernel(CompressArgs a) {
       if (valid && a.index != nullptr && (lane % kLanesPerWord) == 0) *ig = word;
       ig += i_step;
       if constexpr (kL8) {
-        // MMA j = c / 4 reads canonical words 2j (lanes 4j, 4j+1) and 2j+1 (4j+2, 4j+3)
-        const uint32_t next = __shfl_xor_sync(0xFFFFFFFFu, word, 2);
-        if ((c & 3) == 0)
-          img[(c >> 2) * 128 + kRpi * k + rsub] = make_uint4(word, next, kPadWord, kPadWord);
+        // the row's lane takes its 8 canonical words of the stage in order (MMA j reads
+        // words 2j and 2j + 1); lane c holds word c / 2, so lanes c = 0 and c = 8 gather
+        // words 0-3 and 4-7 and write them
+        const uint32_t w1 = __shfl_xor_sync(0xFFFFFFFFu, word, 2);
+        const uint32_t w2 = __shfl_xor_sync(0xFFFFFFFFu, word, 4);
+        const uint32_t w3 = __shfl_xor_sync(0xFFFFFFFFu, word, 6);
+        if ((c & 7) == 0) img[(kRpi * k + rsub) * 2 + (c >> 3)] = make_uint4(word, w1, w2, w3);
       } else {
 #pragma unroll
         for (int i = 0; i < kHalves; ++i) {
@@ -501,17 +506,26 @@ __global__ void __launch_bounds__(128) compress_meta_kernel(CompressArgs a) {
       }
     }
     if constexpr (!kL8) {
-      // lanes whose chunk starts a 16-K half write it for rows r (< 8) and r + 8 of the band
-      if ((c * kElems) % 16 == 0) {
+      // TMEM lane r + 8h of the band (r < 8) takes, for MMA j, 16-K half 2j + h of rows r
+      // (low 16 bits) and r + 8 (high).  Half hidx of a row is held by the lane of chunk
+      // (hidx / kHalves) * kChunksPerHalf, as its value i = hidx % kHalves; the lane of
+      // chunk h gathers the four words of lane r + 8h and writes its 16 bytes.
+      constexpr int kChunksPerHalf = kElems >= 16 ? 1 : 16 / kElems;
 #pragma unroll
-        for (int k = 0; k < kIters / 2; ++k) {
+      for (int k = 0; k < kIters / 2; ++k) {
+        uint32_t wv[kHalves];
 #pragma unroll
-          for (int i = 0; i < kHalves; ++i) {
-            const int hidx = (c * kElems) / 16 + i;
-            const int j = hidx >> 1, h = hidx & 1;
-            const uint32_t w = half16[k][i] | (half16[k + kIters / 2][i] << 16);
-            img[j * 128 + kRpi * k + rsub + 8 * h] = make_uint4(w, kPadWord, kPadWord, kPadWord);
+        for (int i = 0; i < kHalves; ++i) wv[i] = half16[k][i] | (half16[k + kIters / 2][i] << 16);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t w[kMmasPerStage];
+#pragma unroll
+          for (int j = 0; j < kMmasPerStage; ++j) {
+            const int hidx = 2 * j + h;
+            const int cs = (hidx / kHalves) * kChunksPerHalf;
+            w[j] = __shfl_sync(0xFFFFFFFFu, wv[hidx % kHalves], rsub * kCpr + cs);
           }
+          if (c == h) img[kRpi * k + rsub + 8 * h] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     }

@@ -1,29 +1,30 @@
-// meta.cu -- re-layout of the canonical sparsity index into the image the sparse GEMM
-// copies, stage by stage, into tensor memory.
+// meta.cu -- re-layout of the canonical sparsity index into the image from which the
+// sparse GEMM fills, stage by stage, the metadata slots in tensor memory.
 //
 // Canonical index (as sp24_compress writes it): M x K/32 words, group g of row i in bits
 // 4(g%8)..+3 of word g/8, nibble = p0 | p1 << 2.
 //
-// tcgen05.mma.sp reads the metadata of A from tensor memory (TMEM), and each MMA's
-// metadata must start at a 16-column-aligned TMEM address.  The GEMM fills one such slot
-// per MMA with one tcgen05.cp.128x128b, which copies 16 bytes per lane into 4 consecutive
-// columns.  So the image holds, for every 128-row tile, every stage of the GEMM and each
-// of the stage's 4 MMAs, one block [128 lanes][4 words] with the MMA's words first.  The
-// image reaches shared memory by TMA together with the operands, and the tensor pipe
-// copies it to TMEM in order with the MMAs; nothing on the way is written by threads.
+// tcgen05.mma.sp reads the metadata of A from tensor memory (TMEM), one slot per MMA at
+// a 16-column-aligned address.  In the GEMM four writer warps, one per quarter of the
+// TMEM lanes, store each stage's words into the slots with tcgen05.st.  So the image
+// holds, for every 128-row tile and every stage of the GEMM, one block
+// [128 lanes][W words]: lane L's words for the stage's 4 MMAs, in MMA order (W = 4 for
+// 16-bit types, W = 8 for FP8), read by the lane's thread with 16-byte loads.  It is a
+// permutation of the canonical index plus padding: M x K / 8 bytes for whole tiles and
+// stages.
 //
-// Word placement inside a block (measured on sm_103a with tcgen05.mma.sp, M = 128):
+// Word placement (measured on sm_103a with tcgen05.mma.sp, M = 128):
 //   kind::f16 (16-bit types, 32 dense K per MMA, one word per lane): in each 16-row
 //     band b, lane 16b+l holds the halves (h = l/8) of two rows' canonical words:
 //       word = ((w[16b+l%8] >> 16h) & 0xffff) | ((w[16b+l%8+8] >> 16h) & 0xffff) << 16
 //     so nibble q of lane 16b+l is group (q%4)+4h of row 16b+l%8+8(q/4).
-//   kind::f8f6f4 (FP8 types, 64 dense K per MMA, two words per lane): lane = row,
-//     words 0 and 1 = the row's two canonical words of that K range, unchanged.
-//   8-bit integer types run widened to bf16 on kind::f16 and use its layout.
+//   kind::f8f6f4 (FP8 types, 64 dense K per MMA, two words per lane): lane = row, the
+//     MMA's two words = the row's two canonical words of that K range, unchanged; the
+//     lane's 8 words are thus the row's 8 canonical words of the stage in order.
+//   8-bit and 4-bit integer types run widened to bf16 on kind::f16 and use its layout.
 // The image covers M rounded up to a multiple of 256 and K to a multiple of the stage;
-// rows beyond M, words beyond K/32 and the unused words of each 16-byte row hold
-// 0x44444444 (pattern {0,1} in every group).  The matching values are zero, so they add
-// nothing.
+// rows beyond M and words beyond K/32 hold 0x44444444 (pattern {0,1} in every group).
+// The matching values are zero, so they add nothing.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -51,8 +52,7 @@ __device__ __forceinline__ uint4 canon4(const MetaArgs& a, int64_t row, int64_t 
 }
 
 // One thread per (tile, stage, lane): it reads the canonical words its lane needs and
-// writes the lane's 16-byte row of each of the stage's 4 MMA blocks (coalesced across the
-// lanes of a warp).
+// writes the lane's 16 (FP8: 32) bytes of the stage block, coalesced across a warp.
 template <bool kEightBit>
 __global__ void __launch_bounds__(256) meta_kernel(MetaArgs a) {
   griddep_launch_dependents();  // the GEMM after this pass may start its prologue
@@ -64,25 +64,23 @@ __global__ void __launch_bounds__(256) meta_kernel(MetaArgs a) {
     const int64_t mt = blk / a.ksteps, ks = blk % a.ksteps;
     if constexpr (kEightBit) {
       const int64_t row = mt * 128 + lane;
-      uint4* out = reinterpret_cast<uint4*>(a.meta) + blk * (kMmasPerStage * 128) + lane;
-      const uint4 c0 = canon4(a, row, ks * 8), c1 = canon4(a, row, ks * 8 + 4);
-      out[0 * 128] = make_uint4(c0.x, c0.y, kPadWord, kPadWord);
-      out[1 * 128] = make_uint4(c0.z, c0.w, kPadWord, kPadWord);
-      out[2 * 128] = make_uint4(c1.x, c1.y, kPadWord, kPadWord);
-      out[3 * 128] = make_uint4(c1.z, c1.w, kPadWord, kPadWord);
+      uint4* out = reinterpret_cast<uint4*>(a.meta) + (blk * 128 + lane) * 2;
+      out[0] = canon4(a, row, ks * 8);
+      out[1] = canon4(a, row, ks * 8 + 4);
     } else {
       const int band = lane >> 4, l = lane & 15;
       const int64_t rA = mt * 128 + band * 16 + (l & 7);
       const int h = l >> 3;
-      uint4* out = reinterpret_cast<uint4*>(a.meta) + blk * (kMmasPerStage * 128) + lane;
       const uint4 lo4 = canon4(a, rA, ks * 4), hi4 = canon4(a, rA + 8, ks * 4);
       const uint32_t lo[4] = {lo4.x, lo4.y, lo4.z, lo4.w}, hi[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
+      uint32_t w[kMmasPerStage];
 #pragma unroll
       for (int j = 0; j < kMmasPerStage; ++j) {  // MMA j reads canonical word ks * 4 + j
         const uint32_t l16 = (lo[j] >> (16 * h)) & 0xFFFFu;
         const uint32_t h16 = (hi[j] >> (16 * h)) & 0xFFFFu;
-        out[j * 128] = make_uint4(l16 | (h16 << 16), kPadWord, kPadWord, kPadWord);
+        w[j] = l16 | (h16 << 16);
       }
+      reinterpret_cast<uint4*>(a.meta)[blk * 128 + lane] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }

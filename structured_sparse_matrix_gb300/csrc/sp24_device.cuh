@@ -1,6 +1,6 @@
 // sp24_device.cuh -- inline-PTX building blocks for the sm_103a kernels of libsp24:
 // mbarriers with bounded waits, TMA (cp.async.bulk[.tensor]) loads, and the tcgen05
-// family (TMEM allocation, tcgen05.cp, tcgen05.mma.sp, tcgen05.commit, tcgen05.ld).
+// family (TMEM allocation, tcgen05.st, tcgen05.mma.sp, tcgen05.commit, tcgen05.ld).
 #pragma once
 
 #include <cstdint>
@@ -100,7 +100,7 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 // make this thread's generic-proxy shared-memory writes visible to the async proxy
-// (TMA, tcgen05.cp, tcgen05.mma read shared memory through it)
+// (TMA and tcgen05.mma read shared memory through it)
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -166,12 +166,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Copy a row-major [128 rows][16 bytes] block from shared memory into TMEM lanes
-// 0..127, four 32-bit columns starting at taddr (word q of a row -> column q).
-__device__ __forceinline__ void tc_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // One sparse MMA, cta_group::1: D[tmem] (+)= expand(A[smem], meta[tmem]) * B[smem].
@@ -276,10 +270,16 @@ __device__ __forceinline__ uint32_t mapa(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
   return r;
 }
-// arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA)
+// Arrive on an mbarrier given by its shared::cluster address (possibly in the peer CTA),
+// with the instruction's default semantics (release at CTA scope).  Every use follows
+// completed tensor-memory work of this thread (tcgen05.wait::st or ::ld) and a
+// tcgen05.fence::before_thread_sync, which orders that work before the arrive for the
+// thread that waits on the barrier and then issues tcgen05 operations.  A release at
+// cluster scope is not needed for that and was measured to stall: as the writers'
+// per-stage arrive it made the CTA-pair GEMM 1.7x slower (bf16 4096^3: 157 us against
+// 92 us).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // TMA 2-D load into this CTA's shared memory whose completion is counted on an mbarrier
 // of either CTA of the pair (.cta_group::2), given by its shared::cluster address.
@@ -311,10 +311,6 @@ __device__ __forceinline__ void tmem_relinquish_pair() {
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
-}
-// tcgen05.cp for the pair: each CTA's [128][16 B] shared block (same offset) -> its TMEM.
-__device__ __forceinline__ void tc_cp_128x128b_pair(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 // Sparse MMA across the CTA pair (M = 256: 128 rows of A and half of B's N in each CTA).
 template <bool kF8>

@@ -40,18 +40,21 @@ inline bool is_signed_int(int t) { return t == kS8 || t == kS4; }
 // C and D types of the float products: f32, or the 16-bit accumulators
 inline bool is_float_acc(int t) { return t == kF32 || t == kBF16 || t == kF16; }
 
-// ---- sparse-GEMM K-step geometry (one pipeline stage) shared by meta.cu and spmma.cu
+// ---- sparse-GEMM K-step geometry (one pipeline stage) shared by meta.cu, compress.cu
+// and spmma.cu.
 // 16-bit operands: 128 dense K per stage = 4 MMAs of K=32, metadata one TMEM column
 // per MMA; FP8 operands: 256 dense K per stage = 4 MMAs of K=64, two columns per MMA.
 // 8- and 4-bit integers run widened to bf16 on the 16-bit path, so they use its geometry.
 // In both cases a stage of compressed A is 128 rows x 128 bytes, and the stage's
-// metadata is one [128 lanes][4 words] block per MMA (the MMA's words first), the
-// source of one tcgen05.cp.128x128b into the MMA's column-aligned TMEM slot.
+// metadata is one block [128 TMEM lanes][W words] (W = 4 for 16-bit, 8 for FP8): lane
+// L's words for the stage's 4 MMAs in MMA order, which the GEMM's metadata writer warps
+// store into the MMAs' TMEM slots.  The image is therefore the size of the canonical
+// index (plus padding to whole tiles and stages).
 constexpr int kBM = 128;
 constexpr int kMmasPerStage = 4;
-constexpr int kMetaBlockBytes = kBM * 16;  // one [128][4-word] block = one tcgen05.cp
 inline int stage_k(int t) { return is_f8(t) ? 256 : 128; }
-inline int64_t meta_stage_bytes(int) { return int64_t(kMmasPerStage) * kMetaBlockBytes; }
+inline int meta_lane_words(int t) { return is_f8(t) ? 8 : 4; }
+inline int64_t meta_stage_bytes(int t) { return int64_t(kBM) * 4 * meta_lane_words(t); }
 // The image covers whole 256-row tile pairs (the CTA-pair GEMM loads both halves).
 inline int64_t meta_mtiles(int64_t M) { return 2 * ((M + 2 * kBM - 1) / (2 * kBM)); }
 

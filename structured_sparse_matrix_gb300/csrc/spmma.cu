@@ -21,13 +21,18 @@
 //   narrow  (N <= 32): one CTA per 128 x 32 tile (see Geo).
 // Warp roles (persistent over tiles, one CTA per SM):
 //   warp 0   TMA producer: per stage one box of compressed A (K-major, 128-byte swizzle),
-//            the B boxes (K x N row-major = MN-major, 128-byte swizzle) and the stage's
-//            8 KB of the metadata image (one [128 lanes][16 bytes] block per MMA).
-//   warp 1   TMEM owner and MMA issuer: per stage 4 x tcgen05.cp (metadata block -> its
-//            MMA's 16-column-aligned TMEM slot; slot set = ring stage), 4 x tcgen05.mma.sp
-//            and one tcgen05.commit that frees the stage.  The copies run in the same
-//            in-order tcgen05 pipe as the MMAs, so no thread touches the metadata.
-//   warps 2+ epilogue: tcgen05.ld, + C, cast to f32 / bf16, 16-byte stores.
+//            the B boxes (K x N row-major = MN-major, 128-byte swizzle) and this CTA's
+//            block of the metadata image (2 KB, FP8 4 KB: each TMEM lane's words for the
+//            stage's 4 MMAs), the block on a barrier of its own.
+//   warp 1   TMEM owner and MMA issuer: per stage 4 x tcgen05.mma.sp and one
+//            tcgen05.commit that frees the stage.
+//   warps 4+ epilogue: tcgen05.ld, + C, cast to f32 / bf16, 16-byte stores.
+//   last 4   metadata writers, one per quarter of the TMEM lanes: each stage's words go
+//            from the image block to the MMAs' 16-column-aligned TMEM slots (slot set =
+//            ring stage) by tcgen05.st.  Measured on the GB300 with operands resident in
+//            shared memory, a tcgen05.cp of the metadata in front of every MMA costs the
+//            tensor pipe about 44 cycles per MMA (bf16 M=128, N=256: 204 cycles against
+//            160), stores from other warps nothing measurable.
 // Every mbarrier wait is bounded; a wait that gives up sets SP24_DEV_TIMEOUT in the
 // caller's status word and the CTA drains its in-flight work and exits.
 #include <cuda.h>
@@ -71,6 +76,8 @@ struct MmaParams {
   int mtiles, ntiles, num_kb;  // tiles of the variant (128 or 256 rows, 128 or 256 cols)
   int batch;                   // problems of equal shape; problem b's C / D start at
   int64_t stride_c, stride_d;  // C + b * stride_c, D + b * stride_d (elements)
+  const uint8_t* meta;         // metadata image; problem b's at meta + b * stride_meta
+  int64_t stride_meta;         // (bytes)
   uint64_t limit_ns;
 };
 
@@ -84,7 +91,8 @@ struct Geo {
   static constexpr int kStageK = ESZ == 2 ? 128 : 256;       // dense K per stage
   static constexpr int kMmaK = ESZ == 2 ? 32 : 64;            // dense K per MMA
   static constexpr int kMmas = kStageK / kMmaK;               // 4
-  static constexpr int kMetaBytes = kMmas * kMetaBlockBytes;  // 8 KB per stage
+  static constexpr int kMetaWords = ESZ == 1 ? 8 : 4;        // per TMEM lane and stage
+  static constexpr int kMetaBytes = 128 * 4 * kMetaWords;     // image block: 2 / 4 KB
   static constexpr int kTileM = kPair ? 256 : 128;
   static constexpr int kTileN = kPair ? (kHalfN ? 128 : 256) : (kNarrow ? 32 : 128);
   static constexpr int kBCols = kPair ? kTileN / 2 : kTileN;  // B columns staged per CTA
@@ -95,13 +103,23 @@ struct Geo {
   static constexpr int kAtomBytes = kStageK * kAtomInner;     // one B box
   static constexpr int kBBytes = kAtoms * kAtomBytes;
   static constexpr int kStages = kNarrow ? 7 : 4;
-  static constexpr int kStageBytes = kABytes + kBBytes + kMetaBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes;  // the metadata skips shared memory
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
   static constexpr int kAccBufs = (kPair && !kHalfN) ? 1 : 2;
   static constexpr int kAccCols = kAccBufs * kTileN;
   static constexpr uint32_t kMetaCol = kAccCols;              // slot set s at + s * 64
+  // warps: 0 TMA producer, 1 MMA issuer, 2-3 idle, then the epilogue warps, then four
+  // metadata writers (warp id % 4 = the TMEM lane quarter each may access)
   static constexpr int kEpiWarps = kPair ? 8 : 4;
-  static constexpr int kThreads = 32 * (2 + kEpiWarps);       // 320 or 192
+  static constexpr int kEpiWarp0 = 4;
+  static constexpr int kWriterWarp0 = kEpiWarp0 + kEpiWarps;
+  static constexpr int kThreads = 32 * (kWriterWarp0 + 4);    // 512 or 384
+  // pair: 512 threads launch with 128 registers each; the producer / MMA warpgroup and
+  // the writer warpgroup give theirs down to kRegsLight so the two epilogue warpgroups
+  // can hold the drained accumulator (kRegsEpi); the shares add up to at most the launch's
+  static constexpr uint32_t kRegsLight = ESZ == 1 ? 56 : 48;  // FP8 writers hold 32 B/stage
+  static constexpr uint32_t kRegsEpi = ESZ == 1 ? 192 : 200;
+  static_assert(!kPair || (kRegsLight * 256 + kRegsEpi * 256 <= 65536u), "register split");
   static_assert(kAccCols + kStages * kMmas * kSlotCols <= int(kTmemCols), "TMEM budget");
   static_assert(kSmemBytes <= 232448 - 512, "shared memory budget");
   static_assert(kAtoms >= 1, "B atoms");
@@ -364,7 +382,8 @@ __device__ __forceinline__ void store_chunk_s32(const uint32_t* v, const MmaPara
 constexpr int kMaxGroup = 32;
 static_assert(kMaxGroup == kMaxGroupPerLaunch, "one group table per launch");
 struct GroupTable {
-  CUtensorMap a[kMaxGroup], b[kMaxGroup], m[kMaxGroup];
+  CUtensorMap a[kMaxGroup], b[kMaxGroup];
+  const uint8_t* meta[kMaxGroup];
   int count;
   int tile_start[kMaxGroup + 1];  // problem g owns launch tiles tile_start[g] .. [g+1]-1
   int M[kMaxGroup], N[kMaxGroup], K[kMaxGroup], num_kb[kMaxGroup];
@@ -413,6 +432,8 @@ __device__ __forceinline__ void problem_params(const MmaParams& p, const GroupTa
     q.d32 = gt->d32[g];
     q.batch = 1;
     q.stride_c = q.stride_d = 0;
+    q.meta = gt->meta[g];
+    q.stride_meta = 0;
   } else {
     (void)p, (void)gt, (void)g, (void)q;
   }
@@ -421,17 +442,20 @@ __device__ __forceinline__ void problem_params(const MmaParams& p, const GroupTa
 // OUT: 0 = f32 output, 1 = 16-bit float output (bf16 or f16 by p.d_f16), 2 = s32 output
 // (integer mode).  C (nullable) is f32, bf16 or f16 (p.ctype) for float outputs, s32 for
 // integer mode.
-// kGrouped: the tiles of the problems of a group table (tmA/tmB/tmM/idesc unused);
-// otherwise one problem, or a strided batch, with tensor maps tmA, tmB, tmM.
+// kGrouped: the tiles of the problems of a group table (tmA/tmB/idesc unused);
+// otherwise one problem, or a strided batch, with tensor maps tmA, tmB.
 template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN, bool kGrouped>
 __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                           const CUtensorMap* tmM, const MmaParams& p,
+                                           const MmaParams& p,
                                            const uint32_t idesc, const GroupTable* gt) {
   using G = Geo<ESZ, kPair, kNarrow, kHalfN>;
   constexpr int kStages = G::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
+  // meta_full (even CTA): every writer warp of the pair has stored the stage's metadata
+  // into its TMEM slots
+  __shared__ __align__(8) uint64_t meta_full[kStages];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -442,13 +466,13 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
   const int nunits = kPair ? int(gridDim.x >> 1) : int(gridDim.x);
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kABytes;
-  uint8_t* sM = sB + kStages * G::kBBytes;
   const int ntiles_total = kGrouped ? gt->tile_start[gt->count] : p.mtiles * p.ntiles * p.batch;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
+      mbar_init(&meta_full[s], 4 * (kPair ? 2 : 1));
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -462,7 +486,6 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
     if constexpr (!kGrouped) {
       prefetch_tmap(tmA);
       prefetch_tmap(tmB);
-      prefetch_tmap(tmM);
     }
   }
   if (warp == 1) {
@@ -484,6 +507,10 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
   // dependent launch); nothing below runs before that kernel's writes are visible
   griddep_wait();
 
+  // Roles by warpgroup (the pair variant re-divides the register file per warpgroup, so
+  // each role's code sits under its warpgroup's setmaxnreg)
+  if (warp < G::kEpiWarp0) {
+    if constexpr (kPair) regs_dec<G::kRegsLight>();
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -496,19 +523,16 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
         const MmaParams& pp = kGrouped ? qg : p;
         const CUtensorMap* mA = kGrouped ? &gt->a[g] : tmA;
         const CUtensorMap* mB = kGrouped ? &gt->b[g] : tmB;
-        const CUtensorMap* mM = kGrouped ? &gt->m[g] : tmM;
         int b, mt, nt;
         batch_tile<G::kTileM>(pp, lt, b, mt, nt);
         const int mt128 = kPair ? mt * 2 + int(rank) : mt;  // this CTA's 128-row tile
         const int bcol = nt * G::kTileN + int(rank) * G::kBCols;
-        const uint32_t tx =
-            uint32_t(kABytes + pp.batoms * G::kAtomBytes + G::kMetaBytes) * (kPair ? 2u : 1u);
+        const uint32_t tx = uint32_t(kABytes + pp.batoms * G::kAtomBytes) * (kPair ? 2u : 1u);
         for (int kb = 0; kb < pp.num_kb; ++kb, ++q) {
           const int s = q % kStages;
           if (!mbar_wait(&empty_bar[s], ((q / kStages) & 1) ^ 1u, abort, p.limit_ns)) break;
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], tx);
           const int kx = kb * (G::kStageK / 2);
-          const int mrow = (mt128 * pp.num_kb + kb) * (G::kMetaBytes / 128);
           if constexpr (kPair) {
             const uint32_t fb = mapa(&full_bar[s], 0);
             tma_load_3d_pair(sA + s * kABytes, mA, fb, kx, mt128 * 128, b);
@@ -517,7 +541,6 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
               if (a < pp.batoms)
                 tma_load_3d_pair(sB + s * G::kBBytes + a * G::kAtomBytes, mB, fb,
                                  bcol + a * G::kAtomN, kb * G::kStageK, b);
-            tma_load_3d_pair(sM + s * G::kMetaBytes, mM, fb, 0, mrow, b);
           } else {
             tma_load_3d(sA + s * kABytes, mA, &full_bar[s], kx, mt128 * 128, b);
 #pragma unroll
@@ -525,7 +548,6 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
               if (a < pp.batoms)
                 tma_load_3d(sB + s * G::kBBytes + a * G::kAtomBytes, mB, &full_bar[s],
                             bcol + a * G::kAtomN, kb * G::kStageK, b);
-            tma_load_3d(sM + s * G::kMetaBytes, mM, &full_bar[s], 0, mrow, b);
           }
         }
       }
@@ -541,7 +563,6 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
       const uint64_t adesc_hi = smem_desc_hi(16, 1024, 2);
       // B is MN-major: LBO = next atom along N, SBO = next 8 rows of K
       const uint64_t bdesc_hi = smem_desc_hi(G::kAtomBytes, 8 * G::kAtomInner, G::kSwzCode);
-      const uint64_t mdesc_hi = smem_desc_hi(0, 128, 0);
       int q = 0, local = 0, chunk = 0;
       for (int t = unit; t < ntiles_total && !*abort; t += nunits, ++local) {
         int lt;
@@ -575,21 +596,15 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
               d_tmem = tmem + uint32_t(abuf * G::kTileN);
             }
           }
-          if (!mbar_wait(&full_bar[s], par, abort, p.limit_ns)) {
+          // the stage's operands (both CTAs) and its metadata in the TMEM slots (stored
+          // by the writer warps of both CTAs)
+          if (!mbar_wait(&full_bar[s], par, abort, p.limit_ns) ||
+              !mbar_wait(&meta_full[s], par, abort, p.limit_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t e_tmem = tmem + G::kMetaCol + uint32_t(s * G::kMmas * kSlotCols);
-          const uint32_t p_saddr = smem_addr(sM + s * G::kMetaBytes);
-#pragma unroll
-          for (int j = 0; j < G::kMmas; ++j) {
-            const uint64_t md = smem_desc(p_saddr + j * kMetaBlockBytes, mdesc_hi);
-            if constexpr (kPair)
-              tc_cp_128x128b_pair(e_tmem + j * kSlotCols, md);
-            else
-              tc_cp_128x128b(e_tmem + j * kSlotCols, md);
-          }
           const uint32_t a_saddr = smem_addr(sA + s * kABytes);
           const uint32_t b_saddr = smem_addr(sB + s * G::kBBytes);
           const int k0 = kb * G::kStageK;
@@ -635,9 +650,113 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
         tc_commit(&drain_bar);
       mbar_wait_drain(&drain_bar, 0, 1000000000ull);
     }
+  }  // warps 2 and 3 have no role
+  } else if (warp >= G::kWriterWarp0) {
+    if constexpr (kPair) regs_dec<G::kRegsLight>();
+    // ---------------------------------------------------------------- metadata writers
+    // Warp w stores TMEM lanes 32 (w % 4) .. +31 of each stage's four metadata slots.  A
+    // lane's words for a stage (16 or 32 bytes of the image block) are loaded from global
+    // memory kAhead stages early into registers; once the MMAs that last read the slot
+    // set are done (empty_bar, the producer's barrier) the warp stores them with
+    // tcgen05.st, waits for the stores and arrives on the even CTA's meta_full, which the
+    // MMA issuer waits on before the stage's MMAs.
+    constexpr int kAhead = 4;                     // stages of metadata held in registers
+    constexpr int kVecs = G::kMetaWords / 4;      // 16-byte vectors per lane and stage
+    const int quad = warp & 3;
+    const int lrow = quad * 32 + lane;            // this thread's TMEM lane
+    const uint32_t meta_full_addr = kPair ? mapa(&meta_full[0], 0) : smem_addr(&meta_full[0]);
+    const uint32_t lanes = tmem + (uint32_t(quad * 32) << 16) + G::kMetaCol;
+    // a cursor over this CTA's stages in the producer's order: tile t, stage kb of num_kb,
+    // and the address of this lane's words of that stage
+    struct Cursor {
+      int t, kb, num_kb;
+      const uint4* src;
+    };
+    auto seek = [&](Cursor& c, int t) {  // first stage of tile t or a later one
+      for (c.t = t; c.t < ntiles_total; c.t += nunits) {
+        int lt;
+        const int g = tile_problem<kGrouped>(gt, c.t, lt);
+        MmaParams qg;
+        problem_params<kGrouped>(p, gt, g, qg);
+        const MmaParams& pp = kGrouped ? qg : p;
+        if (pp.num_kb == 0) continue;
+        int b, mt, nt;
+        batch_tile<G::kTileM>(pp, lt, b, mt, nt);
+        const int mt128 = kPair ? mt * 2 + int(rank) : mt;
+        c.kb = 0;
+        c.num_kb = pp.num_kb;
+        c.src = reinterpret_cast<const uint4*>(pp.meta + b * pp.stride_meta +
+                                               int64_t(mt128) * pp.num_kb * G::kMetaBytes) +
+                lrow * kVecs;
+        return;
+      }
+    };
+    auto next = [&](Cursor& c) {
+      c.src += G::kMetaBytes / 16;
+      if (++c.kb == c.num_kb) seek(c, c.t + nunits);
+    };
+    auto load = [&](const Cursor& c, uint4 (&v)[kVecs]) {
+      if (c.t < ntiles_total) {
+#pragma unroll
+        for (int i = 0; i < kVecs; ++i) v[i] = __ldg(c.src + i);
+      }
+    };
+    Cursor ld, wr;
+    seek(ld, unit);
+    wr = ld;
+    uint4 buf[kAhead][kVecs];
+#pragma unroll
+    for (int a = 0; a < kAhead; ++a) {
+      load(ld, buf[a]);
+      if (ld.t < ntiles_total) next(ld);
+    }
+    int q = 0;
+    bool ok = true;
+    while (ok && wr.t < ntiles_total) {
+#pragma unroll
+      for (int a = 0; a < kAhead; ++a) {
+        if (wr.t >= ntiles_total) break;
+        const int s = q % kStages;
+        int free_slot = 1;
+        if (lane == 0)
+          free_slot = mbar_wait(&empty_bar[s], ((q / kStages) & 1) ^ 1u, abort, p.limit_ns);
+        if (__shfl_sync(0xFFFFFFFFu, free_slot, 0) == 0) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t e = lanes + uint32_t(s * G::kMmas * kSlotCols);
+        if constexpr (ESZ == 2) {  // kind::f16: one column per MMA
+          tc_st_32x32b_x1(e, buf[a][0].x);
+          tc_st_32x32b_x1(e + kSlotCols, buf[a][0].y);
+          tc_st_32x32b_x1(e + 2 * kSlotCols, buf[a][0].z);
+          tc_st_32x32b_x1(e + 3 * kSlotCols, buf[a][0].w);
+        } else {  // kind::f8f6f4: two columns per MMA
+          tc_st_32x32b_x2(e, buf[a][0].x, buf[a][0].y);
+          tc_st_32x32b_x2(e + kSlotCols, buf[a][0].z, buf[a][0].w);
+          tc_st_32x32b_x2(e + 2 * kSlotCols, buf[a][kVecs - 1].x, buf[a][kVecs - 1].y);
+          tc_st_32x32b_x2(e + 3 * kSlotCols, buf[a][kVecs - 1].z, buf[a][kVecs - 1].w);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair)
+            mbar_arrive_cluster(meta_full_addr + uint32_t(s * sizeof(uint64_t)));
+          else
+            mbar_arrive(&meta_full[s]);
+        }
+        // refill this register slot with the stage kAhead further on
+        load(ld, buf[a]);
+        if (ld.t < ntiles_total) next(ld);
+        next(wr);
+        ++q;
+      }
+    }
   } else {
+    if constexpr (kPair) regs_inc<G::kRegsEpi>();
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - 2;
+    const int ew = warp - G::kEpiWarp0;
     const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 (hardware rule: warp id % 4)
     const uint32_t acc_empty_addr =
         kPair ? mapa(&acc_empty[0], 0) : smem_addr(&acc_empty[0]);
@@ -794,9 +913,9 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
 template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN>
 __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
     spmma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmM, const __grid_constant__ MmaParams p,
+                 const __grid_constant__ MmaParams p,
                  const uint32_t idesc) {
-  spmma_body<ESZ, OUT, kPair, kNarrow, kHalfN, false>(&tmA, &tmB, &tmM, p, idesc, nullptr);
+  spmma_body<ESZ, OUT, kPair, kNarrow, kHalfN, false>(&tmA, &tmB, p, idesc, nullptr);
 }
 
 // The problems of a group table, one persistent grid over all their tiles.
@@ -804,7 +923,7 @@ template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN>
 __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
     spmma_grouped_kernel(const __grid_constant__ MmaParams p,
                          const __grid_constant__ GroupTable gt) {
-  spmma_body<ESZ, OUT, kPair, kNarrow, kHalfN, true>(nullptr, nullptr, nullptr, p, 0u, &gt);
+  spmma_body<ESZ, OUT, kPair, kNarrow, kHalfN, true>(nullptr, nullptr, p, 0u, &gt);
 }
 
 // ------------------------------------------------------------------ host side
@@ -843,6 +962,16 @@ bool make_tmap(CUtensorMap* m, const void* base, int esz, uint64_t cols, uint64_
   return r == CUDA_SUCCESS;
 }
 
+// The pair variant re-divides its registers with setmaxnreg, whose increase waits until
+// the warpgroups' shares fit in what the block was launched with: refuse to launch a build
+// whose register count would leave that wait unsatisfiable.
+template <typename G, typename Kern>
+bool register_split_fits(Kern kern) {
+  cudaFuncAttributes fa;
+  return cudaFuncGetAttributes(&fa, kern) == cudaSuccess &&
+         uint64_t(fa.numRegs) * G::kThreads >= uint64_t(G::kRegsLight + G::kRegsEpi) * 256;
+}
+
 // Per-problem strides of the operands of a batched call (bytes).
 struct BatchStrides {
   int64_t values, meta, b;
@@ -854,10 +983,11 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
   using G = Geo<ESZ, kPair, kNarrow, kHalfN>;
   p.mtiles = (p.M + G::kTileM - 1) / G::kTileM;
   p.ntiles = (p.N + G::kTileN - 1) / G::kTileN;
-  CUtensorMap tA, tB, tM;
+  CUtensorMap tA, tB;
   memset(&tA, 0, sizeof(tA));
   memset(&tB, 0, sizeof(tB));
-  memset(&tM, 0, sizeof(tM));
+  p.meta = static_cast<const uint8_t*>(meta);
+  p.stride_meta = bs.meta;
   if (p.K > 0) {  // with K == 0 no stage is loaded and the maps are never read
     const uint64_t nb = uint64_t(p.batch);
     if (!make_tmap(&tA, values, ESZ, uint64_t(p.K / 2), uint64_t(p.M), uint64_t(ldv) * ESZ,
@@ -867,15 +997,12 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
                    G::kStageK, kNarrow ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B,
                    nb, uint64_t(bs.b)))
       return 4;
-    // the compact metadata image as rows of 128 bytes; one (tile, stage) block per box
-    const uint64_t mrows = uint64_t(meta_mtiles(p.M)) * p.num_kb * (G::kMetaBytes / 128);
-    if (!make_tmap(&tM, meta, 4, 32, mrows, 128, 32, G::kMetaBytes / 128,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, nb, uint64_t(bs.meta)))
-      return 4;
   }
   // the narrow variant loads only the B atoms that hold columns below N
   p.batoms = kNarrow ? (p.N + G::kAtomN - 1) / G::kAtomN : G::kAtoms;
   auto kern = spmma_kernel<ESZ, OUT, kPair, kNarrow, kHalfN>;
+  if constexpr (kPair)
+    if (!register_split_fits<G>(kern)) return 4;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) !=
       cudaSuccess)
     return 4;
@@ -907,7 +1034,7 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
   }
   if (tiles < units) units = tiles;
   cfg.gridDim = dim3(units * (kPair ? 2 : 1), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tM, p, idesc) != cudaSuccess) return 4;
+  if (cudaLaunchKernelEx(&cfg, kern, tA, tB, p, idesc) != cudaSuccess) return 4;
   return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
@@ -971,6 +1098,7 @@ int run_grouped(MmaParams p, const sp24_mma_problem* pr, int count, uint32_t at,
                           : idesc_sparse_f32(at, bt, kPair ? 256 : 128, uint32_t(G::kTileN));
     gt.C[g] = q.C;
     gt.D[g] = q.D;
+    gt.meta[g] = static_cast<const uint8_t*>(q.meta);
     gt.ldc[g] = q.ldc;
     gt.ldd[g] = q.ldd;
     gt.c32[g] = (reinterpret_cast<uintptr_t>(q.C) % 32 == 0 && (q.ldc * 4) % 32 == 0) ? 1 : 0;
@@ -980,10 +1108,7 @@ int run_grouped(MmaParams p, const sp24_mma_problem* pr, int count, uint32_t at,
                      uint64_t(q.ldv) * ESZ, 128 / ESZ, 128, CU_TENSOR_MAP_SWIZZLE_128B, 1, 0) ||
           !make_tmap(&gt.b[g], q.B, ESZ, uint64_t(N), uint64_t(K), uint64_t(q.ldb) * ESZ,
                      G::kAtomN, G::kStageK,
-                     kNarrow ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B, 1, 0) ||
-          !make_tmap(&gt.m[g], q.meta, 4, 32,
-                     uint64_t(meta_mtiles(M)) * gt.num_kb[g] * (G::kMetaBytes / 128), 128, 32,
-                     G::kMetaBytes / 128, CU_TENSOR_MAP_SWIZZLE_NONE, 1, 0))
+                     kNarrow ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B, 1, 0))
         return 4;
     }
     gt.tile_start[g] = tiles;
@@ -991,6 +1116,8 @@ int run_grouped(MmaParams p, const sp24_mma_problem* pr, int count, uint32_t at,
   }
   gt.tile_start[count] = tiles;
   auto kern = spmma_grouped_kernel<ESZ, OUT, kPair, kNarrow, kHalfN>;
+  if constexpr (kPair)
+    if (!register_split_fits<G>(kern)) return 4;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes) !=
       cudaSuccess)
     return 4;

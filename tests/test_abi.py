@@ -51,14 +51,15 @@ def test_version_and_status_strings():
 
 def test_meta_bytes_host_only():
     L = sp.lib()
-    # 8 KiB per (128-row tile, stage): four [128][16-byte] blocks, one per MMA; a stage
-    # is 128 dense K for 16-bit types and 256 for 8-bit types; M rounds up to 256 rows
-    assert L.sp24_meta_bytes(BF16, 4096, 4096) == 32 * 32 * 8192
-    assert L.sp24_meta_bytes(F16, 64, 128) == 2 * 8192
-    assert L.sp24_meta_bytes(F16, 129, 160) == 2 * 2 * 8192
-    assert L.sp24_meta_bytes(E4M3, 8192, 8192) == 64 * 32 * 8192
+    # per (128-row tile, stage) one [128 lanes][W words] block: W = 4 (2 KiB) for 16-bit
+    # types with 128 dense K per stage, W = 8 (4 KiB) for FP8 with 256; M rounds up to
+    # 256 rows, so for whole tiles and stages the image is M x K / 8 bytes
+    assert L.sp24_meta_bytes(BF16, 4096, 4096) == 32 * 32 * 2048 == 4096 * 4096 // 8
+    assert L.sp24_meta_bytes(F16, 64, 128) == 2 * 2048
+    assert L.sp24_meta_bytes(F16, 129, 160) == 2 * 2 * 2048
+    assert L.sp24_meta_bytes(E4M3, 8192, 8192) == 64 * 32 * 4096 == 8192 * 8192 // 8
     # 8-bit integers use the 16-bit layout (their product runs on the bf16 path)
-    assert L.sp24_meta_bytes(S8, 8192, 8192) == 64 * 64 * 8192
+    assert L.sp24_meta_bytes(S8, 8192, 8192) == 64 * 64 * 2048
     assert L.sp24_meta_bytes(F16, 64, 100) == 0      # K % 32 != 0
     assert L.sp24_meta_bytes(F32, 64, 128) == 0      # not an operand type
 
@@ -170,7 +171,7 @@ def test_four_bit_argument_checks():
     L = sp.lib()
     # the 16-bit metadata layout (the product runs widened to bf16)
     assert L.sp24_meta_bytes(S4, 4096, 4096) == L.sp24_meta_bytes(BF16, 4096, 4096)
-    assert L.sp24_meta_bytes(U4, 129, 160) == 2 * 2 * 8192
+    assert L.sp24_meta_bytes(U4, 129, 160) == 2 * 2 * 2048
     # pitches count elements: lda = 144 is 72 bytes, ldv = 80 is 40 bytes
     assert _compress(t=S4, lda=144) == ALIGN
     assert _compress(t=U4, ldv=80) == ALIGN

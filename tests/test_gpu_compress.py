@@ -130,9 +130,10 @@ def test_empty_inputs_are_no_ops():
 # --- metadata image: checked against an independent restatement of the documented layout
 
 def _meta_image_np(index: np.ndarray, M: int, K: int, eight_bit: bool) -> np.ndarray:
-    """Image layout: per (128-row tile, stage, MMA j) one [128 lanes][4 words] block with
-    the MMA's words first (16-bit: one interleaved word; 8-bit: the row's two canonical
-    words) and 0x44444444 elsewhere; the tiles cover M rounded up to 256 rows."""
+    """Image layout: per (128-row tile, stage) one [128 lanes][W words] block holding each
+    lane's words for the stage's 4 MMAs in MMA order (16-bit: one interleaved word per MMA,
+    W = 4; FP8: the MMA's two canonical words, so a lane holds its row's 8 words of the
+    stage, W = 8); the tiles cover M rounded up to 256 rows, padding is 0x44444444."""
     stage = 256 if eight_bit else 128
     mt, ks = 2 * -(-M // 256), -(-K // stage)
     canon = np.full((mt * 128, ks * stage // 32), 0x44444444, dtype=np.uint64)
@@ -140,12 +141,11 @@ def _meta_image_np(index: np.ndarray, M: int, K: int, eight_bit: bool) -> np.nda
     out = []
     for t in range(mt):
         for s in range(ks):
-            for j in range(4):
-                blk = np.full((128, 4), 0x44444444, dtype=np.uint64)
-                if eight_bit:
-                    blk[:, 0] = canon[t * 128:(t + 1) * 128, s * 8 + 2 * j]
-                    blk[:, 1] = canon[t * 128:(t + 1) * 128, s * 8 + 2 * j + 1]
-                else:
+            if eight_bit:
+                blk = canon[t * 128:(t + 1) * 128, s * 8:s * 8 + 8]
+            else:
+                blk = np.zeros((128, 4), dtype=np.uint64)
+                for j in range(4):
                     w = s * 4 + j
                     for lane in range(128):
                         band, l = divmod(lane, 16)
@@ -153,8 +153,8 @@ def _meta_image_np(index: np.ndarray, M: int, K: int, eight_bit: bool) -> np.nda
                         h = l // 8
                         lo = (int(canon[rA, w]) >> (16 * h)) & 0xFFFF
                         hi = (int(canon[rA + 8, w]) >> (16 * h)) & 0xFFFF
-                        blk[lane, 0] = lo | (hi << 16)
-                out.append(blk.reshape(-1))
+                        blk[lane, j] = lo | (hi << 16)
+            out.append(np.asarray(blk).reshape(-1))
     return np.concatenate(out).astype(np.uint32)
 
 
