@@ -20,16 +20,15 @@
 //           next.
 //   narrow  (N <= 32): one CTA per 128 x 32 tile (see Geo).
 // Warp roles (persistent over tiles, one CTA per SM):
-//   warp 0   TMA producer: per stage one box of compressed A (K-major, 128-byte swizzle),
-//            the B boxes (K x N row-major = MN-major, 128-byte swizzle) and this CTA's
-//            block of the metadata image (2 KB, FP8 4 KB: each TMEM lane's words for the
-//            stage's 4 MMAs), the block on a barrier of its own.
+//   warp 0   TMA producer: per stage one box of compressed A (K-major, 128-byte swizzle)
+//            and the B boxes (K x N row-major = MN-major, 128-byte swizzle).
 //   warp 1   TMEM owner and MMA issuer: per stage 4 x tcgen05.mma.sp and one
 //            tcgen05.commit that frees the stage.
 //   warps 4+ epilogue: tcgen05.ld, + C, cast to f32 / bf16, 16-byte stores.
-//   last 4   metadata writers, one per quarter of the TMEM lanes: each stage's words go
-//            from the image block to the MMAs' 16-column-aligned TMEM slots (slot set =
-//            ring stage) by tcgen05.st.  Measured on the GB300 with operands resident in
+//   last 4   metadata writers, one per quarter of the TMEM lanes: each lane's words of a
+//            stage (16 bytes, FP8 32, of the image block) are loaded from global memory a
+//            few stages ahead and stored into the MMAs' 16-column-aligned TMEM slots (slot
+//            set = ring stage) by tcgen05.st.  Measured on the GB300 with operands resident in
 //            shared memory, a tcgen05.cp of the metadata in front of every MMA costs the
 //            tensor pipe about 44 cycles per MMA (bf16 M=128, N=256: 204 cycles against
 //            160), stores from other warps nothing measurable.
@@ -377,7 +376,7 @@ __device__ __forceinline__ void store_chunk_s32(const uint32_t* v, const MmaPara
 
 // A grouped launch: up to kMaxGroup problems of different shapes (same element types)
 // whose tiles share one persistent grid.  Everything the kernel reads per problem, tensor
-// maps included, travels in kernel parameter space (about 15 KB), so the launch needs no
+// maps included, travels in kernel parameter space (about 11 KB), so the launch needs no
 // device memory of its own.
 constexpr int kMaxGroup = 32;
 static_assert(kMaxGroup == kMaxGroupPerLaunch, "one group table per launch");
