@@ -311,9 +311,10 @@ def gpu_arm(args, world, rank, local):
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
 
     fused = args.pass_mode == "fused"
+    by_index = args.pass_mode == "index"  # the product reads the canonical index: no image
     # kernels one step launches: compression (+ re-layout), the product (+ two widening
     # passes for integer operands)
-    launches_per_step = (1 if fused else 2) + (3 if integer else 1)
+    launches_per_step = (1 if fused or by_index else 2) + (3 if integer else 1)
 
     def compress_call(s, st):
         m = s["mask"]
@@ -325,10 +326,17 @@ def gpu_arm(args, world, rank, local):
         rc = L.sp24_compress(cs["ta"], M, K, sp._ptr(s["A"]), K, sp._ptr(m), K,
                              sp.MODES[mode], sp._ptr(s["values"]), K // 2,
                              sp._ptr(s["index"]), K // 32, sp._ptr(status), st)
+        if by_index:
+            return rc
         return rc | L.sp24_meta_prepare(cs["ta"], M, K, sp._ptr(s["index"]), K // 32,
                                         sp._ptr(s["meta"]), st)
 
     def product_call(s, st):
+        if by_index:
+            return L.sp24_mma_index(cs["ta"], cs["tb"], cs["tc"], cs["td"], M, N, K,
+                                    sp._ptr(s["values"]), K // 2, sp._ptr(s["index"]), K // 32,
+                                    sp._ptr(s["B"]), N, sp._ptr(s["C"]), N, sp._ptr(s["D"]), N,
+                                    sp._ptr(ws), ws_bytes, sp._ptr(status), st)
         return L.sp24_mma(cs["ta"], cs["tb"], cs["tc"], cs["td"], M, N, K, sp._ptr(s["values"]),
                           K // 2, sp._ptr(s["meta"]), sp._ptr(s["B"]), N, sp._ptr(s["C"]), N,
                           sp._ptr(s["D"]), N, sp._ptr(ws), ws_bytes, sp._ptr(status), st)
@@ -382,13 +390,12 @@ def gpu_arm(args, world, rank, local):
                                  sp._ptr(s["index"]), K // 32, sp._ptr(status), st)
             if ev is not None:
                 ev[1].record(stream)
-            rc |= L.sp24_meta_prepare(cs["ta"], M, K, sp._ptr(s["index"]), K // 32,
-                                      sp._ptr(s["meta"]), st)
+            if not by_index:
+                rc |= L.sp24_meta_prepare(cs["ta"], M, K, sp._ptr(s["index"]), K // 32,
+                                          sp._ptr(s["meta"]), st)
         if ev is not None:
             ev[2].record(stream)
-        rc |= L.sp24_mma(cs["ta"], cs["tb"], cs["tc"], cs["td"], M, N, K, sp._ptr(s["values"]),
-                         K // 2, sp._ptr(s["meta"]), sp._ptr(s["B"]), N, sp._ptr(s["C"]), N,
-                         sp._ptr(s["D"]), N, sp._ptr(ws), ws_bytes, sp._ptr(status), st)
+        rc |= product_call(s, st)
         if ev is not None:
             ev[3].record(stream)
         if rc != 0:
@@ -537,7 +544,8 @@ def gpu_arm(args, world, rank, local):
     else:
         kernels["sp24_compress_us"] = k_compress * 1e3
         kernels["sp24_compress_gbs"] = cbytes / (k_compress * 1e-3) / 1e9
-        kernels["sp24_meta_prepare_us"] = k_meta * 1e3
+        if not by_index:
+            kernels["sp24_meta_prepare_us"] = k_meta * 1e3
 
     # --- end to end through the C ABI with host buffers: every step copies its inputs from
     # pinned host memory, runs the calls and reads its result back.  Two device buffer
@@ -615,6 +623,7 @@ def gpu_arm(args, world, rank, local):
             "dtype": ta, "data": "synthetic",
             "config": {"workload": desc, "name": args.config, "M": M, "N": N, "K": K,
                        "step": (f"sp24_compress_meta({mode}) + sp24_mma" if fused else
+                                f"sp24_compress({mode}) + sp24_mma_index" if by_index else
                                 f"sp24_compress({mode}) + sp24_meta_prepare + sp24_mma"),
                        "l2": f"{len(sets)} rotating input sets, "
                              f"{len(sets) * set_bytes(sets[0]) / 2**20:.0f} MiB > L2",
@@ -650,8 +659,10 @@ def main():
                          "i+1's compression runs on its own stream during step i's product)")
     ap.add_argument("--eager", action="store_true",
                     help="launch the timed steps one by one instead of as a CUDA graph")
-    ap.add_argument("--pass", dest="pass_mode", default="fused", choices=["fused", "separate"],
-                    help="compression and metadata image in one kernel (fused) or two")
+    ap.add_argument("--pass", dest="pass_mode", default="fused",
+                    choices=["fused", "separate", "index"],
+                    help="compression and metadata image in one kernel (fused), in two "
+                         "(separate), or no image: the product reads the canonical index")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     try:

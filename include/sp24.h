@@ -212,6 +212,22 @@ sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
                      size_t workspace_bytes, int32_t *d_status, void *stream);
 
 /*
+ * sp24_mma_index -- sp24_mma with the sparsity metadata read from the canonical index
+ * itself (as sp24_compress writes it: M x K/32 words, group g of row i in bits
+ * 4(g%8)..+3 of word g/8, nibble = p0 | p1 << 2, "Structured sparsity (2:4 pattern)")
+ * instead of the image: no sp24_meta_prepare pass and no image buffer.  The kernel's
+ * writer warps permute the words into tensor memory themselves.  Results are bit-identical
+ * to sp24_mma on sp24_meta_prepare(index).
+ * index : device, M x K/32 words, ldi >= K/32, 4-byte aligned (any pitch).
+ * Every other argument, type combination and rule as in sp24_mma.
+ */
+sp24_status sp24_mma_index(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
+                           int64_t M, int64_t N, int64_t K, const void *values, int64_t ldv,
+                           const uint32_t *index, int64_t ldi, const void *B, int64_t ldb,
+                           const void *C, int64_t ldc, void *D, int64_t ldd, void *workspace,
+                           size_t workspace_bytes, int32_t *d_status, void *stream);
+
+/*
  * sp24_diag_wait_timeout -- self-test of the bounded waits every kernel uses.  Launches
  * one thread that waits on a barrier nothing ever arrives at; after limit_ns nanoseconds
  * the wait gives up and SP24_DEV_TIMEOUT is OR-ed into *d_status (device, 4 bytes).  The

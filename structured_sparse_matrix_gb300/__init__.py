@@ -26,7 +26,7 @@ import torch
 from . import _build
 
 __all__ = ["lib", "compress", "compress_meta", "decompress", "meta_bytes", "meta_prepare", "mma",
-           "mma_batched", "mma_grouped",
+           "mma_index", "mma_batched", "mma_grouped",
            "workspace_bytes",
            "SparseMatrix", "Sp24Error", "DEV_NOT_2_4", "DEV_TIMEOUT", "DTYPE_CODES"]
 
@@ -44,7 +44,8 @@ DEV_TIMEOUT = 2
 
 # every symbol include/sp24.h declares
 EXPORTS = ("sp24_compress", "sp24_compress_meta", "sp24_decompress", "sp24_meta_bytes", "sp24_meta_prepare",
-           "sp24_mma_workspace_bytes", "sp24_mma", "sp24_mma_strided_batched", "sp24_mma_grouped",
+           "sp24_mma_workspace_bytes", "sp24_mma", "sp24_mma_index", "sp24_mma_strided_batched",
+           "sp24_mma_grouped",
            "sp24_mma_i8_noalloc",
            "sp24_diag_wait_timeout", "sp24_status_string", "sp24_version")
 
@@ -96,6 +97,9 @@ def lib():
             L.sp24_mma.restype = i32
             L.sp24_mma.argtypes = [i32, i32, i32, i32, i64, i64, i64, p, i64, p, p, i64, p, i64,
                                    p, i64, p, ctypes.c_size_t, p, p]
+            L.sp24_mma_index.restype = i32
+            L.sp24_mma_index.argtypes = [i32, i32, i32, i32, i64, i64, i64, p, i64, p, i64, p,
+                                         i64, p, i64, p, i64, p, ctypes.c_size_t, p, p]
             L.sp24_mma_strided_batched.restype = i32
             L.sp24_mma_strided_batched.argtypes = [i32, i32, i32, i32, i64, i64, i64, i64, p, i64,
                                                    i64, p, i64, p, i64, i64, p, i64, i64, p,
@@ -254,6 +258,21 @@ def mma(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor, C: torch.Tens
     Float operands give f32 (default) or bf16 output; integer operands give int32.
     a_elem / b_elem = "s4" / "u4": that operand is packed 4-bit (values M x K/4 bytes,
     B K x N/2 bytes)."""
+    return _mma("sp24_mma", values, (_ptr(meta),), B, C, out_dtype, out, workspace, status,
+                stream, a_elem, b_elem)
+
+
+def mma_index(values: torch.Tensor, index: torch.Tensor, B: torch.Tensor,
+              C: torch.Tensor | None = None, out_dtype=None, out: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+              stream=None, a_elem: str | None = None, b_elem: str | None = None) -> torch.Tensor:
+    """mma() with the metadata read from the canonical index (M x K/32 int32, as compress()
+    returns it) instead of the image; no meta_prepare pass."""
+    return _mma("sp24_mma_index", values, (_ptr(index), _ld(index)), B, C, out_dtype, out,
+                workspace, status, stream, a_elem, b_elem)
+
+
+def _mma(fn, values, meta_args, B, C, out_dtype, out, workspace, status, stream, a_elem, b_elem):
     ta, tb = _elem_code(values, a_elem), _elem_code(B, b_elem)
     M = values.shape[0]
     K, N = B.shape[0], B.shape[1] * (2 if b_elem in PACKED4 else 1)
@@ -266,9 +285,9 @@ def mma(values: torch.Tensor, meta: torch.Tensor, B: torch.Tensor, C: torch.Tens
     ws_bytes = int(lib().sp24_mma_workspace_bytes(ta, tb, M, N, K))
     if ws_bytes and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=B.device)
-    _check("sp24_mma", lib().sp24_mma(
+    _check(fn, getattr(lib(), fn)(
         ta, tb, tc, _code(out.dtype), M, N, K,
-        _ptr(values), _ld(values, a_elem), _ptr(meta), _ptr(B), _ld(B, b_elem), _ptr(C),
+        _ptr(values), _ld(values, a_elem), *meta_args, _ptr(B), _ld(B, b_elem), _ptr(C),
         _ld(C) if C is not None else N, _ptr(out), _ld(out), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(),
         _ptr(status), _stream(stream)))

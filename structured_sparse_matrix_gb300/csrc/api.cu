@@ -212,11 +212,16 @@ size_t sp24_mma_workspace_bytes(sp24_dtype ta, sp24_dtype tb, int64_t M, int64_t
   return 0;
 }
 
-sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td, int64_t M,
-                     int64_t N, int64_t K, const void* values, int64_t ldv, const void* meta,
-                     const void* B, int64_t ldb, const void* C, int64_t ldc, void* D,
-                     int64_t ldd, void* workspace, size_t workspace_bytes, int32_t* d_status,
-                     void* stream) {
+namespace {
+
+// sp24_mma and sp24_mma_index: the product with the metadata from the image (meta) or
+// from the canonical index (index != nullptr, pitch ldi words)
+sp24_status mma_one(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td, int64_t M,
+                    int64_t N, int64_t K, const void* values, int64_t ldv, const void* meta,
+                    const uint32_t* index, int64_t ldi, const void* B, int64_t ldb,
+                    const void* C, int64_t ldc, void* D, int64_t ldd, void* workspace,
+                    size_t workspace_bytes, int32_t* d_status, void* stream) {
+  const bool by_index = meta == nullptr;  // sp24_mma_index passes meta == nullptr
   const bool f16ish = (ta == SP24_F16 || ta == SP24_BF16);
   const bool f8 = is_f8(ta);
   const bool integer = is_int(ta);
@@ -238,22 +243,47 @@ sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
   if (M < 0 || N < 0 || K < 0 || (K % 32) != 0) return SP24_ERR_INVALID_ARG;
   if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return SP24_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return SP24_OK;
-  if (!D || (K > 0 && (!values || !meta || !B))) return SP24_ERR_INVALID_ARG;
+  if (!D || (K > 0 && (!values || !B || (by_index ? !index : !meta))))
+    return SP24_ERR_INVALID_ARG;
   if (ldd < N || (C && ldc < N) || (K > 0 && (ldv < K / 2 || ldb < N))) return SP24_ERR_INVALID_ARG;
+  if (by_index && K > 0 && ldi < K / 32) return SP24_ERR_INVALID_ARG;
   if (integer && K > 0 && (!workspace || workspace_bytes < int_workspace_bytes(M, N, K)))
     return SP24_ERR_INVALID_ARG;
   const int dsz = dtype_bytes(td);
   if (!aligned16(D) || (ldd * dsz) % 16) return SP24_ERR_ALIGN;
   if (C && (!aligned16(C) || (ldc * dtype_bytes(tc)) % 16)) return SP24_ERR_ALIGN;
-  if (K > 0 && (!aligned16(values) || !aligned16(meta) || !aligned16(B) || !ld_ok16(ta, ldv) ||
-                !ld_ok16(tb, ldb)))
+  if (K > 0 && (!aligned16(values) || !aligned16(B) || !ld_ok16(ta, ldv) || !ld_ok16(tb, ldb)))
+    return SP24_ERR_ALIGN;
+  if (K > 0 && (by_index ? (reinterpret_cast<uintptr_t>(index) & 3u) != 0 : !aligned16(meta)))
     return SP24_ERR_ALIGN;
   if (integer && K > 0 && !aligned16(workspace)) return SP24_ERR_ALIGN;
   int sms = 0;
   if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
-  const int rc = launch_spmma(ta, tb, tc, td, M, N, K, values, ldv, meta, B, ldb, C, ldc, D, ldd,
-                              workspace, d_status, sms, static_cast<cudaStream_t>(stream));
+  const int rc = launch_spmma(ta, tb, tc, td, M, N, K, values, ldv, by_index ? nullptr : meta, B,
+                              ldb, C, ldc, D, ldd, workspace, d_status, sms,
+                              static_cast<cudaStream_t>(stream), nullptr,
+                              (by_index && K > 0) ? index : nullptr, ldi);
   return static_cast<sp24_status>(rc);
+}
+
+}  // namespace
+
+sp24_status sp24_mma(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td, int64_t M,
+                     int64_t N, int64_t K, const void* values, int64_t ldv, const void* meta,
+                     const void* B, int64_t ldb, const void* C, int64_t ldc, void* D,
+                     int64_t ldd, void* workspace, size_t workspace_bytes, int32_t* d_status,
+                     void* stream) {
+  return mma_one(ta, tb, tc, td, M, N, K, values, ldv, meta, nullptr, 0, B, ldb, C, ldc, D, ldd,
+                 workspace, workspace_bytes, d_status, stream);
+}
+
+sp24_status sp24_mma_index(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
+                           int64_t M, int64_t N, int64_t K, const void* values, int64_t ldv,
+                           const uint32_t* index, int64_t ldi, const void* B, int64_t ldb,
+                           const void* C, int64_t ldc, void* D, int64_t ldd, void* workspace,
+                           size_t workspace_bytes, int32_t* d_status, void* stream) {
+  return mma_one(ta, tb, tc, td, M, N, K, values, ldv, nullptr, index, ldi, B, ldb, C, ldc, D,
+                 ldd, workspace, workspace_bytes, d_status, stream);
 }
 
 sp24_status sp24_mma_strided_batched(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc,

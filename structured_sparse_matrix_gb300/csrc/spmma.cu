@@ -43,6 +43,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/sp24.h"
 #include "sp24_device.cuh"
@@ -54,6 +55,7 @@ namespace {
 constexpr uint32_t kTmemCols = 512;
 constexpr int kABytes = 128 * 128;  // one stage of compressed A: 128 rows x 128 bytes
 constexpr int kSlotCols = 16;       // TMEM columns per MMA metadata slot (aligned)
+constexpr uint32_t kPadWord = 0x44444444u;  // pattern {0,1} in every group: rows / K past A
 // Integer mode: integers widened to bf16 are exact, and the f32 accumulator holds an exact
 // integer as long as every partial sum stays within 2^24.  A chunk of MmaParams::chunk
 // stages (128 dense K each, half of them kept products) is sized for that: s8 x s8
@@ -77,6 +79,8 @@ struct MmaParams {
   int64_t stride_c, stride_d;  // C + b * stride_c, D + b * stride_d (elements)
   const uint8_t* meta;         // metadata image; problem b's at meta + b * stride_meta
   int64_t stride_meta;         // (bytes)
+  const uint32_t* index;       // or, for one problem, the canonical index itself (M x K/32
+  int64_t ldi;                 // words, pitch ldi); then meta is unused
   uint64_t limit_ns;
 };
 
@@ -654,21 +658,25 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
     if constexpr (kPair) regs_dec<G::kRegsLight>();
     // ---------------------------------------------------------------- metadata writers
     // Warp w stores TMEM lanes 32 (w % 4) .. +31 of each stage's four metadata slots.  A
-    // lane's words for a stage (16 or 32 bytes of the image block) are loaded from global
-    // memory kAhead stages early into registers; once the MMAs that last read the slot
-    // set are done (empty_bar, the producer's barrier) the warp stores them with
-    // tcgen05.st, waits for the stores and arrives on the even CTA's meta_full, which the
-    // MMA issuer waits on before the stage's MMAs.
-    constexpr int kAhead = 4;                     // stages of metadata held in registers
-    constexpr int kVecs = G::kMetaWords / 4;      // 16-byte vectors per lane and stage
+    // lane's words for a stage are loaded from global memory a few stages early into
+    // registers: 16 (FP8: 32) bytes of the image block, or, reading the canonical index
+    // directly, the canonical words they are made of (16-bit layout: 4 words of each of the
+    // lane's two rows, combined by halves at store time; FP8: the row's 8 words).  Once the
+    // MMAs that last read the slot set are done (empty_bar, the producer's barrier) the
+    // warp stores them with tcgen05.st, waits for the stores and arrives on the even CTA's
+    // meta_full, which the MMA issuer waits on before the stage's MMAs.
     const int quad = warp & 3;
     const int lrow = quad * 32 + lane;            // this thread's TMEM lane
+    // kind::f16 layout: TMEM lane 16b + l holds halves h = l / 8 of rows 16b + l % 8 and
+    // 16b + l % 8 + 8 of the tile
+    const int h16 = (lrow >> 3) & 1;
+    const int r16 = (lrow & ~15) + (lrow & 7);
     const uint32_t meta_full_addr = kPair ? mapa(&meta_full[0], 0) : smem_addr(&meta_full[0]);
     const uint32_t lanes = tmem + (uint32_t(quad * 32) << 16) + G::kMetaCol;
     // a cursor over this CTA's stages in the producer's order: tile t, stage kb of num_kb,
-    // and the address of this lane's words of that stage
+    // the tile's first row and the address of this lane's image words of that stage
     struct Cursor {
-      int t, kb, num_kb;
+      int t, kb, num_kb, row0;
       const uint4* src;
     };
     auto seek = [&](Cursor& c, int t) {  // first stage of tile t or a later one
@@ -684,74 +692,116 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
         const int mt128 = kPair ? mt * 2 + int(rank) : mt;
         c.kb = 0;
         c.num_kb = pp.num_kb;
-        c.src = reinterpret_cast<const uint4*>(pp.meta + b * pp.stride_meta +
-                                               int64_t(mt128) * pp.num_kb * G::kMetaBytes) +
-                lrow * kVecs;
+        c.row0 = mt128 * 128;
+        c.src = pp.meta == nullptr
+                    ? nullptr
+                    : reinterpret_cast<const uint4*>(pp.meta + b * pp.stride_meta +
+                                                     int64_t(mt128) * pp.num_kb * G::kMetaBytes) +
+                          lrow * (G::kMetaWords / 4);
         return;
       }
     };
     auto next = [&](Cursor& c) {
-      c.src += G::kMetaBytes / 16;
+      if (c.src != nullptr) c.src += G::kMetaBytes / 16;
       if (++c.kb == c.num_kb) seek(c, c.t + nunits);
     };
-    auto load = [&](const Cursor& c, uint4 (&v)[kVecs]) {
-      if (c.t < ntiles_total) {
+    auto writers = [&](auto index_mode) {
+      constexpr bool kIdx = decltype(index_mode)::value;
+      constexpr int kAhead = kIdx ? 2 : 4;         // stages of words held in registers
+      constexpr int kW = kIdx ? 8 : G::kMetaWords;  // words per lane and stage
+      auto load = [&](const Cursor& c, uint32_t (&w)[kW]) {
+        if (c.t >= ntiles_total) return;
+        if constexpr (kIdx) {
+          const int kw = p.K / 32;  // canonical words per row
+          if constexpr (ESZ == 2) {
+            const int ra = c.row0 + r16;
 #pragma unroll
-        for (int i = 0; i < kVecs; ++i) v[i] = __ldg(c.src + i);
-      }
-    };
-    Cursor ld, wr;
-    seek(ld, unit);
-    wr = ld;
-    uint4 buf[kAhead][kVecs];
+            for (int j = 0; j < 4; ++j) {
+              const int col = c.kb * 4 + j;
+              w[j] = (col < kw && ra < p.M) ? __ldg(p.index + int64_t(ra) * p.ldi + col) : kPadWord;
+              w[4 + j] = (col < kw && ra + 8 < p.M)
+                             ? __ldg(p.index + int64_t(ra + 8) * p.ldi + col)
+                             : kPadWord;
+            }
+          } else {
+            const int r = c.row0 + lrow;
 #pragma unroll
-    for (int a = 0; a < kAhead; ++a) {
-      load(ld, buf[a]);
-      if (ld.t < ntiles_total) next(ld);
-    }
-    int q = 0;
-    bool ok = true;
-    while (ok && wr.t < ntiles_total) {
+            for (int i = 0; i < 8; ++i) {
+              const int col = c.kb * 8 + i;
+              w[i] = (col < kw && r < p.M) ? __ldg(p.index + int64_t(r) * p.ldi + col) : kPadWord;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kW / 4; ++i) {
+            const uint4 v = __ldg(c.src + i);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+          }
+        }
+      };
+      Cursor ld, wr;
+      seek(ld, unit);
+      wr = ld;
+      uint32_t buf[kAhead][kW];
 #pragma unroll
       for (int a = 0; a < kAhead; ++a) {
-        if (wr.t >= ntiles_total) break;
-        const int s = q % kStages;
-        int free_slot = 1;
-        if (lane == 0)
-          free_slot = mbar_wait(&empty_bar[s], ((q / kStages) & 1) ^ 1u, abort, p.limit_ns);
-        if (__shfl_sync(0xFFFFFFFFu, free_slot, 0) == 0) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t e = lanes + uint32_t(s * G::kMmas * kSlotCols);
-        if constexpr (ESZ == 2) {  // kind::f16: one column per MMA
-          tc_st_32x32b_x1(e, buf[a][0].x);
-          tc_st_32x32b_x1(e + kSlotCols, buf[a][0].y);
-          tc_st_32x32b_x1(e + 2 * kSlotCols, buf[a][0].z);
-          tc_st_32x32b_x1(e + 3 * kSlotCols, buf[a][0].w);
-        } else {  // kind::f8f6f4: two columns per MMA
-          tc_st_32x32b_x2(e, buf[a][0].x, buf[a][0].y);
-          tc_st_32x32b_x2(e + kSlotCols, buf[a][0].z, buf[a][0].w);
-          tc_st_32x32b_x2(e + 2 * kSlotCols, buf[a][kVecs - 1].x, buf[a][kVecs - 1].y);
-          tc_st_32x32b_x2(e + 3 * kSlotCols, buf[a][kVecs - 1].z, buf[a][kVecs - 1].w);
-        }
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if constexpr (kPair)
-            mbar_arrive_cluster(meta_full_addr + uint32_t(s * sizeof(uint64_t)));
-          else
-            mbar_arrive(&meta_full[s]);
-        }
-        // refill this register slot with the stage kAhead further on
         load(ld, buf[a]);
         if (ld.t < ntiles_total) next(ld);
-        next(wr);
-        ++q;
       }
-    }
+      int q = 0;
+      bool ok = true;
+      while (ok && wr.t < ntiles_total) {
+#pragma unroll
+        for (int a = 0; a < kAhead; ++a) {
+          if (wr.t >= ntiles_total) break;
+          const int s = q % kStages;
+          int free_slot = 1;
+          if (lane == 0)
+            free_slot = mbar_wait(&empty_bar[s], ((q / kStages) & 1) ^ 1u, abort, p.limit_ns);
+          if (__shfl_sync(0xFFFFFFFFu, free_slot, 0) == 0) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t e = lanes + uint32_t(s * G::kMmas * kSlotCols);
+          if constexpr (ESZ == 2) {  // kind::f16: one column per MMA
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t x = buf[a][j];
+              if constexpr (kIdx)
+                x = ((buf[a][j] >> (16 * h16)) & 0xFFFFu) |
+                    (((buf[a][4 + j] >> (16 * h16)) & 0xFFFFu) << 16);
+              tc_st_32x32b_x1(e + j * kSlotCols, x);
+            }
+          } else {  // kind::f8f6f4: two columns per MMA
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tc_st_32x32b_x2(e + j * kSlotCols, buf[a][2 * j], buf[a][2 * j + 1]);
+          }
+          tc_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (kPair)
+              mbar_arrive_cluster(meta_full_addr + uint32_t(s * sizeof(uint64_t)));
+            else
+              mbar_arrive(&meta_full[s]);
+          }
+          // refill this register slot with the stage kAhead further on
+          load(ld, buf[a]);
+          if (ld.t < ntiles_total) next(ld);
+          next(wr);
+          ++q;
+        }
+      }
+    };
+    if (p.index != nullptr)
+      writers(std::true_type{});
+    else
+      writers(std::false_type{});
   } else {
     if constexpr (kPair) regs_inc<G::kRegsEpi>();
     // ---------------------------------------------------------------- epilogue
@@ -1185,9 +1235,12 @@ int launch_spmma_grouped(int ta, int tb, int tc, int td, const sp24_mma_problem*
 int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K,
                  const void* values, int64_t ldv, const void* meta, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd, void* workspace,
-                 int32_t* status, int num_sms, cudaStream_t s, const BatchArgs* batch) {
+                 int32_t* status, int num_sms, cudaStream_t s, const BatchArgs* batch,
+                 const uint32_t* index, int64_t ldi) {
   MmaParams p;
   memset(&p, 0, sizeof(p));
+  p.index = index;  // canonical index instead of the image (one problem only)
+  p.ldi = ldi;
   BatchStrides bs{0, 0, 0};
   p.batch = 1;
   if (batch != nullptr && batch->count > 1) {

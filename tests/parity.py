@@ -80,9 +80,10 @@ def gpu_compress(c: dict, mode: str):
 
 
 def run_case(c: dict, mode: str = "mask", out_dtype=torch.float32, rows=None, check=True,
-             fused: bool = False):
+             fused: bool = False, by_index: bool = False):
     """Compress + meta_prepare + mma on the GPU (fused: compress_meta), oracle on the CPU,
-    compare."""
+    compare.  by_index: the product reads the canonical index (mma_index), and must equal
+    the product on the image bit for bit."""
     ta, tb = c["ta"], c["tb"]
     M, N, K = c["M"], c["N"], c["K"]
     if fused:
@@ -96,6 +97,12 @@ def run_case(c: dict, mode: str = "mask", out_dtype=torch.float32, rows=None, ch
     B = dev(c["B"])
     C = dev(c["C"])
     D = sp.mma(values, meta, B, C, out_dtype=out_dtype)
+    if by_index:
+        D_img = D
+        D = sp.mma_index(values, index, B, C, out_dtype=out_dtype, status=status)
+        torch.cuda.synchronize()
+        assert torch.equal(D.view(torch.uint8), D_img.view(torch.uint8)), \
+            "product on the canonical index differs from the product on the image"
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     # oracle: its own compression of the same dense input, then its own product

@@ -121,6 +121,30 @@ def test_mma_argument_checks():
     assert _mma(ldd=130) == ALIGN               # 520-byte pitch
     assert _mma(M=0) == OK
     assert _mma(N=0) == OK
+    assert _mma(meta=None) == INVALID          # sp24_mma needs the image
+    assert _mma(meta=FAKE_ODD) == ALIGN
+
+
+def _mma_index(ta=BF16, tb=BF16, tc=F32, td=F32, M=128, N=128, K=128, values=FAKE, ldv=64,
+               index=FAKE, ldi=4, B=FAKE, ldb=128, C=FAKE, ldc=128, D=FAKE, ldd=128, ws=None,
+               ws_bytes=0):
+    return sp.lib().sp24_mma_index(ta, tb, tc, td, M, N, K, values, ldv, index, ldi, B, ldb, C,
+                                   ldc, D, ldd, ws, ws_bytes, None, None)
+
+
+def test_mma_index_argument_checks():
+    # the same type and shape rules as sp24_mma
+    assert _mma_index(ta=F16, tb=BF16) == UNSUPPORTED
+    assert _mma_index(ta=F32, tb=F32) == UNSUPPORTED
+    assert _mma_index(ta=S8, tb=S8, tc=S32, td=S32) == INVALID        # no workspace
+    assert _mma_index(K=48) == INVALID
+    assert _mma_index(D=None) == INVALID
+    # the canonical index: present, ldi >= K/32 words, 4-byte aligned, any pitch
+    assert _mma_index(index=None) == INVALID
+    assert _mma_index(ldi=3) == INVALID
+    assert _mma_index(index=ctypes.c_void_p(0x10002)) == ALIGN
+    assert _mma_index(B=FAKE_ODD) == ALIGN
+    assert _mma_index(M=0) == OK
 
 
 def _bmma(ta=BF16, tb=BF16, tc=F32, td=F32, batch=3, M=128, N=128, K=128, sv=None, sm=None,
@@ -161,6 +185,8 @@ def test_no_device_means_no_cpu_fallback():
     # valid-looking arguments reach the device check and are refused: no CPU path exists
     assert _compress() == NODEV
     assert _mma() == NODEV
+    assert _mma_index() == NODEV
+    assert _mma_index(index=FAKE_ODD, ldi=6) == NODEV  # any 4-byte aligned index and pitch
     assert sp.lib().sp24_diag_wait_timeout(FAKE, 1000, None) == NODEV
 
 
