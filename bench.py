@@ -1,7 +1,12 @@
 """Benchmark of the 2:4 sparse multiply-accumulate hot path on GB300.
 
 One step = one pass of the whole path over one batch of synthetic input:
-    sp24_compress (mask mode)  ->  sp24_meta_prepare  ->  sp24_mma (D = A_sp B + C)
+    sp24_compress_meta (compression and the metadata image in one pass, mask mode)
+    ->  sp24_mma (D = A_sp B + C)
+(--pass separate: sp24_compress -> sp24_meta_prepare -> sp24_mma; --pass index:
+sp24_compress -> sp24_mma_index.)  The K timed steps are independent; by default their
+compressions and products run on two streams so that step i+1's compression overlaps
+step i's product (--serial: one stream).
 Default workload: bf16, M = N = K = 4096, keep-mask drawn per group from the six
 two-of-four patterns, A, B ~ N(0,1), C f32 ~ N(0,1), f32 output.  The metric is
 dense-equivalent TFLOP/s = 2 M N K / step time.
