@@ -40,6 +40,28 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(L, name), name
 
 
+def declared_arity():
+    """Number of parameters of every function the header declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(sp24_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_lists_match_the_header():
+    L = sp.lib()
+    arity = declared_arity()
+    assert set(arity) == set(declared_functions())
+    for name, n in arity.items():
+        argtypes = getattr(L, name).argtypes
+        if argtypes is not None:  # functions called without arguments have none set
+            assert len(argtypes) == n, (name, len(argtypes), n)
+        else:
+            assert n == 0, name
+
+
 def test_version_and_status_strings():
     L = sp.lib()
     assert L.sp24_version() == 1
