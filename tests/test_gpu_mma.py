@@ -291,41 +291,6 @@ def test_bf16_4096_through_the_fused_pass():
     run_case(c, mode="mask", rows=sample_rows(c["M"]), fused=True)
 
 
-# ---- the product on the canonical index itself (no image) ---------------------------------
-
-@pytest.mark.parametrize("ta,tb,tc,out,M,N,K", [
-    ("bf16", "bf16", "f32", torch.float32, 200, 16, 352),    # narrow tiles, ragged M and K
-    ("f16", "f16", None, torch.bfloat16, 130, 96, 160),      # 256 x 128 pair tiles
-    ("bf16", "bf16", "bf16", torch.float32, 257, 272, 1056),  # 256 x 256 pair tiles
-    ("e4m3", "e4m3", None, torch.float32, 131, 80, 544),     # FP8, 128 x 128 tiles
-    ("e5m2", "e4m3", "f32", torch.float32, 300, 304, 800),   # FP8 pair, stage tail
-    ("e4m3", "e4m3", None, torch.bfloat16, 64, 32, 256),     # FP8 narrow tiles
-    ("s8", "s8", "s32", torch.int32, 190, 144, 1088),        # exact integers (16-bit layout)
-])
-def test_product_reads_the_canonical_index(ta, tb, tc, out, M, N, K):
-    c = inputs.case(ta, tb, M, N, K, seed=M + N, tc=tc, dist="full" if ta == "s8" else "normal")
-    run_case(c, mode="mask", out_dtype=out, by_index=True)
-
-
-def test_canonical_index_with_a_padded_pitch():
-    M, N, K = 250, 64, 480
-    c = inputs.case("bf16", "bf16", M, N, K, seed=17, tc="f32")
-    values, index, _ = gpu_compress(c, "mask")
-    wide = torch.full((M, K // 32 + 3), -1, dtype=torch.int32, device="cuda")
-    wide[:, :K // 32] = index
-    B, C = dev(c["B"]), dev(c["C"])
-    D_idx = sp.mma_index(values, wide[:, :K // 32], B, C)
-    D_img = sp.mma(values, sp.meta_prepare(index, torch.bfloat16, M, K), B, C)
-    torch.cuda.synchronize()
-    assert torch.equal(D_idx.view(torch.uint8), D_img.view(torch.uint8))
-
-
-def test_llm_layer_through_the_index():
-    c = inputs.llm_layer(16)
-    run_case(c, mode="magnitude", out_dtype=torch.bfloat16, rows=sample_rows(c["M"]),
-             by_index=True)
-
-
 # ---- CUDA graphs: the calls are stream-ordered and allocation-free, so they capture --------
 
 def test_graph_capture_replays_the_eager_result():
@@ -437,3 +402,38 @@ def test_grouped_many_problems_and_empty_ones():
     B = torch.zeros((128, 16), dtype=torch.bfloat16, device="cuda")
     D = sp.mma_grouped([(values, meta, B, None)])
     assert D[0].shape == (0, 16)
+
+
+# ---- the product on the canonical index itself (no image) ---------------------------------
+
+@pytest.mark.parametrize("ta,tb,tc,out,M,N,K", [
+    ("bf16", "bf16", "f32", torch.float32, 200, 16, 352),    # narrow tiles, ragged M and K
+    ("f16", "f16", None, torch.bfloat16, 130, 96, 160),      # 256 x 128 pair tiles
+    ("bf16", "bf16", "bf16", torch.float32, 257, 272, 1056),  # 256 x 256 pair tiles
+    ("e4m3", "e4m3", None, torch.float32, 131, 80, 544),     # FP8, 128 x 128 tiles
+    ("e5m2", "e4m3", "f32", torch.float32, 300, 304, 800),   # FP8 pair, stage tail
+    ("e4m3", "e4m3", None, torch.bfloat16, 64, 32, 256),     # FP8 narrow tiles
+    ("s8", "s8", "s32", torch.int32, 190, 144, 1088),        # exact integers (16-bit layout)
+])
+def test_product_reads_the_canonical_index(ta, tb, tc, out, M, N, K):
+    c = inputs.case(ta, tb, M, N, K, seed=M + N, tc=tc, dist="full" if ta == "s8" else "normal")
+    run_case(c, mode="mask", out_dtype=out, by_index=True)
+
+
+def test_canonical_index_with_a_padded_pitch():
+    M, N, K = 250, 64, 480
+    c = inputs.case("bf16", "bf16", M, N, K, seed=17, tc="f32")
+    values, index, _ = gpu_compress(c, "mask")
+    wide = torch.full((M, K // 32 + 3), -1, dtype=torch.int32, device="cuda")
+    wide[:, :K // 32] = index
+    B, C = dev(c["B"]), dev(c["C"])
+    D_idx = sp.mma_index(values, wide[:, :K // 32], B, C)
+    D_img = sp.mma(values, sp.meta_prepare(index, torch.bfloat16, M, K), B, C)
+    torch.cuda.synchronize()
+    assert torch.equal(D_idx.view(torch.uint8), D_img.view(torch.uint8))
+
+
+def test_llm_layer_through_the_index():
+    c = inputs.llm_layer(16)
+    run_case(c, mode="magnitude", out_dtype=torch.bfloat16, rows=sample_rows(c["M"]),
+             by_index=True)
