@@ -7,9 +7,13 @@ One step = one pass of the whole path over one batch of synthetic input:
 sp24_compress -> sp24_mma_index.)  The K timed steps are independent; by default their
 compressions and products run on two streams so that step i+1's compression overlaps
 step i's product (--serial: one stream).
-Default workload: bf16, M = N = K = 4096, keep-mask drawn per group from the six
-two-of-four patterns, A, B ~ N(0,1), C f32 ~ N(0,1), f32 output.  The metric is
-dense-equivalent TFLOP/s = 2 M N K / step time.
+Default workload: the largest single-GPU configuration, FP8 E4M3 M = N = K = 8192, keep
+mask drawn per group from the six two-of-four patterns, A, B ~ N(0,1) scaled per tensor to
+the format's range, no C, f32 output (--config bf16-4096 and the others stay selectable).
+The metric is dense-equivalent TFLOP/s (TOP/s for integers) = 2 M N K / step time.
+Timing: the K steps are recorded once (a CUDA graph); the graph is replayed R times, each
+replay bracketed by CUDA events, R chosen so that the timed region lasts at least
+--min-seconds (1 s by default), and the step time is the median replay time / K.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 Prints ONE JSON line (rank 0).  For N > 1 it runs under torch.distributed.run, one rank
@@ -295,7 +299,8 @@ def gpu_arm(args, world, rank, local):
         return sum(t.numel() * t.element_size() for t in s.values() if t is not None)
 
     sets = [make_set(base)]
-    while len(sets) * set_bytes(sets[0]) < 3 * L2_BYTES and len(sets) < 16:
+    # at least two sets, so that no step reads operands the step before it left in L2
+    while (len(sets) < 2 or len(sets) * set_bytes(sets[0]) < 3 * L2_BYTES) and len(sets) < 16:
         # distinct contents per set: roll the rows (cheap, same distribution)
         c2 = dict(base)
         shift = 37 * len(sets)
@@ -448,14 +453,9 @@ def gpu_arm(args, world, rank, local):
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} during warm-up")
 
-    # timed region: K steps back to back, no events between the kernels (the GEMM may
-    # start during the previous kernel's tail)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
+    def run_k_steps():
+        # the K steps back to back, no events between the kernels (the GEMM may start
+        # during the previous kernel's tail)
         if graph is not None:
             graph.replay()
         elif overlap:
@@ -463,11 +463,32 @@ def gpu_arm(args, world, rank, local):
         else:
             for i in range(args.steps):
                 launch(sets[i % len(sets)])
-        t_end.record(stream)
+
+    # replays in the timed region: enough for at least --min-seconds (one untimed probe)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    run_k_steps()
+    p1.record(stream)
+    torch.cuda.synchronize(dev)
+    probe_ms = max(p0.elapsed_time(p1), 1e-3)
+    replays = int(max(1, min(100000, -(-args.min_seconds * 1e3 // probe_ms))))
+    replays = int(max_over_ranks(float(replays), world))
+
+    # timed region: `replays` replays of the K steps, each bracketed by events
+    ev_rep = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(replays)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clk:
+        for a, b in ev_rep:
+            a.record(stream)
+            run_k_steps()
+            b.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
-    total_ms = t_start.elapsed_time(t_end)
-    total_ms = max_over_ranks(total_ms, world)
+    rep_ms = [a.elapsed_time(b) for a, b in ev_rep]
+    total_ms = max_over_ranks(statistics.median(rep_ms), world)
+    timed_s = max_over_ranks(sum(rep_ms) * 1e-3, world)
     # the serial schedule's step time, for comparison (same steps, one stream)
     ms_step_serial = None
     if overlap:
@@ -635,6 +656,9 @@ def gpu_arm(args, world, rank, local):
                        "parallelism": f"replicas x{world}",
                        "launch": ("one CUDA graph of the K steps" if graph is not None
                                   else "eager launches"),
+                       "timing": (f"median over {replays} replays of the K steps, each "
+                                  f"bracketed by CUDA events; {timed_s:.2f} s timed in all"),
+                       "replays": replays,
                        "schedule": ("overlapped: the K independent steps run their "
                                     "compressions on one stream and their products on "
                                     "another, so step i+1's compression overlaps step i's "
@@ -644,7 +668,7 @@ def gpu_arm(args, world, rank, local):
             "kernels": kernels,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps,
+            "gpu_launches": launches_per_step * args.steps * replays,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -655,7 +679,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="bf16-4096", choices=sorted(CONFIGS))
+    ap.add_argument("--config", default="e4m3-8192", choices=sorted(CONFIGS))
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="the timed region replays the K steps until it lasts this long")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

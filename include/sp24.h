@@ -302,7 +302,9 @@ sp24_status sp24_mma_grouped(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_d
  * each call writes what it uses before reading it; calls whose work overlaps on the GPU
  * (no stream ordering between them) race on it.  The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture.
+ * call before any stream capture.  The address is kept per device and context: after the
+ * context is destroyed (cudaDeviceReset) the array's contents are gone, and the next call
+ * in the new context looks the address up again.
  */
 sp24_status sp24_mma_i8_noalloc(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dtype td,
                                 int64_t M, int64_t N, int64_t K, const void *values,

@@ -12,6 +12,7 @@
 // writes the part it uses (the two operands widened to bf16) before reading it, so nothing
 // has to start at zero, and the array keeps the last call's contents.  Two calls whose
 // work overlaps on the GPU (different streams, no ordering between them) race on it.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -25,22 +26,54 @@ namespace {
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[SP24_NOALLOC_SCRATCH_BYTES];
 
-// Device address of the array on device `dev` (which must be current): looked up once per
-// device.  In host code the array's name is only a stand-in, never a device address.
+// The current context's unique id (cuCtxGetId through the runtime's driver entry
+// point, so the library needs no link against the driver library), or 0 if unavailable.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+      ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the array in the current context of device `dev` (which must be
+// current).  In host code the array's name is only a stand-in, never a device address.
+// The address is looked up once per device and context: a context created anew (after
+// cudaDeviceReset, for example) has a different id, and its first call looks it up again.
 void* scratch_address(int dev) {
   static std::mutex mu;
   static void* addr[64];
-  static bool ready[64];
+  static unsigned long long ctx_of[64];
   if (dev < 0 || dev >= 64) return nullptr;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (!ready[dev]) {
+  if (addr[dev] == nullptr || ctx == 0 || ctx_of[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return nullptr;
     }
     addr[dev] = p;
-    ready[dev] = true;
+    ctx_of[dev] = ctx;
   }
   return addr[dev];
 }

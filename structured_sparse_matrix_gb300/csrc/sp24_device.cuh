@@ -314,6 +314,72 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
       : "memory");
 }
 
+// One whole stage of the main loop in a single instruction sequence: test (without
+// waiting) whether the next stage's barrier phase `next_par` at shared address `next_bar`
+// has completed, issue the stage's four sparse MMAs and the commit that arrives on the
+// stage's empty barrier(s), and only then look at the test's outcome.  The issuing thread
+// spends tens of cycles per tcgen05 instruction and over a hundred per barrier test, while
+// four M = 256, N = 256 MMAs keep the tensor pipe busy for about 512 cycles; testing the
+// next barrier while the MMAs are issued keeps its latency off the loop.
+// MMA j reads A at descriptor a0 + j * a_step, B at b0 + j * b_step (descriptor units of 16
+// bytes) and its metadata at TMEM column e0 + 16 j; acc0 = 0 starts the accumulation.
+// kPair: cta_group::2 with a commit multicast to both CTAs of the pair (`mask`);
+// otherwise cta_group::1 and a commit to the local barrier `empty_bar`.
+// Returns whether the next stage's phase had completed at the test.
+template <bool kPair, bool kF8>
+__device__ __forceinline__ bool mma_stage_test_next(uint32_t next_bar, uint32_t next_par,
+                                                    uint32_t d, uint64_t a0, uint64_t b0,
+                                                    uint32_t a_step, uint32_t b_step,
+                                                    uint32_t e0, uint32_t idesc, uint32_t acc0,
+                                                    uint32_t empty_bar) {
+  uint32_t ok;
+#define SP24_STAGE_ASM(GROUP, KIND, COMMIT)                                                   \
+  asm volatile(                                                                              \
+      "{\n"                                                                                  \
+      ".reg .pred pn, pa, pt;\n"                                                             \
+      ".reg .b64 a1, a2, a3, b1, b2, b3, sa, sb;\n"                                          \
+      ".reg .b32 e1, e2, e3;\n"                                                              \
+      "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n"                            \
+      "setp.ne.b32 pa, %10, 0;\n"                                                            \
+      "setp.eq.b32 pt, %2, %2;\n"                                                            \
+      "cvt.u64.u32 sa, %6;\n"                                                                \
+      "cvt.u64.u32 sb, %7;\n"                                                                \
+      "add.s64 a1, %4, sa;\n add.s64 a2, a1, sa;\n add.s64 a3, a2, sa;\n"                   \
+      "add.s64 b1, %5, sb;\n add.s64 b2, b1, sb;\n add.s64 b3, b2, sb;\n"                   \
+      "add.u32 e1, %8, 16;\n add.u32 e2, %8, 32;\n add.u32 e3, %8, 48;\n"                    \
+      "tcgen05.mma.sp." GROUP "." KIND " [%3], %4, %5, [%8], %9, pa;\n"                      \
+      "tcgen05.mma.sp." GROUP "." KIND " [%3], a1, b1, [e1], %9, pt;\n"                      \
+      "tcgen05.mma.sp." GROUP "." KIND " [%3], a2, b2, [e2], %9, pt;\n"                      \
+      "tcgen05.mma.sp." GROUP "." KIND " [%3], a3, b3, [e3], %9, pt;\n" COMMIT               \
+      "selp.b32 %0, 1, 0, pn;\n"                                                             \
+      "}\n"                                                                                  \
+      : "=r"(ok)                                                                             \
+      : "r"(next_bar), "r"(next_par), "r"(d), "l"(a0), "l"(b0), "r"(a_step), "r"(b_step),    \
+        "r"(e0), "r"(idesc), "r"(acc0), "r"(empty_bar), "h"(uint16_t(3))                     \
+      : "memory")
+  if constexpr (kPair) {
+    if constexpr (kF8)
+      SP24_STAGE_ASM("cta_group::2", "kind::f8f6f4",
+                     "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
+                     "multicast::cluster.b64 [%11], %12;\n");
+    else
+      SP24_STAGE_ASM("cta_group::2", "kind::f16",
+                     "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
+                     "multicast::cluster.b64 [%11], %12;\n");
+  } else {
+    if constexpr (kF8)
+      SP24_STAGE_ASM("cta_group::1", "kind::f8f6f4",
+                     "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+                     "[%11];\n");
+    else
+      SP24_STAGE_ASM("cta_group::1", "kind::f16",
+                     "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+                     "[%11];\n");
+  }
+#undef SP24_STAGE_ASM
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor: start address, leading / stride byte offsets,
 // version 1 (bit 46), swizzle mode in bits 61-63 (0 none, 2 = 128-byte).

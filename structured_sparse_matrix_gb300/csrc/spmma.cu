@@ -455,10 +455,9 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
   constexpr int kStages = G::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  // full_bar (even CTA): the stage's operands of both CTAs have landed (TMA bytes) and every
+  // metadata writer warp of the pair has stored the stage's metadata into its TMEM slots
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
-  // meta_full (even CTA): every writer warp of the pair has stored the stage's metadata
-  // into its TMEM slots
-  __shared__ __align__(8) uint64_t meta_full[kStages];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -473,9 +472,8 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full_bar[s], 1);
+      mbar_init(&full_bar[s], 1 + 4 * (kPair ? 2 : 1));  // producer + writer warps
       mbar_init(&empty_bar[s], 1);
-      mbar_init(&meta_full[s], 4 * (kPair ? 2 : 1));
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -567,6 +565,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
       // B is MN-major: LBO = next atom along N, SBO = next 8 rows of K
       const uint64_t bdesc_hi = smem_desc_hi(G::kAtomBytes, 8 * G::kAtomInner, G::kSwzCode);
       int q = 0, local = 0, chunk = 0;
+      bool ready = false;  // stage q's full_bar phase is known to have completed
       for (int t = unit; t < ntiles_total && !*abort; t += nunits, ++local) {
         int lt;
         const int g = tile_problem<kGrouped>(gt, t, lt);
@@ -599,10 +598,10 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
               d_tmem = tmem + uint32_t(abuf * G::kTileN);
             }
           }
-          // the stage's operands (both CTAs) and its metadata in the TMEM slots (stored
-          // by the writer warps of both CTAs)
-          if (!mbar_wait(&full_bar[s], par, abort, p.limit_ns) ||
-              !mbar_wait(&meta_full[s], par, abort, p.limit_ns)) {
+          // the stage's operands (both CTAs) and its metadata in the TMEM slots (the writer
+          // warps of both CTAs arrive on the same barrier); skipped when the previous
+          // stage's test already saw the phase complete
+          if (!ready && !mbar_wait(&full_bar[s], par, abort, p.limit_ns)) {
             ok = false;
             break;
           }
@@ -612,22 +611,34 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
           const uint32_t b_saddr = smem_addr(sB + s * G::kBBytes);
           const int k0 = kb * G::kStageK;
           const int first = (OUT == 2) ? kc : kb;  // accumulate unless the chunk/tile starts
+          if (k0 + G::kStageK <= kdense) {
+            // the whole stage in one sequence, testing the next stage's barrier meanwhile
+            // (MMA j: A 32 bytes further along K, B kMmaK rows further, metadata slot j)
+            const int qn = q + 1;
+            ready = mma_stage_test_next<kPair, ESZ == 1>(
+                smem_addr(&full_bar[qn % kStages]), uint32_t((qn / kStages) & 1), d_tmem,
+                smem_desc(a_saddr, adesc_hi), smem_desc(b_saddr, bdesc_hi), 32u / 16u,
+                uint32_t(G::kMmaK * G::kAtomInner / 16), e_tmem, id, first > 0 ? 1u : 0u,
+                smem_addr(&empty_bar[s]));
+          } else {  // the last, partial stage of a ragged K
+            ready = false;
 #pragma unroll
-          for (int j = 0; j < G::kMmas; ++j) {
-            if (k0 + j * G::kMmaK < kdense) {
-              const uint64_t ad = smem_desc(a_saddr + 32 * j, adesc_hi);
-              const uint64_t bd = smem_desc(b_saddr + j * G::kMmaK * G::kAtomInner, bdesc_hi);
-              const uint32_t acc = (first > 0 || j > 0) ? 1u : 0u;
-              if constexpr (kPair)
-                tc_mma_sp_pair<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, id, acc);
-              else
-                tc_mma_sp<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, id, acc);
+            for (int j = 0; j < G::kMmas; ++j) {
+              if (k0 + j * G::kMmaK < kdense) {
+                const uint64_t ad = smem_desc(a_saddr + 32 * j, adesc_hi);
+                const uint64_t bd = smem_desc(b_saddr + j * G::kMmaK * G::kAtomInner, bdesc_hi);
+                const uint32_t acc = (first > 0 || j > 0) ? 1u : 0u;
+                if constexpr (kPair)
+                  tc_mma_sp_pair<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, id, acc);
+                else
+                  tc_mma_sp<ESZ == 1>(d_tmem, ad, bd, e_tmem + j * kSlotCols, id, acc);
+              }
             }
+            if constexpr (kPair)
+              tc_commit_pair_mc(&empty_bar[s], 3);
+            else
+              tc_commit(&empty_bar[s]);
           }
-          if constexpr (kPair)
-            tc_commit_pair_mc(&empty_bar[s], 3);
-          else
-            tc_commit(&empty_bar[s]);
           if constexpr (OUT == 2) {
             if (kc == p.chunk - 1 || kb == num_kb - 1) {  // chunk done
               if constexpr (kPair)
@@ -664,14 +675,14 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
     // lane's two rows, combined by halves at store time; FP8: the row's 8 words).  Once the
     // MMAs that last read the slot set are done (empty_bar, the producer's barrier) the
     // warp stores them with tcgen05.st, waits for the stores and arrives on the even CTA's
-    // meta_full, which the MMA issuer waits on before the stage's MMAs.
+    // full_bar of the stage, which the MMA issuer waits on before the stage's MMAs.
     const int quad = warp & 3;
     const int lrow = quad * 32 + lane;            // this thread's TMEM lane
     // kind::f16 layout: TMEM lane 16b + l holds halves h = l / 8 of rows 16b + l % 8 and
     // 16b + l % 8 + 8 of the tile
     const int h16 = (lrow >> 3) & 1;
     const int r16 = (lrow & ~15) + (lrow & 7);
-    const uint32_t meta_full_addr = kPair ? mapa(&meta_full[0], 0) : smem_addr(&meta_full[0]);
+    const uint32_t full_addr = kPair ? mapa(&full_bar[0], 0) : smem_addr(&full_bar[0]);
     const uint32_t lanes = tmem + (uint32_t(quad * 32) << 16) + G::kMetaCol;
     // a cursor over this CTA's stages in the producer's order: tile t, stage kb of num_kb,
     // the tile's first row and the address of this lane's image words of that stage
@@ -786,9 +797,9 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
           __syncwarp();
           if (lane == 0) {
             if constexpr (kPair)
-              mbar_arrive_cluster(meta_full_addr + uint32_t(s * sizeof(uint64_t)));
+              mbar_arrive_cluster(full_addr + uint32_t(s * sizeof(uint64_t)));
             else
-              mbar_arrive(&meta_full[s]);
+              mbar_arrive(&full_bar[s]);
           }
           // refill this register slot with the stage kAhead further on
           load(ld, buf[a]);
