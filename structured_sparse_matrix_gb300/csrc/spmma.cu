@@ -341,6 +341,35 @@ __device__ __forceinline__ void prefetch_c_rows(const MmaParams& p, int row0, in
     }
 }
 
+// 32 consecutive columns of one output row held by one thread (a 32x32b accumulator
+// load): add C, cast and store as 8-column pieces (32-byte f32 / 16-byte 16-bit vectors).
+template <int OUT>
+__device__ __forceinline__ void store_row32(const uint32_t (&r)[32], const MmaParams& p, int row,
+                                            int col0, int64_t cofs, int64_t dofs) {
+  float c[4][8];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) load_c8(c[g], p, row, col0 + 8 * g, cofs);
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = (p.K > 0 ? __uint_as_float(r[8 * g + j]) : 0.f) + c[g][j];
+    store8<OUT>(v, p, row, col0 + 8 * g, dofs);
+  }
+}
+
+// Pull one row's C of a coming tile (up to `cols` columns from col0) into L2.
+__device__ __forceinline__ void prefetch_c_row(const MmaParams& p, int row, int col0, int cols,
+                                               int64_t cofs) {
+  if (p.C == nullptr || row >= p.M || col0 >= p.N) return;
+  const int ncols = p.N - col0 < cols ? p.N - col0 : cols;
+  const int csize = p.ctype == 0 ? 4 : 2;
+  const uint32_t bytes = uint32_t(ncols * csize) & ~15u;
+  if (bytes != 0)
+    bulk_prefetch_l2(static_cast<const uint8_t*>(p.C) + (cofs + int64_t(row) * p.ldc + col0) * csize,
+                     bytes);
+}
+
 // Integer epilogue for one 32-column chunk: D = sum + C (s32, nullable), wrapping.
 __device__ __forceinline__ void store_chunk_s32(const uint32_t* v, const MmaParams& p, int row,
                                                 int col0) {
@@ -830,6 +859,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
       int b, mt, nt;
       batch_tile<G::kTileM>(pp, lt, b, mt, nt);
       const int64_t cofs = b * pp.stride_c, dofs = b * pp.stride_d;
+
       const int abuf = G::kAccBufs == 1 ? 0 : (local & 1);
       const int use = G::kAccBufs == 1 ? local : (local >> 1);
       if constexpr (OUT != 2) {
@@ -884,25 +914,22 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
           }
         }
       } else if constexpr (kPair) {
-        // drain this warp's 32 rows x kCols columns (its half of the CTA's columns), free
-        // the accumulator, then store
+        // drain this warp's 32 rows x kCols columns (its half of the CTA's columns) with
+        // 32x32b loads, one row per thread, free the accumulator, then add C and store
+        // each thread's row as 32-byte pieces.  Unlike a transposed layout this takes no
+        // shuffles: the epilogue's instructions share issue slots with the MMA thread.
         constexpr int kCols = G::kTileN / 2;  // 128 (256 x 256 tiles) or 64 (256 x 128)
-        constexpr int kSegP = kCols / 32;
+        constexpr int kChunks = kCols / 32;
         const int half = ew >> 2;
-        uint32_t r[2][16 * kSegP];
+        uint32_t r[kChunks][32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t a = lane_base + (uint32_t(16 * h) << 16) + uint32_t(half * kCols);
-          if constexpr (kSegP == 4)
-            tc_ld_16x256b_x16(a, r[h]);
-          else
-            tc_ld_16x256b_x8(a, r[h]);
-        }
+        for (int c = 0; c < kChunks; ++c)
+          tc_ld_32x32b_x32(lane_base + uint32_t(half * kCols + 32 * c), r[c]);
         tc_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(abuf * sizeof(uint64_t)));
-        const int row0 = mt * G::kTileM + int(rank) * 128 + quad * 32 + (lane >> 2);
+        const int row = mt * G::kTileM + int(rank) * 128 + quad * 32 + lane;
         const int col0 = nt * G::kTileN + half * kCols;
         if (t + nunits < ntiles_total) {  // the next tile's C, needed one mainloop from now
           int b2, mt2, nt2;
@@ -912,14 +939,14 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
           problem_params<kGrouped>(p, gt, g2, qg2);
           const MmaParams& pp2 = kGrouped ? qg2 : p;
           batch_tile<G::kTileM>(pp2, lt2, b2, mt2, nt2);
-          prefetch_c_rows(pp2, mt2 * G::kTileM + int(rank) * 128 + quad * 32 + (lane >> 2),
-                          nt2 * G::kTileN + half * kCols, lane & 3, kCols, b2 * pp2.stride_c);
+          prefetch_c_row(pp2, mt2 * G::kTileM + int(rank) * 128 + quad * 32 + lane,
+                         nt2 * G::kTileN + half * kCols, kCols, b2 * pp2.stride_c);
         }
+        if (row < pp.M) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            store_row<OUT, kSegP>(r[h], e, pp, row0 + 16 * h + 8 * e, col0, lane & 3, cofs, dofs);
+          for (int c = 0; c < kChunks; ++c)
+            if (col0 + 32 * c < pp.N) store_row32<OUT>(r[c], pp, row, col0 + 32 * c, cofs, dofs);
+        }
       } else {
         const int row0 = mt * G::kTileM + quad * 32 + (lane >> 2);
         if (t + nunits < ntiles_total) {  // the next tile's C, needed one mainloop from now
