@@ -236,6 +236,24 @@ sp24_status sp24_mma_index(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_dty
  */
 sp24_status sp24_diag_wait_timeout(int32_t *d_status, uint64_t limit_ns, void *stream);
 
+/*
+ * sp24_diag_mma_stall -- self-test of the sparse product's give-up path.  Launches the very
+ * kernel sp24_mma runs for a float problem of this shape (ta = tb = f16, bf16, E4M3 or
+ * E5M2; no C; f32 D), except that its TMA producer issues no copies, so the operands of the
+ * first stage never arrive.  Every wait of the kernel is bounded by limit_ns nanoseconds
+ * (0 < limit_ns <= 1 s): the MMA thread's wait gives up, the other roles see that (or give
+ * up themselves), the CTAs let their metadata stores finish, free their tensor memory and
+ * exit, and SP24_DEV_TIMEOUT is OR-ed into *d_status.  values / meta / B / D must be valid
+ * device buffers as for sp24_mma (the metadata writers read the first stages' words of
+ * meta); D is left unwritten.  No copy or MMA is in flight when the kernel exits, so the
+ * context stays usable.  The source pages have no counterpart: it exists so that the
+ * failure path is exercised without faulting or hanging a GPU.
+ */
+sp24_status sp24_diag_mma_stall(sp24_dtype ta, int64_t M, int64_t N, int64_t K,
+                                const void *values, int64_t ldv, const void *meta, const void *B,
+                                int64_t ldb, void *D, int64_t ldd, uint64_t limit_ns,
+                                int32_t *d_status, void *stream);
+
 /* Bytes of the fixed device scratch array sp24_mma_i8_noalloc uses (16 MiB). */
 #define SP24_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 

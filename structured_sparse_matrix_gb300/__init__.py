@@ -47,7 +47,7 @@ EXPORTS = ("sp24_compress", "sp24_compress_meta", "sp24_decompress", "sp24_meta_
            "sp24_mma_workspace_bytes", "sp24_mma", "sp24_mma_index", "sp24_mma_strided_batched",
            "sp24_mma_grouped",
            "sp24_mma_i8_noalloc",
-           "sp24_diag_wait_timeout", "sp24_status_string", "sp24_version")
+           "sp24_diag_wait_timeout", "sp24_diag_mma_stall", "sp24_status_string", "sp24_version")
 
 class Problem(ctypes.Structure):
     """One problem of sp24_mma_grouped (the C struct sp24_mma_problem)."""
@@ -111,6 +111,9 @@ def lib():
                                               i64, p, i64, p, i64, p, p]
             L.sp24_diag_wait_timeout.restype = i32
             L.sp24_diag_wait_timeout.argtypes = [p, u64, p]
+            L.sp24_diag_mma_stall.restype = i32
+            L.sp24_diag_mma_stall.argtypes = [i32, i64, i64, i64, p, i64, p, p, i64, p, i64, u64,
+                                              p, p]
             L.sp24_status_string.restype = ctypes.c_char_p
             L.sp24_status_string.argtypes = [i32]
             L.sp24_version.restype = i32

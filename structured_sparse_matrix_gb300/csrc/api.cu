@@ -385,6 +385,27 @@ sp24_status sp24_mma_grouped(sp24_dtype ta, sp24_dtype tb, sp24_dtype tc, sp24_d
   return SP24_OK;
 }
 
+sp24_status sp24_diag_mma_stall(sp24_dtype ta, int64_t M, int64_t N, int64_t K,
+                                const void* values, int64_t ldv, const void* meta, const void* B,
+                                int64_t ldb, void* D, int64_t ldd, uint64_t limit_ns,
+                                int32_t* d_status, void* stream) {
+  if (!(ta == SP24_F16 || ta == SP24_BF16 || is_f8(ta))) return SP24_ERR_UNSUPPORTED;
+  if (!d_status || limit_ns == 0 || limit_ns > 1000000000ull) return SP24_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || (K % 32) != 0) return SP24_ERR_INVALID_ARG;
+  if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2) return SP24_ERR_INVALID_ARG;
+  if (!values || !meta || !B || !D) return SP24_ERR_INVALID_ARG;
+  if (ldd < N || ldv < K / 2 || ldb < N) return SP24_ERR_INVALID_ARG;
+  if (!aligned16(D) || (ldd * 4) % 16 || !aligned16(values) || !aligned16(B) ||
+      !aligned16(meta) || !ld_ok16(ta, ldv) || !ld_ok16(ta, ldb))
+    return SP24_ERR_ALIGN;
+  int sms = 0;
+  if (!current_device(&sms)) return SP24_ERR_NO_DEVICE;
+  const int rc = launch_spmma(ta, ta, SP24_F32, SP24_F32, M, N, K, values, ldv, meta, B, ldb,
+                              nullptr, N, D, ldd, nullptr, d_status, sms,
+                              static_cast<cudaStream_t>(stream), nullptr, nullptr, 0, limit_ns);
+  return static_cast<sp24_status>(rc);
+}
+
 sp24_status sp24_diag_wait_timeout(int32_t* d_status, uint64_t limit_ns, void* stream) {
   if (!d_status) return SP24_ERR_INVALID_ARG;
   int sms = 0;

@@ -111,12 +111,14 @@ struct BatchArgs {
 
 // returns 0 on success, else an sp24_status value; batch == nullptr: one problem.
 // index != nullptr (one problem only): the metadata comes from the canonical index
-// (M x K/32 words, pitch ldi) and meta is not read.
+// (M x K/32 words, pitch ldi) and meta is not read.  diag_stall_ns != 0: the give-up
+// self-test (the kernel's TMA producer issues no copies and every wait gives up after
+// diag_stall_ns nanoseconds, setting the timeout bit of *status).
 int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K,
                  const void* values, int64_t ldv, const void* meta, const void* B, int64_t ldb,
                  const void* C, int64_t ldc, void* D, int64_t ldd, void* workspace,
                  int32_t* status, int num_sms, cudaStream_t s, const BatchArgs* batch = nullptr,
-                 const uint32_t* index = nullptr, int64_t ldi = 0);
+                 const uint32_t* index = nullptr, int64_t ldi = 0, uint64_t diag_stall_ns = 0);
 
 // Up to kMaxGroupPerLaunch validated, non-empty float problems in one launch (the caller
 // splits longer lists); returns 0 or an sp24_status value.

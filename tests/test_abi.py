@@ -210,6 +210,8 @@ def test_no_device_means_no_cpu_fallback():
     assert _mma_index() == NODEV
     assert _mma_index(index=FAKE_ODD, ldi=6) == NODEV  # any 4-byte aligned index and pitch
     assert sp.lib().sp24_diag_wait_timeout(FAKE, 1000, None) == NODEV
+    assert sp.lib().sp24_diag_mma_stall(BF16, 256, 256, 256, FAKE, 128, FAKE, FAKE, 256, FAKE,
+                                        256, 1000, FAKE, None) == NODEV
 
 
 S4, U4 = 8, 9
@@ -319,3 +321,13 @@ def test_header_is_plain_c_and_cpp(tmp_path):
         r = subprocess.run([compiler, std, "-Wall", "-Wextra", "-pedantic", "-fsyntax-only",
                             "-x", lang, HEADER], capture_output=True, text=True)
         assert r.returncode == 0, r.stderr
+
+
+def test_gemm_give_up_self_test_validates_before_the_device():
+    L = sp.lib()
+    args = (256, 256, 256, FAKE, 128, FAKE, FAKE, 256, FAKE, 256)
+    assert L.sp24_diag_mma_stall(S8, *args, 1000, FAKE, None) == UNSUPPORTED  # float only
+    assert L.sp24_diag_mma_stall(BF16, *args, 0, FAKE, None) == INVALID       # no limit
+    assert L.sp24_diag_mma_stall(BF16, *args, 2_000_000_000, FAKE, None) == INVALID
+    assert L.sp24_diag_mma_stall(BF16, *args, 1000, None, None) == INVALID    # no status word
+    assert L.sp24_diag_mma_stall(BF16, 256, 256, 100, *args[3:], 1000, FAKE, None) == INVALID

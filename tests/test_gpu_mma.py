@@ -173,6 +173,33 @@ def test_bounded_wait_gives_up_and_context_survives():
     assert float(x.sum()) == 8.0
 
 
+@pytest.mark.parametrize("ta,N", [("bf16", 256),   # CTA pair, 256 x 256 tiles
+                                  ("bf16", 96),    # CTA pair, 256 x 128 tiles
+                                  ("e4m3", 96),    # one CTA, 128 x 128 tiles
+                                  ("bf16", 16)])   # one CTA, 128 x 32 tiles
+def test_gemm_gives_up_when_operands_never_arrive(ta, N):
+    """The product kernel itself, with its TMA producer issuing nothing: the MMA thread's
+    bounded wait gives up, every role stops, SP24_DEV_TIMEOUT is set, and the context stays
+    usable -- a following ordinary product still matches the oracle."""
+    M, K = 256, 512
+    c = inputs.case(ta, ta, M, N, K, seed=11)
+    values, index, _ = gpu_compress(c, "mask")
+    meta = sp.meta_prepare(index, c["A"].dtype, M, K)
+    B = dev(c["B"])
+    D = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = sp.lib().sp24_diag_mma_stall(sp.DTYPE_CODES[c["A"].dtype], M, N, K, sp._ptr(values),
+                                      values.stride(0), sp._ptr(meta), sp._ptr(B), B.stride(0),
+                                      sp._ptr(D), D.stride(0), 20_000_000, sp._ptr(status),
+                                      sp._stream())
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert status.item() & sp.DEV_TIMEOUT
+    assert torch.all(D == 7.0)  # the epilogue never ran
+    # the context is still usable: the same problem through sp24_mma matches the oracle
+    run_case(c, mode="mask")
+
+
 # ---- full-size workloads, compared on sampled rows --------------------------------------
 
 def test_full_size_bf16_4096():
