@@ -505,9 +505,13 @@ def gpu_arm(args, world, rank, local):
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} in the timed region")
     ms_step = total_ms / args.steps
-    # per-kernel breakdown: the same steps again with events around each kernel
+    # per-kernel breakdown: the same steps again with events around each kernel.  The GPU
+    # first spins for a while so that every launch is enqueued before the first one runs:
+    # events then time the kernels, not the host's launch rate (a kernel of a few us is
+    # shorter than one Python iteration of this loop).
     n_bd = max(3, min(args.steps, 200))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_bd)]
+    torch.cuda._sleep(int(n_bd * 400_000))  # ~0.2 ms of GPU clock per step to enqueue
     for i in range(n_bd):
         launch(sets[i % len(sets)], evs[i])
     torch.cuda.synchronize(dev)

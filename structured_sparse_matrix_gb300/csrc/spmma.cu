@@ -122,8 +122,8 @@ struct Geo {
   // pair: 512 threads launch with 128 registers each; the producer / MMA warpgroup and
   // the writer warpgroup give theirs down to kRegsLight so the two epilogue warpgroups
   // can hold the drained accumulator (kRegsEpi); the shares add up to at most the launch's
-  static constexpr uint32_t kRegsLight = ESZ == 1 ? 56 : 48;  // FP8 writers hold 32 B/stage
-  static constexpr uint32_t kRegsEpi = ESZ == 1 ? 192 : 200;
+  static constexpr uint32_t kRegsLight = 56;
+  static constexpr uint32_t kRegsEpi = 200;
   static_assert(!kPair || (kRegsLight * 256 + kRegsEpi * 256 <= 65536u), "register split");
   static_assert(kAccCols + kStages * kMmas * kSlotCols <= int(kTmemCols), "TMEM budget");
   static_assert(kSmemBytes <= 232448 - 512, "shared memory budget");
@@ -616,10 +616,10 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
           tc_fence_after();
           d_tmem = tmem + uint32_t(abuf * G::kTileN);
         }
-        for (int kb = 0; kb < num_kb; ++kb, ++q) {
+        int kc = 0;  // stage within an integer chunk (kb % p.chunk, counted)
+        for (int kb = 0; kb < num_kb; ++kb, ++q, kc = (kc + 1 == p.chunk) ? 0 : kc + 1) {
           const int s = q % kStages;
           const uint32_t par = (q / kStages) & 1;
-          const int kc = (OUT == 2) ? kb % p.chunk : 0;  // stage within an integer chunk
           if constexpr (OUT == 2) {
             if (kc == 0) {  // new chunk: next accumulator buffer
               abuf = G::kAccBufs == 1 ? 0 : (chunk & 1);

@@ -27,6 +27,14 @@ def sample_rows(M: int) -> np.ndarray:
     return np.array(sorted(rows), dtype=np.int64)
 
 
+def tile_quarter_rows(M: int) -> np.ndarray:
+    """One row from each 32-row quarter of every 128-row tile (the four lane quarters of
+    every CTA's accumulator), at a lane offset that varies from tile to tile."""
+    rows = [t * 128 + q * 32 + (t * 7 + q * 13) % 32
+            for t in range((M + 127) // 128) for q in range(4)]
+    return np.array([r for r in rows if r < M], dtype=np.int64)
+
+
 def bf16_ulp(x: np.ndarray) -> np.ndarray:
     ax = np.abs(x)
     e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))

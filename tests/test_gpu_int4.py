@@ -111,7 +111,8 @@ def test_meta4_uses_the_16_bit_layout():
     assert torch.equal(m4, m16)
 
 
-def _run4(ta, tb, M, N, K, seed, *, nib_a=None, nib_b=None, C=None, b_pitch=None, rows=None):
+def _run4(ta, tb, M, N, K, seed, *, nib_a=None, nib_b=None, C=None, b_pitch=None, rows=None,
+          by_index=False):
     mask = inputs.keep_mask(M, K, inputs.gen(seed + 1))
     if nib_a is None:
         nib_a = inputs.gen_nibbles((M, K), inputs.gen(seed))
@@ -126,6 +127,11 @@ def _run4(ta, tb, M, N, K, seed, *, nib_a=None, nib_b=None, C=None, b_pitch=None
                                 elem=ta)
     meta = sp.meta_prepare(index, ta, M, K)
     D = sp.mma(values, meta, _packed(nib_b, b_pitch), C.cuda(), a_elem=ta, b_elem=tb)
+    if by_index:  # the product on the canonical index must equal the one on the image
+        D_idx = sp.mma_index(values, index, _packed(nib_b, b_pitch), C.cuda(), a_elem=ta,
+                             b_elem=tb)
+        torch.cuda.synchronize()
+        assert torch.equal(D_idx, D)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     v_ref, i_ref, _ = oracle.compress(nib_a, ta, "mask", mask=mask.numpy())
@@ -144,6 +150,12 @@ def _run4(ta, tb, M, N, K, seed, *, nib_a=None, nib_b=None, C=None, b_pitch=None
                                    (257, 288, 320)])
 def test_mma4_exact(ta, tb, M, N, K):
     _run4(ta, tb, M, N, K, seed=M + N + K)
+
+
+@pytest.mark.parametrize("ta,tb,M,N,K", [("s4", "u4", 200, 96, 1056), ("u4", "s4", 33, 288, 8320)])
+def test_mma4_reads_the_canonical_index(ta, tb, M, N, K):
+    # ragged M and K; the second case spans two 8192-K exact chunks
+    _run4(ta, tb, M, N, K, seed=M + K, by_index=True)
 
 
 def test_mma4_ragged_n_through_a_padded_b():

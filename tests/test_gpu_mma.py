@@ -8,7 +8,7 @@ import torch
 import inputs
 import oracle
 import structured_sparse_matrix_gb300 as sp
-from parity import check_float, dev, gpu_compress, run_case, sample_rows
+from parity import check_float, dev, gpu_compress, run_case, sample_rows, tile_quarter_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -210,7 +210,7 @@ def test_full_size_bf16_4096():
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 def test_full_size_fp8_8192(fmt):
     c = inputs.fp8_square(fmt)
-    run_case(c, mode="mask", rows=sample_rows(c["M"])[::4])
+    run_case(c, mode="mask", rows=tile_quarter_rows(c["M"]))
 
 
 @pytest.mark.parametrize("N", [16, 128, 2048])
@@ -261,7 +261,7 @@ def test_int8_wraps_like_int32():
 @pytest.mark.parametrize("ta", ["s8", "u8"])
 def test_full_size_int8_8192(ta):
     c = inputs.int8_square(ta)
-    run_case(c, mode="mask", out_dtype=torch.int32, rows=sample_rows(c["M"])[::4])
+    run_case(c, mode="mask", out_dtype=torch.int32, rows=tile_quarter_rows(c["M"]))
 
 
 # ---- 16-bit C and D: the FP16- / BF16-accumulate forms and mixed accumulator types -------
@@ -441,9 +441,11 @@ def test_grouped_many_problems_and_empty_ones():
     ("e5m2", "e4m3", "f32", torch.float32, 300, 304, 800),   # FP8 pair, stage tail
     ("e4m3", "e4m3", None, torch.bfloat16, 64, 32, 256),     # FP8 narrow tiles
     ("s8", "s8", "s32", torch.int32, 190, 144, 1088),        # exact integers (16-bit layout)
+    ("u8", "s8", "s32", torch.int32, 130, 272, 2080),        # u8 x s8: 1024-K exact chunks
 ])
 def test_product_reads_the_canonical_index(ta, tb, tc, out, M, N, K):
-    c = inputs.case(ta, tb, M, N, K, seed=M + N, tc=tc, dist="full" if ta == "s8" else "normal")
+    c = inputs.case(ta, tb, M, N, K, seed=M + N, tc=tc,
+                    dist="full" if ta in ("s8", "u8") else "normal")
     run_case(c, mode="mask", out_dtype=out, by_index=True)
 
 
