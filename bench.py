@@ -300,7 +300,9 @@ def gpu_arm(args, world, rank, local):
 
     sets = [make_set(base)]
     # at least two sets, so that no step reads operands the step before it left in L2
-    while (len(sets) < 2 or len(sets) * set_bytes(sets[0]) < 3 * L2_BYTES) and len(sets) < 16:
+    # (--sets 1: one set, for profiler captures that save and restore device memory)
+    while (len(sets) < 2 or len(sets) * set_bytes(sets[0]) < 3 * L2_BYTES) and len(sets) < 16 \
+            and (args.sets == 0 or len(sets) < args.sets):
         # distinct contents per set: roll the rows (cheap, same distribution)
         c2 = dict(base)
         shift = 37 * len(sets)
@@ -684,6 +686,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="e4m3-8192", choices=sorted(CONFIGS))
+    ap.add_argument("--sets", type=int, default=0,
+                    help="input sets rotated through the steps (0: as many as keep the "
+                         "working set above three L2 sizes, at least two)")
     ap.add_argument("--min-seconds", type=float, default=1.0,
                     help="the timed region replays the K steps until it lasts this long")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
