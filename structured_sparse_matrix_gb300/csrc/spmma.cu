@@ -109,7 +109,10 @@ struct Geo {
   static constexpr int kBBytes = kAtoms * kAtomBytes;
   static constexpr int kStages = kNarrow ? 7 : 4;
   static constexpr int kStageBytes = kABytes + kBBytes;  // the metadata skips shared memory
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+  // CTA pairs: one 4 KiB staging box per epilogue warp (32 rows x 32 f32 columns) through
+  // which the epilogue's C tiles arrive and its D tiles leave by TMA
+  static constexpr int kStgBytes = kPair ? 8 * 4096 : 0;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kStgBytes + 1024;
   static constexpr int kAccBufs = (kPair && !kHalfN) ? 1 : 2;
   static constexpr int kAccCols = kAccBufs * kTileN;
   static constexpr uint32_t kMetaCol = kAccCols;              // slot set s at + s * 64
@@ -375,6 +378,70 @@ __device__ __forceinline__ void prefetch_c_row(const MmaParams& p, int row, int 
                      bytes);
 }
 
+// Byte offset of 16-byte piece j of row r inside a TMA box whose rows are kRowBytes long
+// (128: SWIZZLE_128B, 64: SWIZZLE_64B): the piece index is XOR-ed with address bits 7+.
+template <int kRowBytes>
+__device__ __forceinline__ uint32_t stg_offset(int r, int j) {
+  constexpr uint32_t kMask = kRowBytes == 128 ? 7u : 3u;
+  const uint32_t off = uint32_t(r * kRowBytes + j * 16);
+  return off ^ (((off >> 7) & kMask) << 4);
+}
+
+// Epilogue of one 32-column chunk of one 32-row block through a staging box in shared
+// memory: the thread of row `lane` adds its row of C (already in the box, in C's type)
+// to the accumulator values v and writes the row of D (in D's type) over it.
+template <int OUT>
+__device__ __forceinline__ void stage_chunk(uint8_t* stg, int lane, float (&v)[32], bool hasC,
+                                            int ctype, bool d_f16) {
+  if (hasC) {
+    if (ctype == 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 c = *reinterpret_cast<const float4*>(stg + stg_offset<128>(lane, j));
+        v[4 * j] += c.x;
+        v[4 * j + 1] += c.y;
+        v[4 * j + 2] += c.z;
+        v[4 * j + 3] += c.w;
+      }
+    } else {
+      const bool f16 = ctype == 2;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 u = *reinterpret_cast<const uint4*>(stg + stg_offset<64>(lane, j));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[8 * j + 2 * k] += half_bits_to_f32(w[k] & 0xFFFFu, f16);
+          v[8 * j + 2 * k + 1] += half_bits_to_f32(w[k] >> 16, f16);
+        }
+      }
+    }
+  }
+  if constexpr (OUT == 0) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(stg + stg_offset<128>(lane, j)) =
+          make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float a = v[8 * j + 2 * k], b = v[8 * j + 2 * k + 1];
+        if (d_f16) {
+          const __half2 h = __floats2half2_rn(a, b);
+          memcpy(&w[k], &h, 4);
+        } else {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+          memcpy(&w[k], &h, 4);
+        }
+      }
+      *reinterpret_cast<uint4*>(stg + stg_offset<64>(lane, j)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 // Integer epilogue for one 32-column chunk: D = sum + C (s32, nullable), wrapping.
 __device__ __forceinline__ void store_chunk_s32(const uint32_t* v, const MmaParams& p, int row,
                                                 int col0) {
@@ -483,6 +550,7 @@ __device__ __forceinline__ void problem_params(const MmaParams& p, const GroupTa
 // otherwise one problem, or a strided batch, with tensor maps tmA, tmB.
 template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN, bool kGrouped>
 __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                           const CUtensorMap* tmC, const CUtensorMap* tmD,
                                            const MmaParams& p,
                                            const uint32_t idesc, const GroupTable* gt) {
   using G = Geo<ESZ, kPair, kNarrow, kHalfN>;
@@ -493,6 +561,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
   // metadata writer warp of the pair has stored the stage's metadata into its TMEM slots
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], drain_bar;
+  __shared__ __align__(8) uint64_t stg_bar[8];  // CTA pairs: a C tile has reached a staging box
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -502,6 +571,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
   const int nunits = kPair ? int(gridDim.x >> 1) : int(gridDim.x);
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kABytes;
+  uint8_t* sStg = sB + kStages * G::kBBytes;  // 1024-byte aligned (stage sizes are)
   const int ntiles_total = kGrouped ? gt->tile_start[gt->count] : p.mtiles * p.ntiles * p.batch;
 
   if (threadIdx.x == 0) {
@@ -514,6 +584,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
       mbar_init(&acc_empty[b], G::kEpiWarps * (kPair ? 2 : 1));
     }
     mbar_init(&drain_bar, 1);
+    for (int w = 0; w < 8; ++w) mbar_init(&stg_bar[w], 1);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -855,6 +926,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
     const uint32_t acc_empty_addr =
         kPair ? mapa(&acc_empty[0], 0) : smem_addr(&acc_empty[0]);
     int local = 0, ichunk = 0;
+    uint32_t stg_phase = 0;  // C tiles this warp has loaded into its staging box
     for (int t = unit; t < ntiles_total; t += nunits, ++local) {
       int lt;
       const int g = tile_problem<kGrouped>(gt, t, lt);
@@ -947,7 +1019,46 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
           prefetch_c_row(pp2, mt2 * G::kTileM + int(rank) * 128 + quad * 32 + lane,
                          nt2 * G::kTileN + half * kCols, kCols, b2 * pp2.stride_c);
         }
-        if (row < pp.M) {
+        if (tmD != nullptr) {
+          // through this warp's staging box: C arrives by TMA, D leaves by TMA (rows and
+          // columns past M and N are zero-filled on the way in and not written on the way out)
+          uint8_t* stg = sStg + ew * 4096;
+          const int row0w = mt * G::kTileM + int(rank) * 128 + quad * 32;
+          const bool hasC = pp.C != nullptr;
+          const uint32_t cbytes = 32u * 32u * (pp.ctype == 0 ? 4u : 2u);
+          bool ok = true;
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            const int col = col0 + 32 * c;
+            if (col >= pp.N || row0w >= pp.M) break;
+            if (lane == 0) bulk_wait_read_all();  // the box's previous D has left
+            __syncwarp();
+            if (hasC) {
+              if (lane == 0) {
+                mbar_arrive_expect_tx(&stg_bar[ew], cbytes);
+                tma_load_3d(stg, tmC, &stg_bar[ew], col, row0w, b);
+              }
+              if (!mbar_wait(&stg_bar[ew], stg_phase & 1u, abort, pp.limit_ns)) {
+                // giving up: let the copy already issued land before the CTA ends
+                mbar_wait_drain(&stg_bar[ew], stg_phase & 1u, 2000000ull);
+                ok = false;
+                break;
+              }
+              ++stg_phase;
+            }
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = pp.K > 0 ? __uint_as_float(r[c][j]) : 0.f;
+            stage_chunk<OUT>(stg, lane, v, hasC, pp.ctype, pp.d_f16 != 0);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(tmD, stg, col, row0w, b);
+              bulk_commit_group();
+            }
+          }
+          if (!ok) break;
+        } else if (row < pp.M) {
 #pragma unroll
           for (int c = 0; c < kChunks; ++c)
             if (col0 + 32 * c < pp.N) store_row32<OUT>(r[c], pp, row, col0 + 32 * c, cofs, dofs);
@@ -986,6 +1097,9 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
         if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(abuf * sizeof(uint64_t)));
       }
     }
+    // this warp's TMA stores of D have completed before the CTA (and its shared memory) ends
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -1005,9 +1119,11 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
 template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN>
 __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
     spmma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ MmaParams p,
-                 const uint32_t idesc) {
-  spmma_body<ESZ, OUT, kPair, kNarrow, kHalfN, false>(&tmA, &tmB, p, idesc, nullptr);
+                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                 const __grid_constant__ MmaParams p, const uint32_t idesc, const int staged) {
+  // staged: the CTA-pair float epilogue moves C and D through shared memory by TMA
+  spmma_body<ESZ, OUT, kPair, kNarrow, kHalfN, false>(&tmA, &tmB, &tmC, staged ? &tmD : nullptr, p,
+                                                      idesc, nullptr);
 }
 
 // The problems of a group table, one persistent grid over all their tiles.
@@ -1015,7 +1131,8 @@ template <int ESZ, int OUT, bool kPair, bool kNarrow, bool kHalfN>
 __global__ void __launch_bounds__(Geo<ESZ, kPair, kNarrow, kHalfN>::kThreads, 1)
     spmma_grouped_kernel(const __grid_constant__ MmaParams p,
                          const __grid_constant__ GroupTable gt) {
-  spmma_body<ESZ, OUT, kPair, kNarrow, kHalfN, true>(nullptr, nullptr, p, 0u, &gt);
+  spmma_body<ESZ, OUT, kPair, kNarrow, kHalfN, true>(nullptr, nullptr, nullptr, nullptr, p, 0u,
+                                                     &gt);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1092,6 +1209,31 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
   }
   // the narrow variant loads only the B atoms that hold columns below N
   p.batoms = kNarrow ? (p.N + G::kAtomN - 1) / G::kAtomN : G::kAtoms;
+  // CTA-pair float products: C and D by TMA through the epilogue's staging boxes, 32 x 32
+  // elements (f32 rows of 128 bytes with 128-byte swizzle, 16-bit rows of 64 bytes with
+  // 64-byte swizzle)
+  CUtensorMap tC, tD;
+  memset(&tC, 0, sizeof(tC));
+  memset(&tD, 0, sizeof(tD));
+  int staged = 0;
+  if constexpr (kPair && OUT != 2) {
+    const uint64_t nb = uint64_t(p.batch);
+    const int dsz = OUT == 0 ? 4 : 2;
+    staged = make_tmap(&tD, p.D, dsz, uint64_t(p.N), uint64_t(p.M), uint64_t(p.ldd) * dsz, 32, 32,
+                       dsz == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, nb,
+                       uint64_t(p.stride_d) * dsz)
+                 ? 1
+                 : 0;
+    if (staged && p.C != nullptr) {
+      const int csz = p.ctype == 0 ? 4 : 2;
+      staged = make_tmap(&tC, p.C, csz, uint64_t(p.N), uint64_t(p.M), uint64_t(p.ldc) * csz, 32,
+                         32, csz == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, nb,
+                         uint64_t(p.stride_c) * csz)
+                   ? 1
+                   : 0;
+    }
+    if (!staged) return 4;
+  }
   auto kern = spmma_kernel<ESZ, OUT, kPair, kNarrow, kHalfN>;
   if constexpr (kPair)
     if (!register_split_fits<G>(kern)) return 4;
@@ -1126,7 +1268,7 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
   }
   if (tiles < units) units = tiles;
   cfg.gridDim = dim3(units * (kPair ? 2 : 1), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kern, tA, tB, p, idesc) != cudaSuccess) return 4;
+  if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tC, tD, p, idesc, staged) != cudaSuccess) return 4;
   return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 
