@@ -983,7 +983,53 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
           }
         }
         if (!ok) break;
-        if (row < pp.M) {
+        if (tmD != nullptr) {
+          // C (s32) in and D (s32) out by TMA through this warp's staging box, as the
+          // float epilogue does
+          uint8_t* stg = sStg + ew * 4096;
+          const int row0w = mt * G::kTileM + int(rank) * 128 + quad * 32;
+          const bool hasC = pp.C != nullptr;
+#pragma unroll
+          for (int c = 0; c < kIntCols / 32; ++c) {
+            const int col = nt * G::kTileN + cbase + c * 32;
+            if (col >= pp.N || row0w >= pp.M) break;
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            if (hasC) {
+              if (lane == 0) {
+                mbar_arrive_expect_tx(&stg_bar[ew], 32u * 32u * 4u);
+                tma_load_3d(stg, tmC, &stg_bar[ew], col, row0w, 0);
+              }
+              if (!mbar_wait(&stg_bar[ew], stg_phase & 1u, abort, pp.limit_ns)) {
+                mbar_wait_drain(&stg_bar[ew], stg_phase & 1u, 2000000ull);
+                ok = false;
+                break;
+              }
+              ++stg_phase;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint4* piece = reinterpret_cast<uint4*>(stg + stg_offset<128>(lane, j));
+              uint4 o = make_uint4(sum[c * 32 + 4 * j], sum[c * 32 + 4 * j + 1],
+                                   sum[c * 32 + 4 * j + 2], sum[c * 32 + 4 * j + 3]);
+              if (hasC) {  // two's-complement wrap
+                const uint4 cv = *piece;
+                o.x += cv.x;
+                o.y += cv.y;
+                o.z += cv.z;
+                o.w += cv.w;
+              }
+              *piece = o;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(tmD, stg, col, row0w, 0);
+              bulk_commit_group();
+            }
+          }
+          if (!ok) break;
+        } else if (row < pp.M) {
 #pragma unroll
           for (int c = 0; c < kIntCols / 32; ++c) {
             const int col0 = nt * G::kTileN + cbase + c * 32;
@@ -1209,16 +1255,16 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
   }
   // the narrow variant loads only the B atoms that hold columns below N
   p.batoms = kNarrow ? (p.N + G::kAtomN - 1) / G::kAtomN : G::kAtoms;
-  // CTA-pair float products: C and D by TMA through the epilogue's staging boxes, 32 x 32
-  // elements (f32 rows of 128 bytes with 128-byte swizzle, 16-bit rows of 64 bytes with
-  // 64-byte swizzle)
+  // CTA-pair products: C and D by TMA through the epilogue's staging boxes, 32 x 32
+  // elements (f32 / s32 rows of 128 bytes with 128-byte swizzle, 16-bit rows of 64 bytes
+  // with 64-byte swizzle)
   CUtensorMap tC, tD;
   memset(&tC, 0, sizeof(tC));
   memset(&tD, 0, sizeof(tD));
   int staged = 0;
-  if constexpr (kPair && OUT != 2) {
+  if constexpr (kPair) {
     const uint64_t nb = uint64_t(p.batch);
-    const int dsz = OUT == 0 ? 4 : 2;
+    const int dsz = OUT == 1 ? 2 : 4;  // f32 or s32 D: 4 bytes
     staged = make_tmap(&tD, p.D, dsz, uint64_t(p.N), uint64_t(p.M), uint64_t(p.ldd) * dsz, 32, 32,
                        dsz == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, nb,
                        uint64_t(p.stride_d) * dsz)
