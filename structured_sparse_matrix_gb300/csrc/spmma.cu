@@ -82,6 +82,7 @@ struct MmaParams {
   int64_t stride_meta;         // (bytes)
   const uint32_t* index;       // or, for one problem, the canonical index itself (M x K/32
   int64_t ldi;                 // words, pitch ldi); then meta is unused
+  int idx_vec;                 // index base 16-byte aligned and ldi % 4 == 0: 16-byte loads
   uint64_t limit_ns;
   int diag_stall;  // self-test: the TMA producer issues nothing, so every wait gives up
 };
@@ -831,6 +832,15 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
           const int kw = p.K / 32;  // canonical words per row
           if constexpr (ESZ == 2) {
             const int ra = c.row0 + r16;
+            if (p.idx_vec && c.kb * 4 + 4 <= kw && ra + 8 < p.M) {
+              // the stage's 4 words of each row are 16 contiguous bytes
+              const uint4 lo = __ldg(reinterpret_cast<const uint4*>(p.index + int64_t(ra) * p.ldi + c.kb * 4));
+              const uint4 hi =
+                  __ldg(reinterpret_cast<const uint4*>(p.index + int64_t(ra + 8) * p.ldi + c.kb * 4));
+              w[0] = lo.x, w[1] = lo.y, w[2] = lo.z, w[3] = lo.w;
+              w[4] = hi.x, w[5] = hi.y, w[6] = hi.z, w[7] = hi.w;
+              return;
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int col = c.kb * 4 + j;
@@ -841,6 +851,14 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
             }
           } else {
             const int r = c.row0 + lrow;
+            if (p.idx_vec && c.kb * 8 + 8 <= kw && r < p.M) {
+              // the stage's 8 words of the row are 32 contiguous bytes
+              const uint4* src = reinterpret_cast<const uint4*>(p.index + int64_t(r) * p.ldi + c.kb * 8);
+              const uint4 a = __ldg(src), b = __ldg(src + 1);
+              w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w;
+              w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
+              return;
+            }
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const int col = c.kb * 8 + i;
@@ -1477,6 +1495,7 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   memset(&p, 0, sizeof(p));
   p.index = index;  // canonical index instead of the image (one problem only)
   p.ldi = ldi;
+  p.idx_vec = (index != nullptr && reinterpret_cast<uintptr_t>(index) % 16 == 0 && ldi % 4 == 0) ? 1 : 0;
   BatchStrides bs{0, 0, 0};
   p.batch = 1;
   if (batch != nullptr && batch->count > 1) {
