@@ -4,9 +4,10 @@ One step = one pass of the whole path over one batch of synthetic input:
     sp24_compress_meta (compression and the metadata image in one pass, mask mode)
     ->  sp24_mma (D = A_sp B + C)
 (--pass separate: sp24_compress -> sp24_meta_prepare -> sp24_mma; --pass index:
-sp24_compress -> sp24_mma_index.)  The K timed steps are independent; by default their
-compressions and products run on two streams so that step i+1's compression overlaps
-step i's product (--serial: one stream).
+sp24_compress -> sp24_mma_index.)  The K timed steps are independent: they run either
+with their compressions and products on two streams, so that step i+1's compression
+overlaps step i's product, or back to back on one stream with the product overlapping the
+compression's tail; by default the faster of the two in an untimed probe (--schedule).
 Default workload: the largest single-GPU configuration, FP8 E4M3 M = N = K = 8192, keep
 mask drawn per group from the six two-of-four patterns, A, B ~ N(0,1) scaled per tensor to
 the format's range, no C, f32 output (--config bf16-4096 and the others stay selectable).
@@ -422,11 +423,12 @@ def gpu_arm(args, world, rank, local):
     # the K steps recorded once as a CUDA graph (launch overhead off the timed path; the
     # GEMM's programmatic dependency on the pass before it becomes a graph edge); eager
     # launches if capture is refused
-    # Schedules: "overlapped" (the default) runs the steps' compressions on one stream and
-    # their products on another, so step i+1's compression fills the SMs that step i's
-    # product leaves idle in its last wave; "serial" runs each step's two calls back to
-    # back on one stream (the product launched to overlap the compression's tail).
-    overlap = not args.serial
+    # Schedules: "overlapped" runs the steps' compressions on one stream and their products
+    # on another, so step i+1's compression fills the SMs that step i's product leaves idle
+    # in its last wave; "serial" runs each step's two calls back to back on one stream (the
+    # product launched to overlap the compression's tail).  "auto" (the default) times one
+    # untimed probe of each before the timed region and keeps the faster for the workload.
+    schedule = "serial" if args.serial else args.schedule
 
     def capture(overlapped):
         g = torch.cuda.CUDAGraph()
@@ -443,37 +445,50 @@ def gpu_arm(args, world, rank, local):
         torch.cuda.synchronize(dev)
         return g
 
-    graph = graph_serial = None
+    graphs = {"overlapped": None, "serial": None}
     if not args.eager:
         try:
-            graph = capture(overlap)
-            graph_serial = capture(False) if overlap else graph
+            for name in graphs:
+                graphs[name] = capture(name == "overlapped")
         except Exception as exc:  # noqa: BLE001 - any capture failure means eager timing
             log(f"graph capture failed, timing eager launches: {exc}")
             torch.cuda.synchronize(dev)
-            graph = graph_serial = None
+            graphs = {"overlapped": None, "serial": None}
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} during warm-up")
 
-    def run_k_steps():
+    def run_schedule(name):
         # the K steps back to back, no events between the kernels (the GEMM may start
         # during the previous kernel's tail)
-        if graph is not None:
-            graph.replay()
-        elif overlap:
+        if graphs[name] is not None:
+            graphs[name].replay()
+        elif name == "overlapped":
             launch_overlapped(args.steps)
         else:
             for i in range(args.steps):
                 launch(sets[i % len(sets)])
 
-    # replays in the timed region: enough for at least --min-seconds (one untimed probe)
-    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    p0.record(stream)
-    run_k_steps()
-    p1.record(stream)
-    torch.cuda.synchronize(dev)
-    probe_ms = max(p0.elapsed_time(p1), 1e-3)
-    replays = int(max(1, min(100000, -(-args.min_seconds * 1e3 // probe_ms))))
+    def probe(name, reps=3):
+        # median ms of `reps` untimed runs of the K steps in one schedule
+        out = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run_schedule(name)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            out.append(a.elapsed_time(b))
+        return max_over_ranks(statistics.median(out), world)
+
+    probe_ms = {name: probe(name) for name in ("overlapped", "serial")}
+    if schedule == "auto":
+        schedule = min(probe_ms, key=probe_ms.get)
+
+    def run_k_steps():
+        run_schedule(schedule)
+
+    # replays in the timed region: enough for at least --min-seconds
+    replays = int(max(1, min(100000, -(-args.min_seconds * 1e3 // max(probe_ms[schedule], 1e-3)))))
     replays = int(max_over_ranks(float(replays), world))
 
     # timed region: `replays` replays of the K steps, each bracketed by events
@@ -491,19 +506,6 @@ def gpu_arm(args, world, rank, local):
     rep_ms = [a.elapsed_time(b) for a, b in ev_rep]
     total_ms = max_over_ranks(statistics.median(rep_ms), world)
     timed_s = max_over_ranks(sum(rep_ms) * 1e-3, world)
-    # the serial schedule's step time, for comparison (same steps, one stream)
-    ms_step_serial = None
-    if overlap:
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        if graph_serial is not None:
-            graph_serial.replay()
-        else:
-            for i in range(args.steps):
-                launch(sets[i % len(sets)])
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        ms_step_serial = a.elapsed_time(b) / args.steps
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} in the timed region")
     ms_step = total_ms / args.steps
@@ -566,7 +568,7 @@ def gpu_arm(args, world, rank, local):
         "note": "sp24_mma time includes the int8->bf16 widening pass" if integer else None,
         "sp24_mma_us": k_mma * 1e3,
         "sp24_mma_tflops": achieved_tf,
-        "step_us_serial_schedule": None if ms_step_serial is None else ms_step_serial * 1e3,
+        "step_us_probe": {name: ms * 1e3 / args.steps for name, ms in probe_ms.items()},
     }
     if fused:
         # + the image written (the separate pass would read the index and write the image)
@@ -660,16 +662,19 @@ def gpu_arm(args, world, rank, local):
                        "l2": f"{len(sets)} rotating input sets, "
                              f"{len(sets) * set_bytes(sets[0]) / 2**20:.0f} MiB > L2",
                        "parallelism": f"replicas x{world}",
-                       "launch": ("one CUDA graph of the K steps" if graph is not None
-                                  else "eager launches"),
+                       "launch": ("one CUDA graph of the K steps"
+                                  if graphs[schedule] is not None else "eager launches"),
                        "timing": (f"median over {replays} replays of the K steps, each "
                                   f"bracketed by CUDA events; {timed_s:.2f} s timed in all"),
                        "replays": replays,
                        "schedule": ("overlapped: the K independent steps run their "
                                     "compressions on one stream and their products on "
                                     "another, so step i+1's compression overlaps step i's "
-                                    "product" if overlap else
-                                    "serial: each step's calls back to back on one stream")},
+                                    "product" if schedule == "overlapped" else
+                                    "serial: each step's calls back to back on one stream, "
+                                    "the product overlapping the compression's tail")
+                                   + ("; chosen as the faster of the two in an untimed probe"
+                                      if args.schedule == "auto" and not args.serial else "")},
             "roofline": roof,
             "kernels": kernels,
             "cpu_baseline": cpu,
@@ -694,9 +699,11 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--serial", action="store_true",
-                    help="run each step's calls back to back on one stream (by default step "
-                         "i+1's compression runs on its own stream during step i's product)")
+    ap.add_argument("--schedule", default="auto", choices=["auto", "overlapped", "serial"],
+                    help="overlapped: step i+1's compression on its own stream during step "
+                         "i's product; serial: each step's calls back to back on one stream; "
+                         "auto: the faster of the two in an untimed probe")
+    ap.add_argument("--serial", action="store_true", help="same as --schedule serial")
     ap.add_argument("--eager", action="store_true",
                     help="launch the timed steps one by one instead of as a CUDA graph")
     ap.add_argument("--pass", dest="pass_mode", default="fused",
