@@ -509,10 +509,15 @@ def gpu_arm(args, world, rank, local):
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} in the timed region")
     ms_step = total_ms / args.steps
-    # per-kernel breakdown: the same steps again with events around each kernel.  The GPU
-    # first spins for a while so that every launch is enqueued before the first one runs:
-    # events then time the kernels, not the host's launch rate (a kernel of a few us is
-    # shorter than one Python iteration of this loop).
+    # per-kernel breakdown, two ways.  (1) Isolated: the same steps again with events
+    # around each kernel; the GPU first spins for a while so that every launch is enqueued
+    # before the first one runs (events then time the kernels, not the host's launch rate),
+    # and each kernel's time includes its launch and ramp-up, which the timed steps overlap
+    # with the kernel before (programmatic dependent launch).  (2) Back to back: one CUDA
+    # graph of n launches of the kernel alone, each on its own operands (rotated through
+    # enough copies that the launches' operands together exceed three L2 sizes, so no launch
+    # reads what an earlier one left in L2), events around the graph, time / n: the
+    # kernel's steady-state duration as a sequence of layers issues it.
     n_bd = max(3, min(args.steps, 200))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_bd)]
     torch.cuda._sleep(int(n_bd * 400_000))  # ~0.2 ms of GPU clock per step to enqueue
@@ -524,9 +529,68 @@ def gpu_arm(args, world, rank, local):
     k_mma = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     value = flops * world / (ms_step * 1e-3) / 1e12
 
-    # --- roofline of the dominant kernel (sp24_mma): tensor-bound sparse contraction
+    def nbytes(t):
+        return 0 if t is None else t.numel() * t.element_size()
+
+    def rotation(keys):
+        # the sets, plus copies of the tensors `keys` of them, until the launches' operands
+        # exceed three L2 sizes
+        per = sum(nbytes(sets[0][k]) for k in keys)
+        want = max(2, -(-3 * L2_BYTES // max(per, 1)))
+        rot = [dict(x) for x in sets]
+        while len(rot) < want:
+            src = sets[len(rot) % len(sets)]
+            rot.append(dict(src, **{k: (None if src[k] is None else src[k].clone())
+                                    for k in keys}))
+        return rot
+
+    def back_to_back(call, rot, n):
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(n):
+                if call(rot[i % len(rot)], sp._stream(cap)) != 0:
+                    raise RuntimeError("sp24 call failed")
+        stream.wait_stream(cap)
+        g.replay()  # untimed: uploads the graph
+        torch.cuda.synchronize(dev)
+        out = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            out.append(a.elapsed_time(b) / n)
+        del g
+        return statistics.median(out)
+
+    n_b2b = max(8, min(args.steps, 60))
+    prod_keys = ["values", "index" if by_index else "meta", "B", "C", "D"]
+    comp_keys = ["A", "mask", "values", "index"] + ([] if by_index else ["meta"])
+    b2b_mma = b2b_compress = None
+    if not args.eager:
+        try:
+            rot = rotation(prod_keys)
+            b2b_mma = back_to_back(product_call, rot, n_b2b)
+            del rot
+            if fused or by_index:
+                rot = rotation(comp_keys)
+                b2b_compress = back_to_back(compress_call, rot, n_b2b)
+                del rot
+            torch.cuda.empty_cache()
+        except Exception as exc:  # noqa: BLE001 - capture refused: isolated times only
+            log(f"back-to-back timing skipped: {exc}")
+            torch.cuda.synchronize(dev)
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} in the per-kernel timing")
+
+    # --- rooflines.  The product: a tensor-bound sparse contraction, or HBM-bound when its
+    # intensity is below the ridge (skinny N); the compression pass: HBM-bound.
     peaks, src = load_peaks()
     dense = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     # 8-bit integers run widened to bf16: their roof is the bf16 sparse rate
     dense_peak = dense * (FP8_OVER_BF16 if ta in ("e4m3", "e5m2") else 1.0)
     peak = dense_peak * SPARSE_OVER_DENSE
@@ -537,48 +601,78 @@ def gpu_arm(args, world, rank, local):
     mma_bytes = (M * K // 2 * esz + M * K // 8 + K * N * esz +
                  (M * N * 4 if base["C"] is not None else 0) + M * N * osz)
     unit = "TOP/s" if integer else "TFLOP/s"
-    achieved_tf = flops / (k_mma * 1e-3) / 1e12
     intensity = flops / mma_bytes
-    ridge = peak * 1e12 / (peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]) * 1e9)
-    if intensity >= ridge:
-        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": peak, "unit": unit,
-                "frac": achieved_tf / peak}
-    else:
-        gbs = mma_bytes / (k_mma * 1e-3) / 1e9
-        hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm}
-    roof["traffic"] = profile_traffic(args.config)
-    roof["kernel"] = "sp24_mma (spmma_kernel)"
-    roof["timing"] = (f"CUDA events around each kernel over {n_bd} steps run right after the "
-                      "timed region on the same stream and inputs (events between the kernels "
-                      "inside the timed region would serialise the GEMM's programmatic launch)")
-    roof["algorithmic_bytes"] = mma_bytes
-    if roof["bound"] == "tensor":
-        roof["peak_source"] = (f"{src}: bf16 dense {dense} TFLOP/s"
-                               f"{' x2 (fp8/bf16 nominal)' if ta in ('e4m3', 'e5m2') else ''}"
-                               " x2 (2:4 sparse / dense nominal), burst figure"
-                               f"{'; int8 runs exactly on the bf16 path' if integer else ''}")
-    else:
-        roof["peak_source"] = (f"{src}: HBM copy bandwidth; the product's intensity "
-                               f"{intensity:.0f} flop/B is below the sparse tensor ridge "
-                               f"{ridge:.0f} flop/B")
+    ridge = peak * 1e12 / (hbm * 1e9)
+    how_b2b = (f"CUDA events around one graph of {n_b2b} back-to-back launches of the kernel "
+               "alone on rotating operands (together > 3 L2 sizes), time / launches, median "
+               "of 5 replays")
+    how_iso = (f"CUDA events around each kernel over {n_bd} steps run right after the timed "
+               "region (each time includes the kernel's launch and ramp-up)")
+
+    def mma_roof(ms, how):
+        tf = flops / (ms * 1e-3) / 1e12
+        if intensity >= ridge:
+            r = {"bound": "tensor", "achieved": tf, "peak": peak, "unit": unit, "frac": tf / peak,
+                 "peak_source": (f"{src}: bf16 dense {dense} TFLOP/s"
+                                 f"{' x2 (fp8/bf16 nominal)' if ta in ('e4m3', 'e5m2') else ''}"
+                                 " x2 (2:4 sparse / dense nominal), burst figure"
+                                 f"{'; int8 runs exactly on the bf16 path' if integer else ''}")}
+        else:
+            gbs = mma_bytes / (ms * 1e-3) / 1e9
+            r = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                 "peak_source": (f"{src}: HBM copy bandwidth; the product's intensity "
+                                 f"{intensity:.0f} flop/B is below the sparse tensor ridge "
+                                 f"{ridge:.0f} flop/B")}
+        r.update({"traffic": profile_traffic(args.config), "kernel": "sp24_mma (spmma_kernel)",
+                  "us": ms * 1e3, "timing": how, "algorithmic_bytes": mma_bytes})
+        return r
+
     # compression kernel: HBM-bound, algorithmic bytes = A + mask read, values + index written
     cbytes = M * K * esz + (M * K if mode == "mask" else 0) + M * K // 2 * esz + M * K // 8
+    # the fused pass also writes the metadata image (at its information size)
+    fbytes = cbytes + (M * K // 8 if fused else 0)
+    cname = ("sp24_compress_meta (compress_meta_kernel)" if fused else
+             "sp24_compress (compress_kernel)")
+
+    def comp_roof(ms, how):
+        gbs = fbytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                "traffic": None, "kernel": cname, "us": ms * 1e3, "timing": how,
+                "algorithmic_bytes": fbytes, "peak_source": f"{src}: HBM copy bandwidth"}
+
+    mma_ms, mma_how = (b2b_mma, how_b2b) if b2b_mma is not None else (k_mma, how_iso)
+    roof_mma = mma_roof(mma_ms, mma_how)
+    roof_comp = None
+    if fused or by_index:
+        c_ms, c_how = ((b2b_compress, how_b2b) if b2b_compress is not None
+                       else (k_compress, how_iso))
+        roof_comp = comp_roof(c_ms, c_how)
+    # the line's roofline is the dominant kernel's: the one that takes longer
+    roof = roof_mma
+    if roof_comp is not None and roof_comp["us"] > roof_mma["us"]:
+        roof = roof_comp
     kernels = {
         "note": "sp24_mma time includes the int8->bf16 widening pass" if integer else None,
         "sp24_mma_us": k_mma * 1e3,
-        "sp24_mma_tflops": achieved_tf,
+        "sp24_mma_us_back_to_back": None if b2b_mma is None else b2b_mma * 1e3,
+        "sp24_mma_tflops": flops / (mma_ms * 1e-3) / 1e12,
+        "sp24_mma_roofline": roof_mma,
         "step_us_probe": {name: ms * 1e3 / args.steps for name, ms in probe_ms.items()},
     }
     if fused:
-        # + the image written (the separate pass would read the index and write the image)
-        fbytes = cbytes + M * K // 8  # + the metadata image at its information size
         kernels["sp24_compress_meta_us"] = k_compress * 1e3
-        kernels["sp24_compress_meta_gbs"] = fbytes / (k_compress * 1e-3) / 1e9
+        kernels["sp24_compress_meta_us_back_to_back"] = (None if b2b_compress is None
+                                                         else b2b_compress * 1e3)
+        kernels["sp24_compress_meta_gbs"] = roof_comp["achieved"]
+        kernels["sp24_compress_meta_roofline"] = roof_comp
     else:
         kernels["sp24_compress_us"] = k_compress * 1e3
         kernels["sp24_compress_gbs"] = cbytes / (k_compress * 1e-3) / 1e9
-        if not by_index:
+        if by_index:
+            kernels["sp24_compress_us_back_to_back"] = (None if b2b_compress is None
+                                                        else b2b_compress * 1e3)
+            kernels["sp24_compress_roofline"] = roof_comp
+        else:
             kernels["sp24_meta_prepare_us"] = k_meta * 1e3
 
     # --- end to end through the C ABI with host buffers: every step copies its inputs from

@@ -75,6 +75,8 @@ struct MmaParams {
   int batoms;    // B boxes loaded per stage and CTA (the narrow variant skips empty ones)
   int M, N, K;
   int mtiles, ntiles, num_kb;  // tiles of the variant (128 or 256 rows, 128 or 256 cols)
+  int img_kb;                  // metadata image stages per 128-row tile (a stage of the
+                               // narrow 16-bit variant spans two)
   int band_rows;               // tile order: bands of this many rows of D, swept along N
   int batch;                   // problems of equal shape; problem b's C / D start at
   int64_t stride_c, stride_d;  // C + b * stride_c, D + b * stride_d (elements)
@@ -91,14 +93,22 @@ struct MmaParams {
 // 256 x 128 tiles and double-buffered accumulators (16-bit operands with 32 < N <= 128),
 // single (128 x 128 tiles: FP8 with 32 < N <= 128) and narrow (128 x 32 tiles for
 // N <= 32: B staged in 32-byte swizzle atoms, so a stage holds only the columns that
-// exist and seven stages fit in shared memory).
+// exist).  A narrow product moves little data per MMA, so its stages are as long as the
+// MMA thread's and the metadata writers' fixed cost per stage allows to hide: 16-bit
+// operands take two image stages (256 dense K, 8 MMAs, two boxes of A) per stage, and
+// three such stages fill the TMEM columns left for metadata slots.
 template <int ESZ, bool kPair, bool kNarrow = false, bool kHalfN = false>
 struct Geo {
-  static constexpr int kStageK = ESZ == 2 ? 128 : 256;       // dense K per stage
+  static constexpr int kImgStageK = ESZ == 2 ? 128 : 256;    // dense K per image stage
+  static constexpr int kImgPer = (kNarrow && ESZ == 2) ? 2 : 1;  // image stages per stage
+  static constexpr int kStageK = kImgStageK * kImgPer;        // dense K per stage
   static constexpr int kMmaK = ESZ == 2 ? 32 : 64;            // dense K per MMA
-  static constexpr int kMmas = kStageK / kMmaK;               // 4
-  static constexpr int kMetaWords = ESZ == 1 ? 8 : 4;        // per TMEM lane and stage
-  static constexpr int kMetaBytes = 128 * 4 * kMetaWords;     // image block: 2 / 4 KB
+  static constexpr int kMmas = kStageK / kMmaK;               // 4 (narrow 16-bit: 8)
+  static constexpr int kImgWords = ESZ == 1 ? 8 : 4;          // per TMEM lane, image stage
+  static constexpr int kImgBytes = 128 * 4 * kImgWords;       // image block: 2 / 4 KB
+  static constexpr int kMetaWords = kImgPer * kImgWords;      // per TMEM lane and stage
+  static constexpr int kABoxes = kImgPer;                     // 128 x 128-byte A boxes
+  static constexpr int kAStage = kABoxes * kABytes;           // compressed A per stage
   static constexpr int kTileM = kPair ? 256 : 128;
   static constexpr int kTileN = kPair ? (kHalfN ? 128 : 256) : (kNarrow ? 32 : 128);
   static constexpr int kBCols = kPair ? kTileN / 2 : kTileN;  // B columns staged per CTA
@@ -108,8 +118,8 @@ struct Geo {
   static constexpr int kAtoms = kBCols / kAtomN;
   static constexpr int kAtomBytes = kStageK * kAtomInner;     // one B box
   static constexpr int kBBytes = kAtoms * kAtomBytes;
-  static constexpr int kStages = kNarrow ? 7 : 4;
-  static constexpr int kStageBytes = kABytes + kBBytes;  // the metadata skips shared memory
+  static constexpr int kStages = kNarrow ? (kImgPer == 2 ? 3 : 7) : 4;
+  static constexpr int kStageBytes = kAStage + kBBytes;  // the metadata skips shared memory
   // CTA pairs: one 4 KiB staging box per epilogue warp (32 rows x 32 f32 columns) through
   // which the epilogue's C tiles arrive and its D tiles leave by TMA
   static constexpr int kStgBytes = kPair ? 8 * 4096 : 0;
@@ -131,6 +141,9 @@ struct Geo {
   static_assert(!kPair || (kRegsLight * 256 + kRegsEpi * 256 <= 65536u), "register split");
   static_assert(kAccCols + kStages * kMmas * kSlotCols <= int(kTmemCols), "TMEM budget");
   static_assert(kSmemBytes <= 232448 - 512, "shared memory budget");
+  // one CTA per SM: a product launched early behind another (programmatic dependent
+  // launch) never shares an SM, and so its TMEM, with a CTA of the one before it
+  static_assert(2 * kSmemBytes > 232448, "one CTA per SM");
   static_assert(kAtoms >= 1, "B atoms");
 };
 
@@ -491,7 +504,7 @@ struct GroupTable {
   const uint8_t* meta[kMaxGroup];
   int count;
   int tile_start[kMaxGroup + 1];  // problem g owns launch tiles tile_start[g] .. [g+1]-1
-  int M[kMaxGroup], N[kMaxGroup], K[kMaxGroup], num_kb[kMaxGroup];
+  int M[kMaxGroup], N[kMaxGroup], K[kMaxGroup], num_kb[kMaxGroup], img_kb[kMaxGroup];
   int mtiles[kMaxGroup], ntiles[kMaxGroup], batoms[kMaxGroup];
   uint32_t idesc[kMaxGroup];
   const void* C[kMaxGroup];
@@ -526,6 +539,7 @@ __device__ __forceinline__ void problem_params(const MmaParams& p, const GroupTa
     q.N = gt->N[g];
     q.K = gt->K[g];
     q.num_kb = gt->num_kb[g];
+    q.img_kb = gt->img_kb[g];
     q.mtiles = gt->mtiles[g];
     q.ntiles = gt->ntiles[g];
     q.batoms = gt->batoms[g];
@@ -571,7 +585,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
   const int unit = kPair ? int(blockIdx.x >> 1) : int(blockIdx.x);
   const int nunits = kPair ? int(gridDim.x >> 1) : int(gridDim.x);
   uint8_t* sA = smem;
-  uint8_t* sB = sA + kStages * kABytes;
+  uint8_t* sB = sA + kStages * G::kAStage;
   uint8_t* sStg = sB + kStages * G::kBBytes;  // 1024-byte aligned (stage sizes are)
   const int ntiles_total = kGrouped ? gt->tile_start[gt->count] : p.mtiles * p.ntiles * p.batch;
 
@@ -610,9 +624,13 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &abort_flag;
-  // the prologue above may overlap the previous kernel on the stream (programmatic
-  // dependent launch); nothing below runs before that kernel's writes are visible
-  griddep_wait();
+  // Programmatic dependent launch: the prologue above may overlap the kernel before this
+  // one on the stream, and the next product on the stream may start its own prologue on
+  // SMs this grid leaves free or frees (a CTA of it cannot share an SM with one of this
+  // grid: each takes more than half of the shared memory).  Every role that touches
+  // global memory first waits (griddep_wait) until the kernel before has completed and its
+  // writes are visible; the MMA thread touches none.
+  griddep_launch_dependents();
 
   // Roles by warpgroup (the pair variant re-divides the register file per warpgroup, so
   // each role's code sits under its warpgroup's setmaxnreg)
@@ -620,6 +638,30 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
     if constexpr (kPair) regs_dec<G::kRegsLight>();
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && !p.diag_stall && unit < ntiles_total) {
+      // While the kernel before may still run, pull this CTA's first stages into L2.  L2
+      // is where every write of that kernel lands, so a line fetched early is updated by
+      // those writes; the loads below read it only after the wait.
+      int lt;
+      const int g = tile_problem<kGrouped>(gt, unit, lt);
+      MmaParams qg;
+      problem_params<kGrouped>(p, gt, g, qg);
+      const MmaParams& pp = kGrouped ? qg : p;
+      const CUtensorMap* mA = kGrouped ? &gt->a[g] : tmA;
+      const CUtensorMap* mB = kGrouped ? &gt->b[g] : tmB;
+      int b, mt, nt;
+      batch_tile<G::kTileM>(pp, lt, b, mt, nt);
+      const int mt128 = kPair ? mt * 2 + int(rank) : mt;
+      const int bcol = nt * G::kTileN + int(rank) * G::kBCols;
+      for (int kb = 0; kb < pp.num_kb && kb < kStages; ++kb) {
+        const int kx = kb * (G::kStageK / 2);
+        for (int i = 0; i < G::kABoxes; ++i)
+          if (2 * (kx + i * (128 / ESZ)) < pp.K) tma_prefetch_3d(mA, kx + i * (128 / ESZ), mt128 * 128, b);
+        for (int a = 0; a < G::kAtoms; ++a)
+          if (a < pp.batoms) tma_prefetch_3d(mB, bcol + a * G::kAtomN, kb * G::kStageK, b);
+      }
+    }
+    griddep_wait();
     if (lane == 0 && !p.diag_stall) {
       int q = 0;
       for (int t = unit; t < ntiles_total && !*abort; t += nunits) {
@@ -634,22 +676,30 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
         batch_tile<G::kTileM>(pp, lt, b, mt, nt);
         const int mt128 = kPair ? mt * 2 + int(rank) : mt;  // this CTA's 128-row tile
         const int bcol = nt * G::kTileN + int(rank) * G::kBCols;
-        const uint32_t tx = uint32_t(kABytes + pp.batoms * G::kAtomBytes) * (kPair ? 2u : 1u);
+        const uint32_t btx = uint32_t(pp.batoms * G::kAtomBytes);
         for (int kb = 0; kb < pp.num_kb; ++kb, ++q) {
           const int s = q % kStages;
           if (!mbar_wait(&empty_bar[s], ((q / kStages) & 1) ^ 1u, abort, p.limit_ns)) break;
-          if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], tx);
-          const int kx = kb * (G::kStageK / 2);
+          const int kx = kb * (G::kStageK / 2);  // compressed elements
+          // boxes of A that hold any K (the last stage of a ragged K may need fewer)
+          int nbox = 1;
+          if constexpr (G::kABoxes > 1)
+            while (nbox < G::kABoxes && 2 * (kx + nbox * (128 / ESZ)) < pp.K) ++nbox;
+          if (rank == 0)
+            mbar_arrive_expect_tx(&full_bar[s],
+                                  (uint32_t(nbox * kABytes) + btx) * (kPair ? 2u : 1u));
           if constexpr (kPair) {
             const uint32_t fb = mapa(&full_bar[s], 0);
-            tma_load_3d_pair(sA + s * kABytes, mA, fb, kx, mt128 * 128, b);
+            tma_load_3d_pair(sA + s * G::kAStage, mA, fb, kx, mt128 * 128, b);
 #pragma unroll
             for (int a = 0; a < G::kAtoms; ++a)
               if (a < pp.batoms)
                 tma_load_3d_pair(sB + s * G::kBBytes + a * G::kAtomBytes, mB, fb,
                                  bcol + a * G::kAtomN, kb * G::kStageK, b);
           } else {
-            tma_load_3d(sA + s * kABytes, mA, &full_bar[s], kx, mt128 * 128, b);
+            for (int i = 0; i < nbox; ++i)
+              tma_load_3d(sA + s * G::kAStage + i * kABytes, mA, &full_bar[s],
+                          kx + i * (128 / ESZ), mt128 * 128, b);
 #pragma unroll
             for (int a = 0; a < G::kAtoms; ++a)
               if (a < pp.batoms)
@@ -713,7 +763,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
           }
           tc_fence_after();
           const uint32_t e_tmem = tmem + G::kMetaCol + uint32_t(s * G::kMmas * kSlotCols);
-          const uint32_t a_saddr = smem_addr(sA + s * kABytes);
+          const uint32_t a_saddr = smem_addr(sA + s * G::kAStage);
           const uint32_t b_saddr = smem_addr(sB + s * G::kBBytes);
           const int k0 = kb * G::kStageK;
           const int first = (OUT == 2) ? kc : kb;  // accumulate unless the chunk/tile starts
@@ -721,17 +771,24 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
             // the whole stage in one sequence, testing the next stage's barrier meanwhile
             // (MMA j: A 32 bytes further along K, B kMmaK rows further, metadata slot j)
             const int qn = q + 1;
-            ready = mma_stage_test_next<kPair, ESZ == 1>(
-                smem_addr(&full_bar[qn % kStages]), uint32_t((qn / kStages) & 1), d_tmem,
-                smem_desc(a_saddr, adesc_hi), smem_desc(b_saddr, bdesc_hi), 32u / 16u,
-                uint32_t(G::kMmaK * G::kAtomInner / 16), e_tmem, id, first > 0 ? 1u : 0u,
-                smem_addr(&empty_bar[s]));
+            if constexpr (G::kMmas == 8)  // narrow 16-bit: two boxes of A, 8 MMAs
+              ready = mma_stage8_test_next(
+                  smem_addr(&full_bar[qn % kStages]), uint32_t((qn / kStages) & 1), d_tmem,
+                  smem_desc(a_saddr, adesc_hi), smem_desc(b_saddr, bdesc_hi), 32u / 16u,
+                  uint32_t(kABytes / 16), uint32_t(G::kMmaK * G::kAtomInner / 16), e_tmem, id,
+                  first > 0 ? 1u : 0u, smem_addr(&empty_bar[s]));
+            else
+              ready = mma_stage_test_next<kPair, ESZ == 1>(
+                  smem_addr(&full_bar[qn % kStages]), uint32_t((qn / kStages) & 1), d_tmem,
+                  smem_desc(a_saddr, adesc_hi), smem_desc(b_saddr, bdesc_hi), 32u / 16u,
+                  uint32_t(G::kMmaK * G::kAtomInner / 16), e_tmem, id, first > 0 ? 1u : 0u,
+                  smem_addr(&empty_bar[s]));
           } else {  // the last, partial stage of a ragged K
             ready = false;
 #pragma unroll
             for (int j = 0; j < G::kMmas; ++j) {
               if (k0 + j * G::kMmaK < kdense) {
-                const uint64_t ad = smem_desc(a_saddr + 32 * j, adesc_hi);
+                const uint64_t ad = smem_desc(a_saddr + (j / 4) * kABytes + 32 * (j % 4), adesc_hi);
                 const uint64_t bd = smem_desc(b_saddr + j * G::kMmaK * G::kAtomInner, bdesc_hi);
                 const uint32_t acc = (first > 0 || j > 0) ? 1u : 0u;
                 if constexpr (kPair)
@@ -793,7 +850,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
     // a cursor over this CTA's stages in the producer's order: tile t, stage kb of num_kb,
     // the tile's first row and the address of this lane's image words of that stage
     struct Cursor {
-      int t, kb, num_kb, row0;
+      int t, kb, num_kb, img_kb, row0;
       const uint4* src;
     };
     auto seek = [&](Cursor& c, int t) {  // first stage of tile t or a later one
@@ -809,76 +866,104 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
         const int mt128 = kPair ? mt * 2 + int(rank) : mt;
         c.kb = 0;
         c.num_kb = pp.num_kb;
+        c.img_kb = pp.img_kb;
         c.row0 = mt128 * 128;
         c.src = pp.meta == nullptr
                     ? nullptr
                     : reinterpret_cast<const uint4*>(pp.meta + b * pp.stride_meta +
-                                                     int64_t(mt128) * pp.num_kb * G::kMetaBytes) +
-                          lrow * (G::kMetaWords / 4);
+                                                     int64_t(mt128) * pp.img_kb * G::kImgBytes) +
+                          lrow * (G::kImgWords / 4);
         return;
       }
     };
     auto next = [&](Cursor& c) {
-      if (c.src != nullptr) c.src += G::kMetaBytes / 16;
+      if (c.src != nullptr) c.src += G::kImgPer * G::kImgBytes / 16;
       if (++c.kb == c.num_kb) seek(c, c.t + nunits);
     };
     auto writers = [&](auto index_mode) {
       constexpr bool kIdx = decltype(index_mode)::value;
       constexpr int kAhead = kIdx ? 2 : 4;         // stages of words held in registers
-      constexpr int kW = kIdx ? 8 : G::kMetaWords;  // words per lane and stage
+      // words per lane and stage: the image's, or the canonical words they are made of
+      // (16-bit: one word per MMA of each of the lane's two rows; FP8: two words per MMA of
+      // the lane's row)
+      constexpr int kW = kIdx ? 2 * G::kMmas : G::kMetaWords;
       auto load = [&](const Cursor& c, uint32_t (&w)[kW]) {
         if (c.t >= ntiles_total) return;
         if constexpr (kIdx) {
           const int kw = p.K / 32;  // canonical words per row
           if constexpr (ESZ == 2) {
+            constexpr int kR = G::kMmas;  // words of each row in the stage
             const int ra = c.row0 + r16;
-            if (p.idx_vec && c.kb * 4 + 4 <= kw && ra + 8 < p.M) {
-              // the stage's 4 words of each row are 16 contiguous bytes
-              const uint4 lo = __ldg(reinterpret_cast<const uint4*>(p.index + int64_t(ra) * p.ldi + c.kb * 4));
-              const uint4 hi =
-                  __ldg(reinterpret_cast<const uint4*>(p.index + int64_t(ra + 8) * p.ldi + c.kb * 4));
-              w[0] = lo.x, w[1] = lo.y, w[2] = lo.z, w[3] = lo.w;
-              w[4] = hi.x, w[5] = hi.y, w[6] = hi.z, w[7] = hi.w;
+            if (p.idx_vec && c.kb * kR + kR <= kw && ra + 8 < p.M) {
+              // the stage's words of each row are contiguous 16-byte vectors
+              const uint4* lo = reinterpret_cast<const uint4*>(p.index + int64_t(ra) * p.ldi + c.kb * kR);
+              const uint4* hi = reinterpret_cast<const uint4*>(p.index + int64_t(ra + 8) * p.ldi + c.kb * kR);
+#pragma unroll
+              for (int v = 0; v < kR / 4; ++v) {
+                const uint4 x = __ldg(lo + v), y = __ldg(hi + v);
+                w[4 * v] = x.x, w[4 * v + 1] = x.y, w[4 * v + 2] = x.z, w[4 * v + 3] = x.w;
+                w[kR + 4 * v] = y.x, w[kR + 4 * v + 1] = y.y, w[kR + 4 * v + 2] = y.z,
+                           w[kR + 4 * v + 3] = y.w;
+              }
               return;
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int col = c.kb * 4 + j;
+            for (int j = 0; j < kR; ++j) {
+              const int col = c.kb * kR + j;
               w[j] = (col < kw && ra < p.M) ? __ldg(p.index + int64_t(ra) * p.ldi + col) : kPadWord;
-              w[4 + j] = (col < kw && ra + 8 < p.M)
-                             ? __ldg(p.index + int64_t(ra + 8) * p.ldi + col)
-                             : kPadWord;
+              w[kR + j] = (col < kw && ra + 8 < p.M)
+                              ? __ldg(p.index + int64_t(ra + 8) * p.ldi + col)
+                              : kPadWord;
             }
           } else {
             const int r = c.row0 + lrow;
-            if (p.idx_vec && c.kb * 8 + 8 <= kw && r < p.M) {
-              // the stage's 8 words of the row are 32 contiguous bytes
-              const uint4* src = reinterpret_cast<const uint4*>(p.index + int64_t(r) * p.ldi + c.kb * 8);
-              const uint4 a = __ldg(src), b = __ldg(src + 1);
-              w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w;
-              w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
+            if (p.idx_vec && c.kb * kW + kW <= kw && r < p.M) {
+              // the stage's words of the row are contiguous 16-byte vectors
+              const uint4* src = reinterpret_cast<const uint4*>(p.index + int64_t(r) * p.ldi + c.kb * kW);
+#pragma unroll
+              for (int v = 0; v < kW / 4; ++v) {
+                const uint4 x = __ldg(src + v);
+                w[4 * v] = x.x, w[4 * v + 1] = x.y, w[4 * v + 2] = x.z, w[4 * v + 3] = x.w;
+              }
               return;
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int col = c.kb * 8 + i;
+            for (int i = 0; i < kW; ++i) {
+              const int col = c.kb * kW + i;
               w[i] = (col < kw && r < p.M) ? __ldg(p.index + int64_t(r) * p.ldi + col) : kPadWord;
             }
           }
         } else {
+          // the lane's words of each image stage the kernel stage covers (past the last
+          // image stage of a ragged K: the pad pattern)
 #pragma unroll
-          for (int i = 0; i < kW / 4; ++i) {
-            const uint4 v = __ldg(c.src + i);
-            w[4 * i] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
+          for (int i = 0; i < G::kImgPer; ++i) {
+            const bool in = c.kb * G::kImgPer + i < c.img_kb;
+#pragma unroll
+            for (int v = 0; v < G::kImgWords / 4; ++v) {
+              const uint4 x = in ? __ldg(c.src + i * (G::kImgBytes / 16) + v)
+                                 : make_uint4(kPadWord, kPadWord, kPadWord, kPadWord);
+              uint32_t* o = w + i * G::kImgWords + 4 * v;
+              o[0] = x.x;
+              o[1] = x.y;
+              o[2] = x.z;
+              o[3] = x.w;
+            }
           }
         }
       };
       Cursor ld, wr;
       seek(ld, unit);
       wr = ld;
+      if constexpr (!kIdx) {
+        // the first stages' image blocks of the first tile into L2 before the wait (see
+        // the producer)
+        if (quad == 0 && lane == 0 && ld.t < ntiles_total) {
+          const int n = ld.img_kb < kStages * G::kImgPer ? ld.img_kb : kStages * G::kImgPer;
+          bulk_prefetch_l2(ld.src - lrow * (G::kImgWords / 4), uint32_t(n * G::kImgBytes));
+        }
+      }
+      griddep_wait();
       uint32_t buf[kAhead][kW];
 #pragma unroll
       for (int a = 0; a < kAhead; ++a) {
@@ -903,16 +988,16 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
           const uint32_t e = lanes + uint32_t(s * G::kMmas * kSlotCols);
           if constexpr (ESZ == 2) {  // kind::f16: one column per MMA
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < G::kMmas; ++j) {
               uint32_t x = buf[a][j];
               if constexpr (kIdx)
                 x = ((buf[a][j] >> (16 * h16)) & 0xFFFFu) |
-                    (((buf[a][4 + j] >> (16 * h16)) & 0xFFFFu) << 16);
+                    (((buf[a][G::kMmas + j] >> (16 * h16)) & 0xFFFFu) << 16);
               tc_st_32x32b_x1(e + j * kSlotCols, x);
             }
           } else {  // kind::f8f6f4: two columns per MMA
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < G::kMmas; ++j)
               tc_st_32x32b_x2(e + j * kSlotCols, buf[a][2 * j], buf[a][2 * j + 1]);
           }
           tc_wait_st();
@@ -939,6 +1024,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
   } else {
     if constexpr (kPair) regs_inc<G::kRegsEpi>();
     // ---------------------------------------------------------------- epilogue
+    griddep_wait();  // C is read and D written only after the kernel before has completed
     const int ew = warp - G::kEpiWarp0;
     const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 (hardware rule: warp id % 4)
     const uint32_t acc_empty_addr =
@@ -1256,6 +1342,7 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
   using G = Geo<ESZ, kPair, kNarrow, kHalfN>;
   p.mtiles = (p.M + G::kTileM - 1) / G::kTileM;
   p.ntiles = (p.N + G::kTileN - 1) / G::kTileN;
+  p.num_kb = (p.K + G::kStageK - 1) / G::kStageK;  // stages of this variant
   CUtensorMap tA, tB;
   memset(&tA, 0, sizeof(tA));
   memset(&tB, 0, sizeof(tB));
@@ -1388,7 +1475,8 @@ int run_grouped(MmaParams p, const sp24_mma_problem* pr, int count, uint32_t at,
     gt.M[g] = M;
     gt.N[g] = N;
     gt.K[g] = K;
-    gt.num_kb[g] = (K + stage_k - 1) / stage_k;
+    gt.num_kb[g] = (K + G::kStageK - 1) / G::kStageK;
+    gt.img_kb[g] = (K + stage_k - 1) / stage_k;
     gt.mtiles[g] = (M + G::kTileM - 1) / G::kTileM;
     gt.ntiles[g] = (N + G::kTileN - 1) / G::kTileN;
     gt.batoms[g] = kNarrow ? (N + G::kAtomN - 1) / G::kAtomN : G::kAtoms;
@@ -1520,7 +1608,8 @@ int launch_spmma(int ta, int tb, int tc, int td, int64_t M, int64_t N, int64_t K
   p.N = int(N);
   p.K = int(K);
   p.mtiles = p.ntiles = 0;
-  p.num_kb = int((K + stage_k(ta) - 1) / stage_k(ta));
+  p.img_kb = int((K + stage_k(ta) - 1) / stage_k(ta));  // metadata image stages per tile
+  p.num_kb = p.img_kb;  // the variant's own stage count is set at launch
   p.limit_ns = 1000000000ull;  // 1 s per wait
   p.band_rows = band_rows_for(N);
   if (diag_stall_ns != 0) {  // give-up self-test: no copies, short waits
