@@ -87,23 +87,26 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-# the sources sp24_mma's kernel is built from (its ncu summary is stale once they change)
+# the sources each kernel is built from (its ncu summary is stale once they change)
 SPMMA_SOURCES = ("spmma.cu", "sp24_device.cuh", "sp24_internal.h")
+COMPRESS_SOURCES = ("compress.cu", "sp24_device.cuh", "sp24_internal.h")
 
 
-def source_hash() -> str:
+def source_hash(sources=SPMMA_SOURCES) -> str:
     h = hashlib.sha256()
     cs = os.path.join(ROOT, "structured_sparse_matrix_gb300", "csrc")
-    for name in SPMMA_SOURCES:
+    for name in sources:
         with open(os.path.join(cs, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def profile_traffic(config: str):
-    """DRAM bytes per sp24_mma launch from the committed ncu summary of this workload,
-    or None when no summary exists or the kernel sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"spmma_{config}.txt")
+def profile_traffic(config: str, kernel: str = "spmma"):
+    """DRAM bytes per launch of a kernel ("spmma" or "compress_meta") from the committed
+    ncu summary of this workload, or None when no summary exists or the kernel's sources
+    changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{config}.txt")
+    sources = SPMMA_SOURCES if kernel == "spmma" else COMPRESS_SOURCES
     try:
         fields = {}
         with open(path) as f:
@@ -111,7 +114,7 @@ def profile_traffic(config: str):
                 if ":" in line:
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip()
-        if fields.get("source_hash") != source_hash():
+        if fields.get("source_hash") != source_hash(sources):
             return None
         return float(fields["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -637,7 +640,8 @@ def gpu_arm(args, world, rank, local):
     def comp_roof(ms, how):
         gbs = fbytes / (ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                "traffic": None, "kernel": cname, "us": ms * 1e3, "timing": how,
+                "traffic": profile_traffic(args.config, "compress_meta") if fused else None,
+                "kernel": cname, "us": ms * 1e3, "timing": how,
                 "algorithmic_bytes": fbytes, "peak_source": f"{src}: HBM copy bandwidth"}
 
     mma_ms, mma_how = (b2b_mma, how_b2b) if b2b_mma is not None else (k_mma, how_iso)

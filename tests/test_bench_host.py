@@ -32,14 +32,23 @@ def test_clock_summary_without_samples():
 
 def test_profile_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     (tmp_path / "profiles").mkdir()
-    (tmp_path / "profiles" / "spmma_demo.txt").write_text(
-        "# title\nsource_hash: abc123\ndram_bytes_per_launch: 4096\n")
+    for kernel in ("spmma", "compress_meta"):
+        (tmp_path / "profiles" / f"{kernel}_demo.txt").write_text(
+            "# title\nsource_hash: abc123\ndram_bytes_per_launch: 4096\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "source_hash", lambda: "abc123")
+    monkeypatch.setattr(bench, "source_hash", lambda sources=bench.SPMMA_SOURCES: "abc123")
     assert bench.profile_traffic("demo") == 4096.0
-    monkeypatch.setattr(bench, "source_hash", lambda: "changed")
+    assert bench.profile_traffic("demo", "compress_meta") == 4096.0
+    monkeypatch.setattr(bench, "source_hash", lambda sources=bench.SPMMA_SOURCES: "changed")
     assert bench.profile_traffic("demo") is None     # kernel changed since the capture
+    assert bench.profile_traffic("demo", "compress_meta") is None
     assert bench.profile_traffic("missing") is None
+
+
+def test_each_kernel_is_hashed_from_its_own_sources():
+    assert "spmma.cu" in bench.SPMMA_SOURCES and "compress.cu" not in bench.SPMMA_SOURCES
+    assert "compress.cu" in bench.COMPRESS_SOURCES and "spmma.cu" not in bench.COMPRESS_SOURCES
+    assert bench.source_hash() != bench.source_hash(bench.COMPRESS_SOURCES)
 
 
 def test_committed_gemm_profiles_name_their_command_and_counters():

@@ -32,9 +32,12 @@ def test_small_ragged_shapes(ta, M, N, K):
 
 
 @pytest.mark.parametrize("ta", ["f16", "bf16"])
-@pytest.mark.parametrize("M,N,K", [(130, 24, 256), (64, 8, 128), (300, 16, 2080)])
+@pytest.mark.parametrize("M,N,K", [(130, 24, 256), (64, 8, 128), (300, 16, 2080),
+                                   (130, 16, 480), (129, 32, 4256)])
 def test_skinny_outputs(ta, M, N, K):
-    # N <= 32 runs on 128 x 32 tiles that stage only the B columns below N
+    # N <= 32 runs on 128 x 32 tiles that stage only the B columns below N; 16-bit
+    # operands take 256 dense K (two boxes of A, eight MMAs) per stage, so K = 480 and
+    # 4256 end on a stage whose second box is partly past K
     c = inputs.case(ta, ta, M, N, K, seed=M + N + K, tc="f32")
     run_case(c, mode="mask")
     run_case(dict(c, C=None, tc=None), mode="mask", out_dtype=torch.bfloat16)
@@ -435,6 +438,7 @@ def test_grouped_many_problems_and_empty_ones():
 
 @pytest.mark.parametrize("ta,tb,tc,out,M,N,K", [
     ("bf16", "bf16", "f32", torch.float32, 200, 16, 352),    # narrow tiles, ragged M and K
+    ("f16", "f16", "f32", torch.float32, 150, 24, 480),      # narrow: last stage's 2nd box
     ("f16", "f16", None, torch.bfloat16, 130, 96, 160),      # 256 x 128 pair tiles
     ("bf16", "bf16", "bf16", torch.float32, 257, 272, 1056),  # 256 x 256 pair tiles
     ("e4m3", "e4m3", None, torch.float32, 131, 80, 544),     # FP8, 128 x 128 tiles
@@ -449,8 +453,10 @@ def test_product_reads_the_canonical_index(ta, tb, tc, out, M, N, K):
     run_case(c, mode="mask", out_dtype=out, by_index=True)
 
 
-def test_canonical_index_with_a_padded_pitch():
-    M, N, K = 250, 64, 480
+@pytest.mark.parametrize("N", [64, 16])
+def test_canonical_index_with_a_padded_pitch(N):
+    # a pitch of K/32 + 3 words: the writers load the words one by one
+    M, K = 250, 480
     c = inputs.case("bf16", "bf16", M, N, K, seed=17, tc="f32")
     values, index, _ = gpu_compress(c, "mask")
     wide = torch.full((M, K // 32 + 3), -1, dtype=torch.int32, device="cuda")
