@@ -14,7 +14,7 @@ the format's range, no C, f32 output (--config bf16-4096 and the others stay sel
 The metric is dense-equivalent TFLOP/s (TOP/s for integers) = 2 M N K / step time.
 Timing: the K steps are recorded once (a CUDA graph); the graph is replayed R times, each
 replay bracketed by CUDA events, R chosen so that the timed region lasts at least
---min-seconds (1 s by default), and the step time is the median replay time / K.
+--min-seconds (2 s by default), and the step time is the median replay time / K.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 Prints ONE JSON line (rank 0).  For N > 1 it runs under torch.distributed.run, one rank
@@ -792,7 +792,7 @@ def main():
     ap.add_argument("--sets", type=int, default=0,
                     help="input sets rotated through the steps (0: as many as keep the "
                          "working set above three L2 sizes, at least two)")
-    ap.add_argument("--min-seconds", type=float, default=1.0,
+    ap.add_argument("--min-seconds", type=float, default=2.0,
                     help="the timed region replays the K steps until it lasts this long")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
