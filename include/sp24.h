@@ -28,6 +28,14 @@
  *     the stream has synchronised.  The library never clears that word.
  *   - There is no CPU fallback: without an sm_103 device every compute call returns
  *     SP24_ERR_NO_DEVICE.
+ *   - Stream order is kept as for any kernel, with one refinement: the products
+ *     (sp24_mma*) are launched with programmatic stream serialisation, so a product
+ *     may be placed on the GPU and run its set-up (shared-memory barriers, tensor-memory
+ *     allocation) while the kernel before it on the stream is still running, and the next
+ *     product on the stream may do the same while it runs.  A product reads or writes
+ *     global memory only after the kernel before it has completed and its writes are
+ *     visible, except that it may ask for the first part of its own A operand, metadata
+ *     and B to be fetched into the L2 cache earlier (a hint with no effect on results).
  */
 #ifndef SP24_H
 #define SP24_H
