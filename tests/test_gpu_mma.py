@@ -472,3 +472,59 @@ def test_llm_layer_through_the_index():
     c = inputs.llm_layer(16)
     run_case(c, mode="magnitude", out_dtype=torch.bfloat16, rows=sample_rows(c["M"]),
              by_index=True)
+
+
+# ---- products back to back on one stream, the second reading the first's output --------
+
+@pytest.mark.parametrize("N", [16, 288])          # narrow tiles; 256 x 256 pair tiles
+@pytest.mark.parametrize("graph", [False, True])
+def test_layers_chained_on_one_stream(N, graph):
+    # Y1 = W1 X, then Y2 = W2 Y1 + Y0, enqueued back to back with no synchronisation: the
+    # second product takes the first's output as its B.  Products overlap their launch and
+    # set-up with the kernel before them and fetch their first stages into L2 early, so this
+    # checks that the second one reads Y1 only once the first has written all of it (Y1
+    # and Y2 start out holding huge values, which would show up in any early read).
+    M1, K1, M2 = 384, 512, 320
+    c1 = inputs.case("bf16", "bf16", M1, N, K1, seed=N + 1, tc=None)
+    c2 = inputs.case("bf16", "bf16", M2, N, M1, seed=N + 2, tc="f32")
+    v1, i1, s1 = gpu_compress(c1, "mask")
+    v2, i2, s2 = gpu_compress(c2, "mask")
+    m1 = sp.meta_prepare(i1, torch.bfloat16, M1, K1)
+    m2 = sp.meta_prepare(i2, torch.bfloat16, M2, M1)
+    X, Y0 = dev(c1["B"]), dev(c2["C"])
+    Y1 = torch.empty((M1, N), dtype=torch.bfloat16, device="cuda")
+    Y2 = torch.empty((M2, N), dtype=torch.float32, device="cuda")
+
+    def poison():
+        Y1.fill_(3.0e38)
+        Y2.fill_(-3.0e38)
+
+    def layers():
+        sp.mma(v1, m1, X, None, out=Y1)
+        sp.mma(v2, m2, Y1, Y0, out=Y2)
+
+    if graph:
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                layers()
+        torch.cuda.current_stream().wait_stream(side)
+        for _ in range(2):
+            poison()
+            g.replay()
+    else:
+        poison()
+        layers()
+    torch.cuda.synchronize()
+    assert int(s1.item()) == 0 and int(s2.item()) == 0
+    # layer 1 against the oracle; layer 2 against the oracle applied to the Y1 the GPU made
+    va, ia, _ = oracle.compress(inputs.bits(c1["A"]), "bf16", "mask", mask=c1["mask"].numpy())
+    R1, S1 = oracle.mma_f64(va, ia, inputs.bits(c1["B"]), None, "bf16", "bf16", K1)
+    check_float(Y1.float().cpu().numpy(), R1, S1, "bf16", "layer 1")
+    vb, ib, _ = oracle.compress(inputs.bits(c2["A"]), "bf16", "mask", mask=c2["mask"].numpy())
+    R2, S2 = oracle.mma_f64(vb, ib, inputs.bits(Y1.cpu()), inputs.bits(c2["C"]), "bf16", "bf16",
+                            M1, tc="f32")
+    check_float(Y2.cpu().numpy(), R2, S2, None, "layer 2")
