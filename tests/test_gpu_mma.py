@@ -98,6 +98,7 @@ def test_padded_leading_dimensions_and_ragged_N(ta):
 @pytest.mark.parametrize("ta,tb,M,N,K", [("bf16", "bf16", 200, 304, 384),   # pair tiles
                                         ("f16", "f16", 130, 96, 256),     # single tiles
                                         ("e4m3", "e5m2", 257, 16, 512),   # narrow tiles
+                                        ("bf16", "bf16", 257, 16, 480),   # narrow, 256-K stages
                                         ("bf16", "bf16", 64, 272, 0)])    # K = 0: D = C
 def test_strided_batch(ta, tb, M, N, K):
     # four problems of one shape in one launch, each against the oracle, and bit for bit
@@ -415,6 +416,8 @@ def _grouped_case(ta, shapes, tc, out, seed):
      torch.float32),
     # widest N <= 32: narrow tiles, each problem its own MMA N
     ("e4m3", [(1000, 16, 512), (200, 32, 256), (64, 32, 1024)], None, torch.bfloat16),
+    # the same with 16-bit operands (256-K stages; each problem its own ragged last stage)
+    ("bf16", [(500, 16, 480), (130, 24, 256), (64, 8, 96)], "f32", torch.float32),
     # 32 < widest N <= 128, 16-bit: 256 x 128 pair tiles; FP8: 128 x 128 single tiles
     ("f16", [(700, 104, 384), (129, 40, 128), (256, 128, 2048)], "f16", torch.float16),
     ("e5m2", [(700, 112, 512), (129, 48, 256)], "f32", torch.float32),
