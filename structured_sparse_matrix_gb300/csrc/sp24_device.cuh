@@ -425,9 +425,11 @@ __device__ __forceinline__ bool mma_stage_test_next(uint32_t next_bar, uint32_t 
   return ok != 0;
 }
 
-// The same for a stage of eight cta_group::1 kind::f16 MMAs whose A spans two 128-byte
-// swizzle boxes: MMAs 0-3 read A at a0 + j * a_step, MMAs 4-7 at a0 + a_box +
-// (j - 4) * a_step; B at b0 + j * b_step; metadata at e0 + 16 j.
+// The same for a stage of eight kind::f16 MMAs whose A spans two 128-byte swizzle boxes:
+// MMAs 0-3 read A at a0 + j * a_step, MMAs 4-7 at a0 + a_box + (j - 4) * a_step; B at
+// b0 + j * b_step; metadata at e0 + 16 j.  kPair: cta_group::2 with the commit multicast to
+// both CTAs of the pair; otherwise cta_group::1 and a commit to the local barrier.
+template <bool kPair>
 __device__ __forceinline__ bool mma_stage8_test_next(uint32_t next_bar, uint32_t next_par,
                                                      uint32_t d, uint64_t a0, uint64_t b0,
                                                      uint32_t a_step, uint32_t a_box,
@@ -435,38 +437,50 @@ __device__ __forceinline__ bool mma_stage8_test_next(uint32_t next_bar, uint32_t
                                                      uint32_t idesc, uint32_t acc0,
                                                      uint32_t empty_bar) {
   uint32_t ok;
-  asm volatile(
-      "{\n"
-      ".reg .pred pn, pa, pt;\n"
-      ".reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7, sa, sx, sb;\n"
-      ".reg .b32 e1, e2, e3, e4, e5, e6, e7;\n"
-      "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n"
-      "setp.ne.b32 pa, %11, 0;\n"
-      "setp.eq.b32 pt, %2, %2;\n"
-      "cvt.u64.u32 sa, %6;\n"
-      "cvt.u64.u32 sx, %7;\n"
-      "cvt.u64.u32 sb, %8;\n"
-      "add.s64 a1, %4, sa;\n add.s64 a2, a1, sa;\n add.s64 a3, a2, sa;\n"
-      "add.s64 a4, %4, sx;\n add.s64 a5, a4, sa;\n add.s64 a6, a5, sa;\n add.s64 a7, a6, sa;\n"
-      "add.s64 b1, %5, sb;\n add.s64 b2, b1, sb;\n add.s64 b3, b2, sb;\n"
-      "add.s64 b4, b3, sb;\n add.s64 b5, b4, sb;\n add.s64 b6, b5, sb;\n add.s64 b7, b6, sb;\n"
-      "add.u32 e1, %9, 16;\n add.u32 e2, %9, 32;\n add.u32 e3, %9, 48;\n"
-      "add.u32 e4, %9, 64;\n add.u32 e5, %9, 80;\n add.u32 e6, %9, 96;\n add.u32 e7, %9, 112;\n"
-      "tcgen05.mma.sp.cta_group::1.kind::f16 [%3], %4, %5, [%9], %10, pa;\n"
-      "tcgen05.mma.sp.cta_group::1.kind::f16 [%3], a1, b1, [e1], %10, pt;\n"
-      "tcgen05.mma.sp.cta_group::1.kind::f16 [%3], a2, b2, [e2], %10, pt;\n"
-      "tcgen05.mma.sp.cta_group::1.kind::f16 [%3], a3, b3, [e3], %10, pt;\n"
-      "tcgen05.mma.sp.cta_group::1.kind::f16 [%3], a4, b4, [e4], %10, pt;\n"
-      "tcgen05.mma.sp.cta_group::1.kind::f16 [%3], a5, b5, [e5], %10, pt;\n"
-      "tcgen05.mma.sp.cta_group::1.kind::f16 [%3], a6, b6, [e6], %10, pt;\n"
-      "tcgen05.mma.sp.cta_group::1.kind::f16 [%3], a7, b7, [e7], %10, pt;\n"
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n"
-      "selp.b32 %0, 1, 0, pn;\n"
-      "}\n"
-      : "=r"(ok)
-      : "r"(next_bar), "r"(next_par), "r"(d), "l"(a0), "l"(b0), "r"(a_step), "r"(a_box),
-        "r"(b_step), "r"(e0), "r"(idesc), "r"(acc0), "r"(empty_bar)
-      : "memory");
+#define SP24_STAGE8_ASM(GROUP, COMMIT)                                                        \
+  asm volatile(                                                                              \
+      "{\n"                                                                                  \
+      ".reg .pred pn, pa, pt;\n"                                                             \
+      ".reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7, sa, sx, sb;\n"      \
+      ".reg .b32 e1, e2, e3, e4, e5, e6, e7;\n"                                              \
+      "mbarrier.test_wait.parity.shared::cta.b64 pn, [%1], %2;\n"                            \
+      "setp.ne.b32 pa, %11, 0;\n"                                                            \
+      "setp.eq.b32 pt, %2, %2;\n"                                                            \
+      "cvt.u64.u32 sa, %6;\n"                                                                \
+      "cvt.u64.u32 sx, %7;\n"                                                                \
+      "cvt.u64.u32 sb, %8;\n"                                                                \
+      "add.s64 a1, %4, sa;\n add.s64 a2, a1, sa;\n add.s64 a3, a2, sa;\n"                   \
+      "add.s64 a4, %4, sx;\n add.s64 a5, a4, sa;\n add.s64 a6, a5, sa;\n"                   \
+      "add.s64 a7, a6, sa;\n"                                                                \
+      "add.s64 b1, %5, sb;\n add.s64 b2, b1, sb;\n add.s64 b3, b2, sb;\n"                   \
+      "add.s64 b4, b3, sb;\n add.s64 b5, b4, sb;\n add.s64 b6, b5, sb;\n"                   \
+      "add.s64 b7, b6, sb;\n"                                                                \
+      "add.u32 e1, %9, 16;\n add.u32 e2, %9, 32;\n add.u32 e3, %9, 48;\n"                    \
+      "add.u32 e4, %9, 64;\n add.u32 e5, %9, 80;\n add.u32 e6, %9, 96;\n"                    \
+      "add.u32 e7, %9, 112;\n"                                                               \
+      "tcgen05.mma.sp." GROUP ".kind::f16 [%3], %4, %5, [%9], %10, pa;\n"                   \
+      "tcgen05.mma.sp." GROUP ".kind::f16 [%3], a1, b1, [e1], %10, pt;\n"                   \
+      "tcgen05.mma.sp." GROUP ".kind::f16 [%3], a2, b2, [e2], %10, pt;\n"                   \
+      "tcgen05.mma.sp." GROUP ".kind::f16 [%3], a3, b3, [e3], %10, pt;\n"                   \
+      "tcgen05.mma.sp." GROUP ".kind::f16 [%3], a4, b4, [e4], %10, pt;\n"                   \
+      "tcgen05.mma.sp." GROUP ".kind::f16 [%3], a5, b5, [e5], %10, pt;\n"                   \
+      "tcgen05.mma.sp." GROUP ".kind::f16 [%3], a6, b6, [e6], %10, pt;\n"                   \
+      "tcgen05.mma.sp." GROUP ".kind::f16 [%3], a7, b7, [e7], %10, pt;\n" COMMIT            \
+      "selp.b32 %0, 1, 0, pn;\n"                                                             \
+      "}\n"                                                                                  \
+      : "=r"(ok)                                                                             \
+      : "r"(next_bar), "r"(next_par), "r"(d), "l"(a0), "l"(b0), "r"(a_step), "r"(a_box),     \
+        "r"(b_step), "r"(e0), "r"(idesc), "r"(acc0), "r"(empty_bar), "h"(uint16_t(3))        \
+      : "memory")
+  if constexpr (kPair)
+    SP24_STAGE8_ASM("cta_group::2",
+                    "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
+                    "multicast::cluster.b64 [%12], %13;\n");
+  else
+    SP24_STAGE8_ASM("cta_group::1",
+                    "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+                    "[%12];\n");
+#undef SP24_STAGE8_ASM
   return ok != 0;
 }
 

@@ -14,7 +14,7 @@
 //           first and release it before they add C and store.
 //           Integer products (widened to bf16) use it too, summing f32 chunks into int32.
 //   pair 256 x 128 (16-bit operands with 32 < N <= 128): the same with 64-column halves
-//           of B and double-buffered 128-column accumulators.
+//           of B and 256-K stages (see Geo).
 //   single  (FP8 with 32 < N <= 128): one CTA per 128 x 128 tile, cta_group::1,
 //           accumulator double-buffered in TMEM so the epilogue of one tile overlaps the
 //           next.
@@ -76,7 +76,7 @@ struct MmaParams {
   int M, N, K;
   int mtiles, ntiles, num_kb;  // tiles of the variant (128 or 256 rows, 128 or 256 cols)
   int img_kb;                  // metadata image stages per 128-row tile (a stage of the
-                               // narrow 16-bit variant spans two)
+                               // narrow and 256 x 128 16-bit variants spans two)
   int band_rows;               // tile order: bands of this many rows of D, swept along N
   int batch;                   // problems of equal shape; problem b's C / D start at
   int64_t stride_c, stride_d;  // C + b * stride_c, D + b * stride_d (elements)
@@ -93,14 +93,16 @@ struct MmaParams {
 // 256 x 128 tiles and double-buffered accumulators (16-bit operands with 32 < N <= 128),
 // single (128 x 128 tiles: FP8 with 32 < N <= 128) and narrow (128 x 32 tiles for
 // N <= 32: B staged in 32-byte swizzle atoms, so a stage holds only the columns that
-// exist).  A narrow product moves little data per MMA, so its stages are as long as the
-// MMA thread's and the metadata writers' fixed cost per stage allows to hide: 16-bit
-// operands take two image stages (256 dense K, 8 MMAs, two boxes of A) per stage, and
-// three such stages fill the TMEM columns left for metadata slots.
+// exist).  The narrow and 256 x 128 products move little data per MMA, so their stages
+// are as long as the MMA thread's and the metadata writers' fixed cost per stage allows to
+// hide: 16-bit operands take two image stages (256 dense K, 8 MMAs, two boxes of A) per
+// stage, and three such stages fill the TMEM columns left for metadata slots (the 256 x 128
+// tiles then keep a single 128-column accumulator: measured faster than two accumulators
+// with 128-K stages, also on shapes with many tiles per CTA pair).
 template <int ESZ, bool kPair, bool kNarrow = false, bool kHalfN = false>
 struct Geo {
   static constexpr int kImgStageK = ESZ == 2 ? 128 : 256;    // dense K per image stage
-  static constexpr int kImgPer = (kNarrow && ESZ == 2) ? 2 : 1;  // image stages per stage
+  static constexpr int kImgPer = ((kNarrow || kHalfN) && ESZ == 2) ? 2 : 1;  // per stage
   static constexpr int kStageK = kImgStageK * kImgPer;        // dense K per stage
   static constexpr int kMmaK = ESZ == 2 ? 32 : 64;            // dense K per MMA
   static constexpr int kMmas = kStageK / kMmaK;               // 4 (narrow 16-bit: 8)
@@ -118,13 +120,13 @@ struct Geo {
   static constexpr int kAtoms = kBCols / kAtomN;
   static constexpr int kAtomBytes = kStageK * kAtomInner;     // one B box
   static constexpr int kBBytes = kAtoms * kAtomBytes;
-  static constexpr int kStages = kNarrow ? (kImgPer == 2 ? 3 : 7) : 4;
+  static constexpr int kStages = kImgPer == 2 ? 3 : (kNarrow ? 7 : 4);
   static constexpr int kStageBytes = kAStage + kBBytes;  // the metadata skips shared memory
   // CTA pairs: one 4 KiB staging box per epilogue warp (32 rows x 32 f32 columns) through
   // which the epilogue's C tiles arrive and its D tiles leave by TMA
   static constexpr int kStgBytes = kPair ? 8 * 4096 : 0;
   static constexpr int kSmemBytes = kStages * kStageBytes + kStgBytes + 1024;
-  static constexpr int kAccBufs = (kPair && !kHalfN) ? 1 : 2;
+  static constexpr int kAccBufs = (kPair && (!kHalfN || kImgPer == 2)) ? 1 : 2;
   static constexpr int kAccCols = kAccBufs * kTileN;
   static constexpr uint32_t kMetaCol = kAccCols;              // slot set s at + s * 64
   // warps: 0 TMA producer, 1 MMA issuer, 2-3 idle, then the epilogue warps, then four
@@ -678,7 +680,9 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
                                   (uint32_t(nbox * kABytes) + btx) * (kPair ? 2u : 1u));
           if constexpr (kPair) {
             const uint32_t fb = mapa(&full_bar[s], 0);
-            tma_load_3d_pair(sA + s * G::kAStage, mA, fb, kx, mt128 * 128, b);
+            for (int i = 0; i < nbox; ++i)
+              tma_load_3d_pair(sA + s * G::kAStage + i * kABytes, mA, fb, kx + i * (128 / ESZ),
+                               mt128 * 128, b);
 #pragma unroll
             for (int a = 0; a < G::kAtoms; ++a)
               if (a < pp.batoms)
@@ -759,8 +763,8 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
             // the whole stage in one sequence, testing the next stage's barrier meanwhile
             // (MMA j: A 32 bytes further along K, B kMmaK rows further, metadata slot j)
             const int qn = q + 1;
-            if constexpr (G::kMmas == 8)  // narrow 16-bit: two boxes of A, 8 MMAs
-              ready = mma_stage8_test_next(
+            if constexpr (G::kMmas == 8)  // 256-K stages: two boxes of A, 8 MMAs
+              ready = mma_stage8_test_next<kPair>(
                   smem_addr(&full_bar[qn % kStages]), uint32_t((qn / kStages) & 1), d_tmem,
                   smem_desc(a_saddr, adesc_hi), smem_desc(b_saddr, bdesc_hi), 32u / 16u,
                   uint32_t(kABytes / 16), uint32_t(G::kMmaK * G::kAtomInner / 16), e_tmem, id,
