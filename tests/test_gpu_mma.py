@@ -207,8 +207,9 @@ def test_gemm_gives_up_when_operands_never_arrive(ta, N):
 # ---- full-size workloads, compared on sampled rows --------------------------------------
 
 def test_full_size_bf16_4096():
+    # every element of the 4096^3 product against the oracle (about 20 s of oracle time)
     c = inputs.bf16_square()
-    run_case(c, mode="mask", rows=sample_rows(c["M"]))
+    run_case(c, mode="mask")
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
@@ -219,8 +220,10 @@ def test_full_size_fp8_8192(fmt):
 
 @pytest.mark.parametrize("N", [16, 128, 2048])
 def test_llm_layer(N):
+    # N = 16 and 128: every row; N = 2048: sampled rows
     c = inputs.llm_layer(N=N)
-    run_case(c, mode="magnitude", out_dtype=torch.bfloat16, rows=sample_rows(c["M"]))
+    run_case(c, mode="magnitude", out_dtype=torch.bfloat16,
+             rows=sample_rows(c["M"]) if N > 128 else None)
 
 
 # ---- 8-bit integers: exact, through the bf16 path with chunked int32 accumulation ----------
