@@ -11,7 +11,9 @@
 //           stages its own 128 rows of A and its own 128-column half of B and the even
 //           CTA issues the MMAs, so each loaded byte feeds twice the work.  The 256-column
 //           accumulator is single-buffered; eight epilogue warps drain it to registers
-//           first and release it before they add C and store.
+//           first and release it before they add C and store.  With 16-bit float
+//           operands, when the last round of tiles would leave more than half of the CTA
+//           pairs idle, those tiles run as two 256 x 128 halves each.
 //           Integer products (widened to bf16) use it too, summing f32 chunks into int32.
 //   pair 256 x 128 (16-bit operands with 32 < N <= 128): the same with 64-column halves
 //           of B and 256-K stages (see Geo).
@@ -86,6 +88,9 @@ struct MmaParams {
   int64_t ldi;                 // words, pitch ldi); then meta is unused
   int idx_vec;                 // index base 16-byte aligned and ldi % 4 == 0: 16-byte loads
   uint64_t limit_ns;
+  int units;            // work units of the launch: tiles, plus the split tiles' halves
+  int n_full;           // units below n_full are whole tiles; the rest are halves (N / 2)
+  uint32_t idesc_half;  // instruction descriptor of a half tile
   int diag_stall;  // self-test: the TMA producer issues nothing, so every wait gives up
 };
 
@@ -518,6 +523,19 @@ __device__ __forceinline__ int tile_problem(const GroupTable* gt, int t, int& lo
   }
 }
 
+// Unit u of a one-problem launch: the whole tile u below n_full; above, the halves of
+// the remaining tiles (half 0: the tile's first kTileN / 2 columns, half 1: the rest).
+__device__ __forceinline__ void unit_tile(const MmaParams& p, int u, int& t, int& hf) {
+  if (u < p.n_full) {
+    t = u;
+    hf = -1;
+  } else {
+    const int h = u - p.n_full;
+    t = p.n_full + (h >> 1);
+    hf = h & 1;
+  }
+}
+
 // The kernel parameters as one problem of a group sees them (the launch's own parameters
 // without a group table).
 template <bool kGrouped>
@@ -577,7 +595,10 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * G::kAStage;
   uint8_t* sStg = sB + kStages * G::kBBytes;  // 1024-byte aligned (stage sizes are)
-  const int ntiles_total = kGrouped ? gt->tile_start[gt->count] : p.mtiles * p.ntiles * p.batch;
+  const int ntiles_total = kGrouped ? gt->tile_start[gt->count] : p.units;
+  // CTA pairs with 16-bit float operands may split the tiles of the last, partial round
+  // into halves (host decision: n_full < units)
+  constexpr bool kHalves = kPair && !kHalfN && !kGrouped && ESZ == 2 && OUT != 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -632,8 +653,9 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
       // While the kernel before may still run, pull this CTA's first stages into L2.  L2
       // is where every write of that kernel lands, so a line fetched early is updated by
       // those writes; the loads below read it only after the wait.
-      int lt;
+      int lt, hf = -1;
       const int g = tile_problem<kGrouped>(gt, unit, lt);
+      if constexpr (kHalves) unit_tile(p, unit, lt, hf);
       MmaParams qg;
       problem_params<kGrouped>(p, gt, g, qg);
       const MmaParams& pp = kGrouped ? qg : p;
@@ -642,21 +664,24 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
       int b, mt, nt;
       batch_tile<G::kTileM>(pp, lt, b, mt, nt);
       const int mt128 = kPair ? mt * 2 + int(rank) : mt;
-      const int bcol = nt * G::kTileN + int(rank) * G::kBCols;
+      const int bcol = hf < 0 ? nt * G::kTileN + int(rank) * G::kBCols
+                              : nt * G::kTileN + hf * (G::kTileN / 2) + int(rank) * (G::kBCols / 2);
+      const int na = hf < 0 ? pp.batoms : G::kAtoms / 2;
       for (int kb = 0; kb < pp.num_kb && kb < kStages; ++kb) {
         const int kx = kb * (G::kStageK / 2);
         for (int i = 0; i < G::kABoxes; ++i)
           if (2 * (kx + i * (128 / ESZ)) < pp.K) tma_prefetch_3d(mA, kx + i * (128 / ESZ), mt128 * 128, b);
         for (int a = 0; a < G::kAtoms; ++a)
-          if (a < pp.batoms) tma_prefetch_3d(mB, bcol + a * G::kAtomN, kb * G::kStageK, b);
+          if (a < na) tma_prefetch_3d(mB, bcol + a * G::kAtomN, kb * G::kStageK, b);
       }
     }
     griddep_wait();
     if (lane == 0 && !p.diag_stall) {
       int q = 0;
       for (int t = unit; t < ntiles_total && !*abort; t += nunits) {
-        int lt;
+        int lt, hf = -1;
         const int g = tile_problem<kGrouped>(gt, t, lt);
+        if constexpr (kHalves) unit_tile(p, t, lt, hf);
         MmaParams qg;
         problem_params<kGrouped>(p, gt, g, qg);
         const MmaParams& pp = kGrouped ? qg : p;
@@ -665,8 +690,11 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
         int b, mt, nt;
         batch_tile<G::kTileM>(pp, lt, b, mt, nt);
         const int mt128 = kPair ? mt * 2 + int(rank) : mt;  // this CTA's 128-row tile
-        const int bcol = nt * G::kTileN + int(rank) * G::kBCols;
-        const uint32_t btx = uint32_t(pp.batoms * G::kAtomBytes);
+        // a half tile: each CTA stages half of its usual B columns (one atom)
+        const int bcol = hf < 0 ? nt * G::kTileN + int(rank) * G::kBCols
+                                : nt * G::kTileN + hf * (G::kTileN / 2) + int(rank) * (G::kBCols / 2);
+        const int na = hf < 0 ? pp.batoms : G::kAtoms / 2;
+        const uint32_t btx = uint32_t(na * G::kAtomBytes);
         for (int kb = 0; kb < pp.num_kb; ++kb, ++q) {
           const int s = q % kStages;
           if (!mbar_wait(&empty_bar[s], ((q / kStages) & 1) ^ 1u, abort, p.limit_ns)) break;
@@ -685,7 +713,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
                                mt128 * 128, b);
 #pragma unroll
             for (int a = 0; a < G::kAtoms; ++a)
-              if (a < pp.batoms)
+              if (a < na)
                 tma_load_3d_pair(sB + s * G::kBBytes + a * G::kAtomBytes, mB, fb,
                                  bcol + a * G::kAtomN, kb * G::kStageK, b);
           } else {
@@ -715,11 +743,12 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
       int q = 0, local = 0, chunk = 0;
       bool ready = false;  // stage q's full_bar phase is known to have completed
       for (int t = unit; t < ntiles_total && !*abort; t += nunits, ++local) {
-        int lt;
+        int lt, hf = -1;
         const int g = tile_problem<kGrouped>(gt, t, lt);
+        if constexpr (kHalves) unit_tile(p, t, lt, hf);
         const int num_kb = kGrouped ? gt->num_kb[g] : p.num_kb;
         const int kdense = kGrouped ? gt->K[g] : p.K;
-        const uint32_t id = kGrouped ? gt->idesc[g] : idesc;
+        const uint32_t id = kGrouped ? gt->idesc[g] : (hf < 0 ? idesc : p.idesc_half);
         bool ok = true;
         int abuf = 0;
         uint32_t d_tmem = tmem;
@@ -847,8 +876,10 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
     };
     auto seek = [&](Cursor& c, int t) {  // first stage of tile t or a later one
       for (c.t = t; c.t < ntiles_total; c.t += nunits) {
-        int lt;
+        int lt, hf = -1;
         const int g = tile_problem<kGrouped>(gt, c.t, lt);
+        if constexpr (kHalves) unit_tile(p, c.t, lt, hf);
+        (void)hf;
         MmaParams qg;
         problem_params<kGrouped>(p, gt, g, qg);
         const MmaParams& pp = kGrouped ? qg : p;
@@ -1024,8 +1055,9 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
     int local = 0, ichunk = 0;
     uint32_t stg_phase = 0;  // C tiles this warp has loaded into its staging box
     for (int t = unit; t < ntiles_total; t += nunits, ++local) {
-      int lt;
+      int lt, hf = -1;
       const int g = tile_problem<kGrouped>(gt, t, lt);
+      if constexpr (kHalves) unit_tile(p, t, lt, hf);
       MmaParams qg;
       problem_params<kGrouped>(p, gt, g, qg);
       const MmaParams& pp = kGrouped ? qg : p;
@@ -1140,16 +1172,19 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
         constexpr int kCols = G::kTileN / 2;  // 128 (256 x 256 tiles) or 64 (256 x 128)
         constexpr int kChunks = kCols / 32;
         const int half = ew >> 2;
+        // a half tile (N / 2 columns) gives each warp half as many columns
+        const int cols = hf < 0 ? kCols : kCols / 2;
+        const int nch = cols / 32;
         uint32_t r[kChunks][32];
 #pragma unroll
         for (int c = 0; c < kChunks; ++c)
-          tc_ld_32x32b_x32(lane_base + uint32_t(half * kCols + 32 * c), r[c]);
+          if (c < nch) tc_ld_32x32b_x32(lane_base + uint32_t(half * cols + 32 * c), r[c]);
         tc_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty_addr + uint32_t(abuf * sizeof(uint64_t)));
         const int row = mt * G::kTileM + int(rank) * 128 + quad * 32 + lane;
-        const int col0 = nt * G::kTileN + half * kCols;
+        const int col0 = nt * G::kTileN + (hf < 0 ? 0 : hf * (G::kTileN / 2)) + half * cols;
         // C is not pulled into L2 ahead of time: a tile's worth prefetched one main loop
         // early was partly evicted again before its use (measured on bf16 4096^3 with f32 C:
         // 176 instead of 134 MB read from DRAM per launch, and 5% slower)
@@ -1164,7 +1199,7 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
 #pragma unroll
           for (int c = 0; c < kChunks; ++c) {
             const int col = col0 + 32 * c;
-            if (col >= pp.N || row0w >= pp.M) break;
+            if (c >= nch || col >= pp.N || row0w >= pp.M) break;
             if (lane == 0) bulk_wait_read_all();  // the box's previous D has left
             __syncwarp();
             if (hasC) {
@@ -1195,7 +1230,8 @@ __device__ __forceinline__ void spmma_body(const CUtensorMap* tmA, const CUtenso
         } else if (row < pp.M) {
 #pragma unroll
           for (int c = 0; c < kChunks; ++c)
-            if (col0 + 32 * c < pp.N) store_row32<OUT>(r[c], pp, row, col0 + 32 * c, cofs, dofs);
+            if (c < nch && col0 + 32 * c < pp.N)
+              store_row32<OUT>(r[c], pp, row, col0 + 32 * c, cofs, dofs);
         }
       } else {
         const int row0 = mt * G::kTileM + quad * 32 + (lane >> 2);
@@ -1320,6 +1356,12 @@ struct BatchStrides {
   int64_t values, meta, b;
 };
 
+// The same instruction descriptor with half the MMA N (bits 17-22 hold N / 8).
+inline uint32_t idesc_half_n(uint32_t id) {
+  const uint32_t n = ((id >> 17) & 0x3Fu) << 3;
+  return (id & ~(0x3Fu << 17)) | ((((n / 2) >> 3) & 0x3Fu) << 17);
+}
+
 template <int ESZ, int OUT, bool kPair, bool kNarrow = false, bool kHalfN = false>
 int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const void* B,
         int64_t ldb, uint32_t idesc, int num_sms, cudaStream_t s, const BatchStrides& bs) {
@@ -1390,6 +1432,8 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const int tiles = p.mtiles * p.ntiles * p.batch;
+  p.units = tiles;
+  p.n_full = tiles;
   int units = num_sms;
   if (kPair) {
     cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
@@ -1402,6 +1446,17 @@ int run(MmaParams p, const void* values, int64_t ldv, const void* meta, const vo
     units = max_clusters;
   }
   if (tiles < units) units = tiles;
+  // 16-bit float products on 256 x 256 pair tiles: when the last round of tiles would
+  // leave more than half of the CTA pairs idle, its tiles run as two halves each (N / 2:
+  // one B atom per CTA, half the MMA N), so the round takes about half as long
+  if constexpr (kPair && !kHalfN && ESZ == 2 && OUT != 2) {
+    const int rem = tiles % units;
+    if (tiles > units && rem > 0 && 2 * rem <= units) {
+      p.n_full = tiles - rem;
+      p.units = p.n_full + 2 * rem;
+      p.idesc_half = idesc_half_n(idesc);
+    }
+  }
   cfg.gridDim = dim3(units * (kPair ? 2 : 1), 1, 1);
   if (cudaLaunchKernelEx(&cfg, kern, tA, tB, tC, tD, p, idesc, staged) != cudaSuccess) return 4;
   return cudaGetLastError() == cudaSuccess ? 0 : 4;

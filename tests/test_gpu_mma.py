@@ -534,3 +534,14 @@ def test_layers_chained_on_one_stream(N, graph):
     R2, S2 = oracle.mma_f64(vb, ib, inputs.bits(Y1.cpu()), inputs.bits(c2["C"]), "bf16", "bf16",
                             M1, tc="f32")
     check_float(Y2.cpu().numpy(), R2, S2, None, "layer 2")
+
+
+@pytest.mark.parametrize("ta,tc,out,M,N,K", [
+    ("bf16", "f32", torch.float32, 2500, 2296, 320),    # 90 tiles, ragged M, N and K
+    ("f16", "bf16", torch.bfloat16, 3000, 2104, 288),  # 108 tiles, ragged M, N and K
+])
+def test_more_tiles_than_cta_pairs(ta, tc, out, M, N, K):
+    # more 256 x 256 tiles than CTA pairs, with a last round that leaves pairs idle (its
+    # tiles may run as halves): every element against the oracle
+    c = inputs.case(ta, ta, M, N, K, seed=M + N, tc=tc)
+    run_case(c, mode="mask", out_dtype=out)
