@@ -387,3 +387,17 @@ class SparseMatrix:
     def matmul(self, B, C=None, out_dtype=None, status=None, stream=None):
         return mma(self.values, self.meta, B, C, out_dtype=out_dtype, status=status,
                    stream=stream)
+
+    def state_dict(self) -> dict:
+        """The compressed operand as plain tensors (for torch.save): the kept values, the
+        canonical index, the metadata image and the dense K.  A compressed weight is kept and
+        reloaded this way instead of being compressed again."""
+        return {"values": self.values, "index": self.index, "meta": self.meta,
+                "K": torch.tensor(self.K, dtype=torch.int64)}
+
+    @classmethod
+    def from_state_dict(cls, state: dict, device=None) -> "SparseMatrix":
+        """Rebuild from state_dict() (the tensors moved to `device` if one is given)."""
+        move = (lambda t: t.to(device)) if device is not None else (lambda t: t)
+        return cls(move(state["values"]), move(state["index"]), move(state["meta"]),
+                   int(state["K"]))

@@ -331,3 +331,20 @@ def test_gemm_give_up_self_test_validates_before_the_device():
     assert L.sp24_diag_mma_stall(BF16, *args, 2_000_000_000, FAKE, None) == INVALID
     assert L.sp24_diag_mma_stall(BF16, *args, 1000, None, None) == INVALID    # no status word
     assert L.sp24_diag_mma_stall(BF16, 256, 256, 100, *args[3:], 1000, FAKE, None) == INVALID
+
+
+def test_sparse_matrix_state_round_trip():
+    # a compressed operand saved with torch.save and loaded back is the same operand
+    import io
+    g = torch.Generator().manual_seed(3)
+    values = torch.randn(64, 96, generator=g).to(torch.bfloat16)
+    index = torch.randint(0, 2**31 - 1, (64, 6), generator=g, dtype=torch.int32)
+    meta = torch.randint(0, 256, (64 * 6 * 4,), generator=g, dtype=torch.uint8)
+    W = sp.SparseMatrix(values, index, meta, 192)
+    buf = io.BytesIO()
+    torch.save(W.state_dict(), buf)
+    buf.seek(0)
+    R = sp.SparseMatrix.from_state_dict(torch.load(buf))
+    assert R.shape == W.shape == (64, 192)
+    for a, b in ((R.values, values), (R.index, index), (R.meta, meta)):
+        assert a.dtype == b.dtype and torch.equal(a, b)
